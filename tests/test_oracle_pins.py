@@ -1,0 +1,509 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each group ties one oracle function to a library routine, a brute-force
+enumeration, a closed form, an invariant the pages state, or a value the
+pages print (fixtures under tests/golden). Chosen so that a plausible slip
+(a dropped envelope, a wrong sign, a missing 1/f, a transposed operand, a
+wrong tie-break, double rounding) fails at least one of them.
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from conftest import golden
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+def _bf16_bits_torch(x32):
+    return torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_decode_matches_torch():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 1 << 16, size=20000, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    got = O.decode_kdt(bits, "bf16")
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    assert np.array_equal(ref[~np.isnan(ref)], got[~np.isnan(got)])
+    ref16 = torch.from_numpy(bits.view(np.int16)).view(torch.float16).double().numpy()
+    got16 = O.decode_kdt(bits, "fp16")
+    m = ~np.isnan(ref16)
+    assert np.array_equal(ref16[m], got16[m])
+
+
+def test_round_bf16_matches_torch_float32_cast():
+    # float32 inputs are exact in float64, so one rounding from float64 equals
+    # torch's single rounding from float32 (round to nearest even).
+    rng = np.random.default_rng(2)
+    x = np.concatenate([
+        rng.standard_normal(50000).astype(np.float32),
+        (rng.standard_normal(5000) * 1e-38).astype(np.float32),     # subnormal range
+        (rng.standard_normal(5000) * 3e38).astype(np.float32),      # near overflow
+        np.array([0.0, -0.0, np.inf, -np.inf], dtype=np.float32),
+    ])
+    # exact ties: a bf16 value plus half its spacing
+    base = _bf16_bits_torch(rng.standard_normal(5000).astype(np.float32))
+    b64 = O.decode_kdt(base, "bf16")
+    ties = (b64 + 0.5 * O.ulp_kdt(b64, "bf16")).astype(np.float32)
+    x = np.concatenate([x, ties])
+    assert np.array_equal(O.encode_kdt(x.astype(np.float64), "bf16"), _bf16_bits_torch(x))
+
+
+def test_round_fp16_matches_numpy_direct_cast():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(50000) * s for s in (1.0, 1e-6, 3e4, 1e5)])
+    x = np.concatenate([x, [0.0, -0.0, 65504.0, 65520.0, 65519.99, 2.0 ** -25, 2.0 ** -24]])
+    ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(O.encode_kdt(x, "fp16"), ref)
+
+
+def test_round_once_not_twice():
+    # A float64 value just above a bf16 midpoint must round up; rounding to
+    # float32 first would land exactly on the midpoint and round to even (down).
+    one = 1.0
+    mid = one + 2.0 ** -8                 # midpoint between 1 and 1 + 2^-7
+    x = mid + 2.0 ** -40                  # above it, but collapses onto it in float32
+    assert float(np.float32(x)) == mid
+    assert O.round_to_kdt(x, "bf16") == one + 2.0 ** -7
+
+
+def test_bf16_facts_printed_on_vortex_page():
+    g = golden("vortex_h2o_constants.txt")
+    decay = float(g["default_decay"])
+    assert O.round_to_kdt(decay, "bf16") == decay == 1 - 2 ** -6
+    # the accumulator climbs to 8.0 from below, where the bf16 spacing is 2^-5
+    below8 = float(O.round_to_kdt(7.96875, "bf16"))
+    assert below8 < 8.0 and O.ulp_kdt(below8, "bf16") == float(g["bf16_ulp_near_8"])
+    inc = float(g["typical_increment"])
+    assert inc < 0.5 * float(g["bf16_ulp_near_8"])
+    assert O.round_to_kdt(below8 + inc, "bf16") == below8         # the increment is lost
+    assert O.round_to_kdt(8.0 + inc, "bf16") == 8.0
+    assert abs(O.default_scale(int(g["head_dim"])) - float(g["resolved_scale"])) < 5e-7
+    assert 1.0 / (1.0 - decay) == float(g["steady_state_mass"])
+
+
+# ---------------------------------------------------------------------------
+# A1 page statistics
+# ---------------------------------------------------------------------------
+def _exact_rne(fr: Fraction, p=8, emin=-126):
+    """Exact-rational round-to-nearest-even onto a binary grid (independent of numpy)."""
+    if fr == 0:
+        return 0.0
+    a = abs(fr)
+    E = math.floor(math.log2(a))
+    while Fraction(2) ** E > a:
+        E -= 1
+    while Fraction(2) ** (E + 1) <= a:
+        E += 1
+    E = max(E, emin)
+    quantum = Fraction(2) ** (E - (p - 1))
+    r = round(fr / quantum) * quantum      # Python rounds Fractions half to even
+    return float(r)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_page_stats_brute_force(dtype):
+    rng = np.random.default_rng(4)
+    p, emin = (8, -126) if dtype == "bf16" else (11, -14)
+    for f in (1, 2, 3, 7, 16):
+        k = O.decode_kdt(O.encode_kdt(rng.standard_normal((f, 24)) * 2.0, dtype), dtype)
+        mn, mx, me = O.page_stats(k, dtype)
+        for d in range(24):
+            col = [float(v) for v in k[:, d]]
+            assert mn[d] == min(col) and mx[d] == max(col)
+            exact = sum(Fraction(v) for v in col) / f
+            assert me[d] == _exact_rne(exact, p, emin)
+        if f == 1:
+            assert np.array_equal(mn, k[0]) and np.array_equal(mx, k[0]) and np.array_equal(me, k[0])
+
+
+def test_cache_meta_ignores_positions_past_length():
+    rng = np.random.default_rng(5)
+    bits = O.encode_kdt(rng.standard_normal((37, 2, 8)), "bf16")
+    poisoned = bits.copy()
+    poisoned[37 - 5:] = 0x7FC0                    # NaN past a shorter length
+    a = O.cache_meta(bits, 32, 16, "bf16")
+    b = O.cache_meta(poisoned, 32, 16, "bf16")
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    mn, mx, me = O.cache_meta(bits, 37, 16, "bf16")
+    assert mn.shape == (3, 2, 8)
+    tail = O.decode_kdt(bits[32:37], "bf16")
+    assert np.array_equal(mn[2], tail.min(0)) and np.array_equal(mx[2], tail.max(0))
+
+
+# ---------------------------------------------------------------------------
+# A2 page scores
+# ---------------------------------------------------------------------------
+def test_envelope_bounds_true_max_per_head_and_group():
+    rng = np.random.default_rng(6)
+    for _ in range(200):
+        f = int(rng.integers(1, 17))
+        G = int(rng.integers(1, 9))
+        k = rng.standard_normal((f, 16)) + rng.standard_normal(16)
+        q = rng.standard_normal((G, 16))                    # signed queries
+        mn, mx = k.min(0), k.max(0)
+        s = O.score_pages(mn[None], mx[None], np.zeros((1, 16)), q, 0.0, 1.0)[0]
+        true_max = (q @ k.T).max(1)                          # per head, brute force
+        per_head = np.array([O.score_pages(mn[None], mx[None], np.zeros((1, 16)), q[g:g + 1], 0.0, 1.0)[0]
+                             for g in range(G)])
+        assert np.all(per_head >= true_max - 1e-12)
+        assert s >= true_max.mean() - 1e-12
+        assert abs(s - per_head.mean()) < 1e-12
+
+
+def test_envelope_is_tight_for_single_token_and_equal_keys():
+    rng = np.random.default_rng(7)
+    for f in (1, 5):
+        row = rng.standard_normal(32)
+        k = np.repeat(row[None], f, 0)
+        q = rng.standard_normal((3, 32))
+        s = O.score_pages(k.min(0)[None], k.max(0)[None], np.zeros((1, 32)), q, 0.0, 1.0)[0]
+        assert abs(s - (q @ row).mean()) < 1e-12
+
+
+def test_average_term_is_mean_attention_logit():
+    # integer keys and f = 16: the page mean is exact in bf16, so
+    # q . mean(k) = (1/f) sum_j q . k_j exactly up to float64 rounding.
+    rng = np.random.default_rng(8)
+    k = rng.integers(-8, 9, size=(16, 32)).astype(np.float64)
+    q = rng.standard_normal((4, 32))
+    mn, mx, me = O.page_stats(k, "bf16")
+    s = O.score_pages(mn[None], mx[None], me[None], q, 1.0, 0.0)[0]
+    assert abs(s - (q @ k.T).mean()) < 1e-12
+
+
+def test_linearised_form_equals_plain_form():
+    # max(q*M, q*m) = q+ * M + q- * m when M >= m, so the group score equals
+    # sum_d [w_avg qbar_d mean_d + w_peak (P_d M_d + N_d m_d)].
+    rng = np.random.default_rng(9)
+    n, G, D = 50, 8, 64
+    k = rng.standard_normal((n, 16, D))
+    mn, mx, me = k.min(1), k.max(1), k.mean(1)
+    q = rng.standard_normal((G, D))
+    s = O.score_pages(mn, mx, me, q, 0.7, 0.3)
+    P, N, qb = np.maximum(q, 0).mean(0), np.minimum(q, 0).mean(0), q.mean(0)
+    lin = 0.7 * me @ qb + 0.3 * (mx @ P + mn @ N)
+    assert np.allclose(s, lin, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# A3 selection
+# ---------------------------------------------------------------------------
+def _brute_select(s, n, topk):
+    if n <= topk:
+        return list(range(n))
+    cand = list(range(n - 1))
+
+    def better(x, y):  # x ranks strictly before y
+        sx, sy = s[x], s[y]
+        nx, ny = math.isnan(sx), math.isnan(sy)
+        if nx != ny:
+            return ny
+        if not nx and sx != sy:          # -0.0 == 0.0 in Python
+            return sx > sy
+        return x < y
+
+    sols = []
+    for X in itertools.combinations(cand, topk - 1):
+        Xs = set(X)
+        if all(better(x, y) for x in Xs for y in cand if y not in Xs):
+            sols.append(sorted(X) + [n - 1])
+    assert len(sols) == 1
+    return sols[0]
+
+
+def test_select_brute_force_with_ties_zeros_nans():
+    rng = np.random.default_rng(10)
+    pool = np.array([0.0, -0.0, 1.0, 1.0, -1.0, np.nan, -np.inf, np.inf, 0.5, 0.5, 2.0])
+    for _ in range(300):
+        n = int(rng.integers(1, 10))
+        topk = int(rng.integers(1, 8))
+        s = rng.choice(pool, size=n)
+        got = O.select_pages(s, n, topk).tolist()
+        assert got == _brute_select(list(s), n, topk)
+
+
+def test_select_edges():
+    assert O.select_pages(np.zeros(0), 0, 4).tolist() == []
+    assert O.select_pages(np.array([5.0, 1.0, 3.0]), 3, 1).tolist() == [2]       # tail only
+    assert O.select_pages(np.array([5.0, 1.0, 3.0]), 3, 3).tolist() == [0, 1, 2]
+    assert O.select_pages(np.array([5.0, 1.0, 3.0, 9.0]), 4, 2).tolist() == [0, 3]
+    # the tail's own score is irrelevant
+    assert O.select_pages(np.array([1.0, 2.0, 3.0, -99.0]), 4, 2).tolist() == [2, 3]
+
+
+# ---------------------------------------------------------------------------
+# A4 attention and the LSE merge
+# ---------------------------------------------------------------------------
+def test_attention_matches_library_sdpa():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(11)
+    for G, n, D in ((1, 1, 8), (4, 37, 64), (8, 300, 128), (3, 17, 128)):
+        q, k, v = rng.standard_normal((G, D)), rng.standard_normal((n, D)), rng.standard_normal((n, D))
+        sc = D ** -0.5
+        o, lse, z = O.attention(q, k, v, sc)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q)[None, :, None, :], torch.from_numpy(k)[None, None].expand(1, G, n, D),
+            torch.from_numpy(v)[None, None].expand(1, G, n, D), scale=sc)[0, :, 0, :].numpy()
+        assert np.allclose(o, ref, rtol=0, atol=1e-12)
+        assert np.allclose(lse, logsumexp(sc * q @ k.T, axis=1), rtol=0, atol=1e-12)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(12)
+    q, k, v = rng.standard_normal((4, 16)), rng.standard_normal((1, 16)), rng.standard_normal((1, 16))
+    o, lse, _ = O.attention(q, k, v, 0.25)
+    assert np.array_equal(o, np.repeat(v, 4, 0))
+    assert np.allclose(lse, 0.25 * (q @ k[0]))
+    kk = np.repeat(k, 9, 0)
+    vv = rng.standard_normal((9, 16))
+    o, lse, _ = O.attention(q, kk, vv, 0.25)
+    assert np.allclose(o, np.repeat(vv.mean(0, keepdims=True), 4, 0), atol=1e-14)
+    assert np.allclose(lse, 0.25 * (q @ k[0]) + math.log(9))
+    o, lse, _ = O.attention(q, np.zeros((0, 16)), np.zeros((0, 16)), 0.25)
+    assert np.array_equal(o, np.zeros((4, 16))) and np.all(lse == -np.inf)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 16, 200])
+def test_chunked_merge_equals_single_shot(S):
+    rng = np.random.default_rng(13)
+    G, n, D = 8, 200, 64
+    q, k, v = rng.standard_normal((G, D)), rng.standard_normal((n, D)) * 2, rng.standard_normal((n, D))
+    full_o, full_lse, _ = O.attention(q, k, v, D ** -0.5)
+    bounds = np.linspace(0, n, S + 1).astype(int)
+    parts = [O.attention(q, k[a:b], v[a:b], D ** -0.5) for a, b in zip(bounds[:-1], bounds[1:])]
+    o, lse = O.merge_partials([p[0] for p in parts], [p[1] for p in parts])
+    assert np.allclose(o, full_o, atol=1e-12) and np.allclose(lse, full_lse, atol=1e-12)
+
+
+def test_merge_edge_cases_from_vllmcpp_construction():
+    g = golden("vllmcpp_merge_edge_cases.txt")
+    T, H, Dm = int(g["tokens"]), int(g["heads"]), int(g["dim"])
+    rng = np.random.default_rng(14)
+    p_out = rng.uniform(-1, 1, (T, H, Dm))
+    s_out = rng.uniform(-1, 1, (T, H, Dm))
+    i = np.arange(H * T).reshape(H, T)
+    p_lse = (i % 7) * 0.5 - 1.0
+    s_lse = (i % 5) * 0.25 + 0.125
+    expect = {}
+    for c in g["case"]:
+        parts = c.split()
+        t, h = int(parts[0]), int(parts[1])
+        kv = dict(x.split("=") for x in parts[2:])
+        if kv["prefix"] != "keep":
+            p_lse[h, t] = float(kv["prefix"].replace("+inf", "inf"))
+        if kv["suffix"] != "keep":
+            s_lse[h, t] = float(kv["suffix"].replace("+inf", "inf"))
+        expect[(t, h)] = kv["expect"]
+    for t in range(T):
+        for h in range(H):
+            o, lse = O.merge_partials(np.stack([p_out[t, h][None], s_out[t, h][None]]),
+                                      np.array([[p_lse[h, t]], [s_lse[h, t]]]))
+            e = expect.get((t, h))
+            if e == "suffix":
+                assert np.allclose(o[0], s_out[t, h], atol=1e-15) and lse[0] == s_lse[h, t]
+            elif e == "empty":
+                assert np.all(o == 0) and lse[0] == -np.inf
+            else:
+                # both finite: the merge weights are a softmax over the two lse
+                w = 1.0 / (1.0 + math.exp(s_lse[h, t] - p_lse[h, t]))
+                assert np.allclose(o[0], w * p_out[t, h] + (1 - w) * s_out[t, h], atol=1e-14)
+                assert abs(lse[0] - np.logaddexp(p_lse[h, t], s_lse[h, t])) < 1e-14
+
+
+def test_page_decode_all_pages_is_dense_attention():
+    # topk >= n_pages selects every page, so the unit equals dense attention
+    # over all L cached tokens (textbook routine).
+    rng = np.random.default_rng(15)
+    L, D, G, ps = 75, 64, 4, 16
+    kb = O.encode_kdt(rng.standard_normal((L, D)), "bf16")
+    vb = O.encode_kdt(rng.standard_normal((L, D)), "bf16")
+    qb = O.encode_kdt(rng.standard_normal((G, D)), "bf16")
+    r = O.page_decode_unit(kb, vb, L, qb, ps=ps, topk=100, w_avg=1, w_peak=0.25, dtype="bf16")
+    assert r["sel"].tolist() == list(range(5))
+    q, k, v = (O.decode_kdt(x, "bf16") for x in (qb, kb, vb))
+    ref = torch.softmax(torch.from_numpy(D ** -0.5 * q @ k.T), 1).numpy() @ v
+    assert np.allclose(r["out"], ref, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# paged addressing
+# ---------------------------------------------------------------------------
+def test_reverse_interleaved_table_matches_vllmcpp_construction():
+    from sa_synth import reverse_interleaved
+    want = np.loadtxt(__import__("os").path.join(
+        __import__("os").path.dirname(__file__), "golden", "vllmcpp_reverse_interleaved_3x8.txt"),
+        dtype=np.int64, comments="#")
+    assert np.array_equal(reverse_interleaved(3, 8, 24), want)
+
+
+@pytest.mark.parametrize("table", ["reverse", "shuffle", "contiguous"])
+def test_gather_through_any_table_recovers_logical_rows(table):
+    from sa_synth import reverse_interleaved, shuffled_table, contiguous_table
+    rng = np.random.default_rng(16)
+    B, H, D, ps, L = 3, 2, 8, 4, 30
+    maxp = 8
+    NB = B * maxp + 5
+    if table == "reverse":
+        bt = reverse_interleaved(B, maxp, NB)
+    elif table == "shuffle":
+        bt = shuffled_table(B, maxp, [maxp] * B, NB, rng)
+    else:
+        bt = contiguous_table(B, maxp)
+    seqs = rng.integers(0, 60000, size=(B, L, H, D)).astype(np.uint16)
+    pool = np.full((NB, H, ps, D), 0x7FC0, dtype=np.uint16)
+    for b in range(B):
+        for j in range(L):
+            pool[bt[b, j // ps], :, j % ps] = seqs[b, j]
+    for b in range(B):
+        for h in range(H):
+            rows = O.gather_rows(pool, bt[b], np.arange(L), h, ps)
+            assert np.array_equal(rows, seqs[b, :, h])
+
+
+# ---------------------------------------------------------------------------
+# A5 H2O accumulate
+# ---------------------------------------------------------------------------
+def test_probabilities_sum_to_one_and_decay_one_is_plain_sum():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(17)
+    z = rng.standard_normal((4, 50)) * 3
+    lse = logsumexp(z, axis=1)
+    hh0 = np.zeros(50)
+    p = O.h2o_fold(hh0, z, lse, 0.5)
+    assert abs(p.sum() - 1.0) < 1e-12
+    hh = rng.random(50)
+    assert np.array_equal(O.h2o_fold(hh, z, lse, 1.0), hh + p)
+
+
+def test_decayed_mass_closed_form():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(18)
+    for decay in (0.984375, 0.5, 1.0):
+        hh = np.zeros(40)
+        T = 300
+        for t in range(T):
+            z = rng.standard_normal((4, 40))
+            hh = O.h2o_fold(hh, z, logsumexp(z, axis=1), decay)
+        closed = T if decay == 1.0 else (1 - decay ** T) / (1 - decay)
+        assert abs(hh.sum() - closed) < 1e-9 * closed
+
+
+def _vortex_recurrence(decay, steps, probs):
+    hh = np.zeros(probs.shape[1])
+    exact = np.zeros(probs.shape[1])
+    d = float(O.round_to_kdt(decay, "bf16"))
+    for s in range(steps):
+        z = np.log(probs[s])[None]                    # log-probs as logits, lse = 0
+        hh = O.h2o_store(O.h2o_fold(hh, z, np.zeros(1), d))
+        exact = probs[s] + d * exact
+    return hh, exact
+
+
+def test_bf16_accumulator_tracks_exact_recurrence_as_the_vortex_check():
+    g = golden("vortex_h2o_constants.txt")
+    n, T = int(g["recurrence_tokens"]), int(g["recurrence_steps"])
+    rng = np.random.default_rng(19)
+    aff = rng.standard_normal(n) * float(g["recurrence_affinity_scale"])
+    logits = aff[None] + rng.standard_normal((T, n)) * float(g["recurrence_noise_scale"])
+    probs = np.exp(logits - logits.max(1, keepdims=True))
+    probs /= probs.sum(1, keepdims=True)
+    k = int(g["recurrence_topk"])
+    hh, ex = _vortex_recurrence(float(g["default_decay"]), T, probs)
+    rel = np.abs(hh - ex).max() / np.abs(ex).max()
+    assert rel < float(g["recurrence_rel_err_max"])
+    srt = np.sort(ex)[::-1]
+    gap, ulp = srt[k - 1] - srt[k], O.ulp_kdt(srt[k - 1], "bf16")
+    if gap > ulp:
+        assert set(np.argsort(-hh, kind="stable")[:k]) == set(np.argsort(-ex, kind="stable")[:k])
+    assert hh.max() < float(g["recurrence_max_bound"])
+    probs2 = probs.copy()
+    probs2[-1] = 1.0 / n
+    hh2, _ = _vortex_recurrence(float(g["default_decay"]), T, probs2)
+    assert np.abs(hh - hh2).max() > float(g["recurrence_response_min"])
+    # the undecayed bf16 sum freezes and fails the page's own bar
+    hh1, ex1 = _vortex_recurrence(1.0, T, probs)
+    assert np.abs(hh1 - ex1).max() / np.abs(ex1).max() >= float(g["oracle_final_rel_err_fail"])
+
+
+# ---------------------------------------------------------------------------
+# A5 H2O eviction
+# ---------------------------------------------------------------------------
+def _bulk_evict(hh, pos, budget, n_sink, grace):
+    """Independent characterisation: the m = |R| - budget smallest (score, position)
+    pairs among list indices [n_sink, |R| - grace) leave."""
+    n = len(pos)
+    m = max(0, n - budget)
+    elig = sorted(range(n_sink, n - grace), key=lambda j: (hh[j], pos[j]))
+    gone = set(elig[:m])
+    return [pos[j] for j in range(n) if j not in gone], sorted(pos[j] for j in gone)
+
+
+def test_evict_matches_bulk_characterisation_with_ties():
+    rng = np.random.default_rng(20)
+    for _ in range(300):
+        n = int(rng.integers(9, 60))
+        n_sink, grace = int(rng.integers(0, 4)), int(rng.integers(0, 5))
+        budget = int(rng.integers(n_sink + grace + 1, n + 3))
+        pos = np.sort(rng.choice(1000, size=n, replace=False))
+        hh = rng.choice([0.0, 0.25, 0.5, 0.5, 1.0, 0.125], size=n)
+        kept, kept_hh, ev = O.h2o_evict(hh, pos, budget, n_sink, grace)
+        bk, bev = _bulk_evict(list(hh), list(pos), budget, n_sink, grace)
+        assert kept.tolist() == bk and sorted(ev) == bev
+        assert len(kept) == min(n, budget)
+        assert np.all(np.diff(kept) > 0)
+        assert kept[:n_sink].tolist() == pos[:n_sink].tolist()       # sinks survive
+        if grace:
+            assert kept[-grace:].tolist() == pos[-grace:].tolist()   # grace survives
+        idx = {p: j for j, p in enumerate(pos)}
+        assert np.array_equal(kept_hh, hh[[idx[p] for p in kept]])  # untouched values identical
+
+
+def test_evict_rules_from_velox_evidence():
+    pos = np.arange(10)
+    hh = np.array([0.0, 0.0, 5, 4, 3, 2, 1, 0.5, 0.0, 0.0])
+    # budget + 1 -> exactly budget; sinks survive although they hold the minimum
+    kept, _, ev = O.h2o_evict(hh, pos, 9, 2, 0)
+    assert len(kept) == 9 and ev == [8]
+    # grace protects the newest even when they hold the lowest score
+    kept, _, ev = O.h2o_evict(hh, pos, 9, 2, 2)
+    assert ev == [7]
+    # n_sink = 0: everything is eligible
+    kept, _, ev = O.h2o_evict(hh, pos, 9, 0, 0)
+    assert ev == [0]
+    # tie -> lowest position
+    kept, _, ev = O.h2o_evict(np.array([1.0, 0.5, 0.5, 0.5]), np.array([3, 7, 9, 12]), 3, 0, 0)
+    assert ev == [7]
+    with pytest.raises(ValueError):
+        O.h2o_evict(np.zeros(5), np.arange(5), 3, 2, 2)
+
+
+def test_h2o_unit_step_mass_without_eviction():
+    # Each step injects probability mass 1 (new tokens enter at 0), so without
+    # eviction the float64 mass after T steps is (1 - decay^T) / (1 - decay).
+    g = golden("vortex_h2o_constants.txt")
+    decay = float(g["default_decay"])
+    rng = np.random.default_rng(21)
+    D, G, L0, T = 32, 4, 20, 120
+    K = O.encode_kdt(rng.standard_normal((L0 + T, D)), "bf16")
+    V = O.encode_kdt(rng.standard_normal((L0 + T, D)), "bf16")
+    pos = list(range(L0))
+    hh_exact = np.zeros(L0)
+    for t in range(T):
+        pos.append(L0 + t)
+        hh_exact = np.append(hh_exact, 0.0)
+        q = O.encode_kdt(rng.standard_normal((G, D)), "bf16")
+        r = O.h2o_unit_step(O.h2o_store(hh_exact), pos, K, V, q, dtype="bf16", decay=decay,
+                            budget=10 ** 6, n_sink=4, grace=16)
+        assert r["kept"].tolist() == pos and r["evicted"] == []
+        hh_exact = O.h2o_fold(hh_exact, r["logits"], r["lse"], decay)
+    closed = (1 - decay ** T) / (1 - decay)
+    assert abs(hh_exact.sum() - closed) < 1e-9
