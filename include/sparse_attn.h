@@ -1,0 +1,265 @@
+/*
+ * sparse_attn.h -- C ABI of the GB300 (sm_103a) page-selected sparse decode
+ * library (libsparse_attn / _sparse_attn.so).
+ *
+ * One decode step of page-selected sparse attention over a paged KV cache:
+ *   sa_append_kv      write new keys/values, refresh the written pages'
+ *                     element-wise key statistics, zero their H2O slots
+ *   sa_score_pages    score every page per KV head from the statistics
+ *   sa_select_topk    top-k pages per KV head, the tail page always kept
+ *   sa_sparse_decode  exact softmax attention over the selected pages only,
+ *                     split across pages, partials merged by log-sum-exp
+ *   sa_h2o_update     token-level (page_size 1) decayed heavy-hitter fold and
+ *                     sink/grace-protected eviction
+ *
+ * Sources (cited by page title and section):
+ *   [vortex]  "flow: add H2O sparse attention (page-level and token-level,
+ *             MHA + GQA)", vortex_torch pull request 6.
+ *   [velox]   "H2O -- Cumulative Attention-Mass Heavy-Hitter Oracle
+ *             Eviction", VeloxQuant-MLX docs.
+ *   [vllmcpp] "test_ops_mla_chunked_context.cpp", vllm.cpp tests.
+ *   [entmax]  "EntmaxKV" README.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Ownership: the caller owns every buffer. All array pointers are DEVICE
+ *   pointers (CUDA global memory of the current device) unless marked "host".
+ *   Struct arguments themselves are read on the host during the call and may
+ *   be freed when it returns. The library never allocates device memory;
+ *   scratch comes from a caller-provided workspace.
+ * Asynchrony: every call only enqueues work on `stream` (a cudaStream_t
+ *   passed as void*; NULL = the legacy default stream) and returns; nothing
+ *   synchronises. Results are visible in stream order.
+ * Host errors: arguments are validated before anything is launched; a
+ *   violation returns SA_ERR_INVALID_ARG / SA_ERR_UNSUPPORTED /
+ *   SA_ERR_WORKSPACE and launches nothing. A failed launch returns
+ *   SA_ERR_CUDA.
+ * Data errors: faults that only the data reveals (a block-table entry outside
+ *   [0, num_blocks), a page index outside the request, a full retained list)
+ *   never trap. The kernel sets sticky bits in the caller's int32 status word
+ *   `dev_status` (nullable: then not recorded), skips the bad unit's memory
+ *   access, and finishes; the caller reads the word when convenient.
+ * Layout: pools are [num_blocks, num_kv_heads, page_size, head_dim] (one
+ *   contiguous (block, head) tile), row-major; this differs from vLLM's
+ *   [2, num_blocks, page_size, H_kv, D] (cited by [entmax] "How it works")
+ *   only in the order of the middle axes. Logical page p of request b lives in
+ *   block block_table[b * bt_stride + p]; position j is page j / page_size,
+ *   slot j % page_size. Query head g' belongs to KV head g' / G with
+ *   G = num_q_heads / num_kv_heads.
+ * Supported: dtype bf16 or fp16; head_dim 64 or 128; page_size a power of two
+ *   in [1, 128]; G in [1, 16].
+ */
+#ifndef SPARSE_ATTN_H_
+#define SPARSE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sa_status {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1,   /* a null required pointer, a bad size or a broken constraint */
+  SA_ERR_UNSUPPORTED = 2,   /* a valid configuration this build does not implement */
+  SA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than sa_decode_workspace_size() */
+  SA_ERR_CUDA = 4           /* a CUDA launch or runtime call failed */
+} sa_status;
+
+typedef enum sa_dtype { SA_BF16 = 0, SA_FP16 = 1 } sa_dtype;
+
+/* Sticky bits of the device status word. */
+#define SA_DEV_BAD_BLOCK 1  /* block-table entry outside [0, num_blocks), or page index out of range */
+#define SA_DEV_OVERFLOW 2   /* table or retained-list capacity exceeded; the excess was dropped */
+#define SA_DEV_BAD_COUNT 4  /* a selection / retained count outside [0, stride] (clamped) */
+
+/* The paged cache: pools plus per-page statistics. */
+typedef struct sa_cache {
+  void* k;              /* [num_blocks, num_kv_heads, page_size, head_dim], dtype */
+  void* v;              /* same layout as k */
+  void* meta;           /* [num_blocks, num_kv_heads, 3, head_dim], dtype: rows (k_min, k_max,
+                           k_mean) of the page's valid tokens; may be NULL where no call needs it */
+  int32_t dtype;        /* sa_dtype */
+  int32_t num_blocks;
+  int32_t num_kv_heads;
+  int32_t page_size;
+  int32_t head_dim;
+} sa_cache;
+
+/* The batch: block table and lengths. */
+typedef struct sa_batch {
+  const int32_t* block_table;  /* [batch, bt_stride]: logical page -> physical block */
+  int32_t* seq_lens;           /* [batch]: cached tokens per request; advanced only by sa_append_kv */
+  int32_t batch;
+  int32_t bt_stride;           /* table row length = page capacity per request */
+} sa_batch;
+
+/*
+ * sa_append_kv -- append new tokens and refresh the statistics of every page
+ * they touch.
+ *
+ * [vortex] "Page-level variants" and "Token-level variants" point 2:
+ * k_min / k_max / k_mean are overwriting reductions recomputed over a written
+ * page, and hh_score of the written pages is reset to zero because a recycled
+ * pool page keeps stale contents. [entmax] "How it works" / "Quick start":
+ * the decode call appends k_new / v_new and refreshes per-page key statistics.
+ *
+ * Request b's new tokens are rows new_cu[b] .. new_cu[b+1]-1 of k_new / v_new
+ * ([T_total, num_kv_heads, head_dim], dtype) and go to positions
+ * seq_lens[b] .. seq_lens[b] + n_b - 1. For every page touched, each KV head's
+ * statistics are recomputed over the page's valid tokens only (old tokens read
+ * from the pool, stale slots past the new length never read): k_min and k_max
+ * exactly, k_mean as the float64 mean rounded once (to nearest even) to dtype.
+ * Written if cache->meta != NULL.
+ *   new_cu            [batch + 1] int32, device, non-decreasing, new_cu[0] = 0
+ *   max_new_per_req   host: an upper bound on any n_b (sizes the grid); n_b above
+ *                     it sets SA_DEV_OVERFLOW and the excess is dropped
+ *   hh                nullable bf16 [num_blocks * page_size, num_kv_heads]: the
+ *                     H2O score of token slot (block * page_size + slot); the
+ *                     slots written here are set to 0
+ *   ret_pos, ret_cnt  nullable (both or neither): token-level retained lists
+ *                     [batch, num_kv_heads, ret_cap] int32 positions, ascending,
+ *                     and their counts [batch, num_kv_heads]; the new positions
+ *                     are appended to every KV head's list
+ * Finally seq_lens[b] += n_b (and ret_cnt += n_b), after all reads of the old
+ * values. A position beyond bt_stride * page_size, or a list beyond ret_cap,
+ * sets SA_DEV_OVERFLOW and is dropped.
+ */
+sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, const void* k_new,
+                       const void* v_new, const int32_t* new_cu, int32_t max_new_per_req,
+                       void* hh, int32_t* ret_pos, int32_t* ret_cnt, int32_t ret_cap,
+                       int32_t* dev_status, void* stream);
+
+/*
+ * sa_score_pages -- score every cached page of every (request, KV head).
+ *
+ * [vortex] "Page-level variants": average relevance q . mean(k) and the peak
+ * relevance envelope bound sum_d max(q_d * max_d, q_d * min_d) >= max_k q . k
+ * (both envelopes, since q is signed), combined as w_avg * avg + w_peak * peak
+ * (the Add(alpha = w_avg, beta = w_peak) of the page); [entmax] "How it works"
+ * (scored from page statistics without touching the cached tokens). The G
+ * query heads of a KV head are reduced to one ranking by the mean of their
+ * scores; no softmax scale is applied.
+ *   q        [batch, num_q_heads, head_dim], dtype
+ *   scores   [batch, num_kv_heads, max_pages] float32; entry (b, h, p) is
+ *            written for p < ceil(seq_lens[b] / page_size), others untouched
+ *   max_pages  host: row length of scores, >= every request's page count
+ *            (else SA_DEV_OVERFLOW for that request)
+ * A page whose block id is out of range scores NaN and sets SA_DEV_BAD_BLOCK.
+ * Needs cache->meta. Arithmetic: float32, using the exact identity
+ * max(q*M, q*m) = max(q,0)*M + min(q,0)*m (M >= m) so the cost per page does
+ * not grow with G.
+ */
+sa_status sa_score_pages(const sa_cache* cache, const sa_batch* batch, const void* q,
+                         int32_t num_q_heads, float w_avg, float w_peak, float* scores,
+                         int32_t max_pages, int32_t* dev_status, void* stream);
+
+/*
+ * sa_select_topk -- top-k pages per (request, KV head), tail page forced.
+ *
+ * [entmax] "How it works", "Top-k": keep topk pages, the budget counting the
+ * always-attended tail page. With n = ceil(seq_lens[b] / page_size): if
+ * n <= topk every page is selected; otherwise page n-1 plus the topk-1 best of
+ * pages 0..n-2 by (score descending, page index ascending), -0 equal to +0,
+ * NaN after every number. Output indices ascending.
+ *   scores   [batch, num_kv_heads, max_pages] float32 (from sa_score_pages)
+ *   sel_idx  [batch, num_kv_heads, topk] int32; entries past sel_cnt untouched
+ *   sel_cnt  [batch, num_kv_heads] int32 = min(topk, n)
+ * Limits: max_pages <= 49152 (the candidate keys of one (request, KV head)
+ * are held in shared memory), else SA_ERR_UNSUPPORTED.
+ */
+sa_status sa_select_topk(const float* scores, int32_t max_pages, const sa_batch* batch,
+                         int32_t page_size, int32_t num_kv_heads, int32_t topk,
+                         int32_t* sel_idx, int32_t* sel_cnt, int32_t* dev_status,
+                         void* stream);
+
+/*
+ * sa_decode_workspace_size -- bytes of workspace sa_sparse_decode needs for
+ * these sizes (host function, no GPU access). The workspace holds the split
+ * partial states and one ticket counter per (request, KV head); it must be
+ * zero-filled once before its first use (sa_decode_workspace_init does this)
+ * and every call leaves the counters at zero again. Calls that share a
+ * workspace must be ordered on one stream.
+ */
+size_t sa_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads,
+                                int32_t head_dim, int32_t page_size, int32_t sel_stride);
+
+/* Zero-fill a decode workspace on `stream` (cudaMemsetAsync; allocates nothing). */
+sa_status sa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * sa_sparse_decode -- exact softmax attention of each query head over the
+ * valid tokens of its KV head's selected pages.
+ *
+ * [entmax] "How it works": only the selected pages are attended and the
+ * attention is exact over that selection. [vortex] "Token-level variants"
+ * point 1: the softmax scale defaults to head_dim ** -0.5. [vllmcpp] the
+ * chunked loop must equal single-shot attention: the selected tokens are split
+ * across CTAs, each emits a partial (o_s, lse_s) (lse_s = -inf when empty),
+ * and the partials are merged exactly: lse = log sum_s exp(lse_s),
+ * o = sum_s exp(lse_s - lse) o_s; no tokens at all gives o = 0, lse = -inf.
+ *   q          [batch, num_q_heads, head_dim], dtype
+ *   sel_idx    [batch, num_kv_heads, sel_stride] int32 logical page indices
+ *              (for page_size 1: token positions), sel_cnt [batch, num_kv_heads];
+ *              the selection may be in any order; entries are visited in order
+ *   scale      softmax scale; <= 0 selects head_dim ** -0.5
+ *   out        [batch, num_q_heads, head_dim], dtype
+ *   lse        nullable float32 [batch, num_q_heads], natural log
+ *   logits     nullable float32 [batch, num_q_heads, logits_stride]: the scaled
+ *              logit scale * q . k of selection token i = e * page_size + slot
+ *              (entry e, slot within the page); -inf for slots past the page's
+ *              fill; logits_stride >= sel_stride * page_size
+ *   workspace  see sa_decode_workspace_size
+ * Only the valid tokens of each selected page are read (the tail page's stale
+ * slots are zero-filled in shared memory, never loaded). Tensor cores
+ * (mma.sync bf16/fp16, float32 accumulate) compute q.K and P.V; softmax in
+ * float32. Selected pages whose block id is out of range are skipped with
+ * SA_DEV_BAD_BLOCK.
+ */
+sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* batch, const void* q,
+                           int32_t num_q_heads, const int32_t* sel_idx, const int32_t* sel_cnt,
+                           int32_t sel_stride, float scale, void* out, float* lse,
+                           float* logits, int32_t logits_stride, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * sa_h2o_update -- token-level H2O: fold this step's attention probabilities
+ * into the bf16 heavy-hitter scores and evict above budget (page_size 1).
+ *
+ * [vortex] "Token-level variants" points 1 and 3: the accumulated quantity is
+ * the softmax probability (not the logit), hh_score is bf16 and decays,
+ * out = 1 * attn + decay * old. [velox] "Parameters" and "How it works": the
+ * first n_sink retained tokens and the newest `grace` are never evicted;
+ * while more than `budget` tokens remain the lowest-scoring eligible one is
+ * removed (ties to the lowest position); afterwards at most `budget` remain.
+ * For every retained entry j of (b, h) (position ret_pos[b, h, j]):
+ *   p_bar_j = (1/G) sum_g exp(logits[b, h*G+g, j] - lse[b, h*G+g])   (float32)
+ *   hh[slot_j, h] = bf16(decay * hh[slot_j, h] + p_bar_j)   (float64 fma, one rounding)
+ * with slot_j = block_table[b, pos_j] (page_size 1); then the eviction, which
+ * compacts ret_pos in place (order kept) and sets ret_cnt.
+ *   logits, lse  from sa_sparse_decode over sel_idx = ret_pos, sel_cnt = ret_cnt
+ *   hh           bf16 [num_slots, num_kv_heads], num_slots = blocks of the pool
+ *   evicted      nullable int32 [batch, num_kv_heads, ret_cap]: evicted positions,
+ *                ascending; evicted_cnt nullable int32 [batch, num_kv_heads]
+ * Constraints: budget > n_sink + grace (as [velox] requires), 0 < decay <= 1,
+ * ret_cap <= 32768.
+ */
+sa_status sa_h2o_update(const sa_batch* batch, int32_t num_kv_heads, int32_t num_q_heads,
+                        const float* logits, int32_t logits_stride, const float* lse, void* hh,
+                        int32_t num_slots, int32_t* ret_pos, int32_t* ret_cnt, int32_t ret_cap,
+                        int32_t budget, int32_t n_sink, int32_t grace, float decay,
+                        int32_t* evicted, int32_t* evicted_cnt, int32_t* dev_status,
+                        void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* sa_status_string(sa_status status);
+
+/* Library version, e.g. "0.1.0" (static string). */
+const char* sa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_ATTN_H_ */

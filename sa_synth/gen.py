@@ -266,6 +266,12 @@ class Workload:
 
     def kv_new(self, t: int) -> Tuple[np.ndarray, np.ndarray]:
         """uint16 [B, H_kv, D] key and value appended at decode step t."""
+        cache = self.__dict__.setdefault("_kv_cache", {})
+        if t not in cache:
+            cache[t] = self._kv_new(t)
+        return cache[t]
+
+    def _kv_new(self, t: int) -> Tuple[np.ndarray, np.ndarray]:
         c = self.cfg
         k = np.random.default_rng([self._seed, 4, t]).standard_normal((c.B, c.H_kv, c.D), dtype=np.float32)
         v = np.random.default_rng([self._seed, 5, t]).standard_normal((c.B, c.H_kv, c.D), dtype=np.float32)
@@ -292,8 +298,8 @@ class Workload:
         rows = src[self.pre_cu[b]:self.pre_cu[b + 1]]
         if steps_done == 0:
             return rows
-        new = [self.kv_new(t)[which][b][None] for t in range(steps_done)]
-        return np.concatenate([rows] + new, 0)
+        new = np.stack([self.kv_new(t)[which][b] for t in range(steps_done)], 0)
+        return np.concatenate([rows, new], 0)
 
 
 def make_workload(cfg: Config, extra_steps: int = 0) -> Workload:

@@ -1,0 +1,178 @@
+"""Thin torch-tensor binding of the C ABI (include/sparse_attn.h).
+
+Argument marshalling only: every step runs in the native library's CUDA
+kernels. Functions keep the C names and argument order; tensors must be CUDA,
+contiguous and of the documented dtype; ``stream`` defaults to torch's current
+stream. A non-OK status raises :class:`SaError`.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import SaBatch, SaCache
+
+__all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKVCache",
+           "sa_append_kv", "sa_score_pages", "sa_select_topk", "sa_decode_workspace_size",
+           "sa_decode_workspace_init", "sa_sparse_decode", "sa_h2o_update", "sa_status_string",
+           "sa_version", "alloc_decode_workspace"]
+
+_DT = {torch.bfloat16: _lib.SA_BF16, torch.float16: _lib.SA_FP16}
+
+
+class SaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {sa_status_string(status)} ({status})")
+
+
+def _check(fn, st):
+    if st != 0:
+        raise SaError(fn, st)
+
+
+def _p(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return t.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_cache(k: torch.Tensor, v: torch.Tensor, meta: Optional[torch.Tensor]) -> SaCache:
+    """Struct view of pools [num_blocks, H_kv, page_size, D] and meta [num_blocks, H_kv, 3, D]."""
+    if k.dtype not in _DT or v.dtype != k.dtype or k.shape != v.shape or k.dim() != 4:
+        raise ValueError("k, v must be bf16/fp16 [num_blocks, H_kv, page_size, D] of equal shape")
+    nb, hkv, ps, d = k.shape
+    if meta is not None and (meta.dtype != k.dtype or tuple(meta.shape) != (nb, hkv, 3, d)):
+        raise ValueError("meta must be [num_blocks, H_kv, 3, D] in the pool dtype")
+    c = SaCache(_p(k, name="k"), _p(v, name="v"), _p(meta, name="meta"), _DT[k.dtype], nb, hkv,
+                ps, d)
+    c._keep = (k, v, meta)
+    return c
+
+
+def make_batch(block_table: torch.Tensor, seq_lens: torch.Tensor) -> SaBatch:
+    """Struct view of block_table [B, bt_stride] int32 and seq_lens [B] int32."""
+    if block_table.dim() != 2 or seq_lens.dim() != 1 or seq_lens.shape[0] != block_table.shape[0]:
+        raise ValueError("block_table [B, stride] and seq_lens [B] expected")
+    b = SaBatch(_p(block_table, torch.int32, "block_table"), _p(seq_lens, torch.int32, "seq_lens"),
+                block_table.shape[0], block_table.shape[1])
+    b._keep = (block_table, seq_lens)
+    return b
+
+
+class PagedKVCache:
+    """Device buffers of one paged cache (PyTorch allocates; kernels do the work)."""
+
+    def __init__(self, num_blocks, num_kv_heads, page_size, head_dim, dtype=torch.bfloat16,
+                 device="cuda", with_meta=True, with_hh=False):
+        shape = (num_blocks, num_kv_heads, page_size, head_dim)
+        self.k = torch.empty(shape, dtype=dtype, device=device)
+        self.v = torch.empty(shape, dtype=dtype, device=device)
+        self.meta = (torch.empty((num_blocks, num_kv_heads, 3, head_dim), dtype=dtype, device=device)
+                     if with_meta else None)
+        self.hh = (torch.zeros((num_blocks * page_size, num_kv_heads), dtype=torch.bfloat16,
+                               device=device) if with_hh else None)
+        self.struct = make_cache(self.k, self.v, self.meta)
+
+
+def sa_status_string(status: int) -> str:
+    return _lib.load().sa_status_string(int(status)).decode()
+
+
+def sa_version() -> str:
+    return _lib.load().sa_version().decode()
+
+
+def sa_append_kv(cache: SaCache, batch: SaBatch, k_new, v_new, new_cu, max_new_per_req: int,
+                 hh=None, ret_pos=None, ret_cnt=None, ret_cap: int = 0, dev_status=None,
+                 stream=None):
+    lib = _lib.load()
+    _check("sa_append_kv", lib.sa_append_kv(
+        ctypes.byref(cache), ctypes.byref(batch), _p(k_new, name="k_new"), _p(v_new, name="v_new"),
+        _p(new_cu, torch.int32, "new_cu"), int(max_new_per_req),
+        _p(hh, torch.bfloat16, "hh"), _p(ret_pos, torch.int32, "ret_pos"),
+        _p(ret_cnt, torch.int32, "ret_cnt"), int(ret_cap),
+        _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_score_pages(cache: SaCache, batch: SaBatch, q, num_q_heads: int, w_avg: float,
+                   w_peak: float, scores, max_pages: int, dev_status=None, stream=None):
+    lib = _lib.load()
+    _check("sa_score_pages", lib.sa_score_pages(
+        ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads),
+        float(w_avg), float(w_peak), _p(scores, torch.float32, "scores"), int(max_pages),
+        _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_select_topk(scores, max_pages: int, batch: SaBatch, page_size: int, num_kv_heads: int,
+                   topk: int, sel_idx, sel_cnt, dev_status=None, stream=None):
+    lib = _lib.load()
+    _check("sa_select_topk", lib.sa_select_topk(
+        _p(scores, torch.float32, "scores"), int(max_pages), ctypes.byref(batch), int(page_size),
+        int(num_kv_heads), int(topk), _p(sel_idx, torch.int32, "sel_idx"),
+        _p(sel_cnt, torch.int32, "sel_cnt"), _p(dev_status, torch.int32, "dev_status"),
+        _s(stream)))
+
+
+def sa_decode_workspace_size(batch: int, num_kv_heads: int, num_q_heads: int, head_dim: int,
+                             page_size: int, sel_stride: int) -> int:
+    return int(_lib.load().sa_decode_workspace_size(batch, num_kv_heads, num_q_heads, head_dim,
+                                                    page_size, sel_stride))
+
+
+def sa_decode_workspace_init(workspace, stream=None):
+    _check("sa_decode_workspace_init", _lib.load().sa_decode_workspace_init(
+        _p(workspace, name="workspace"), workspace.numel() * workspace.element_size(), _s(stream)))
+
+
+def alloc_decode_workspace(batch, num_kv_heads, num_q_heads, head_dim, page_size, sel_stride,
+                           device="cuda"):
+    """A zero-filled workspace tensor of the size sa_sparse_decode needs."""
+    n = max(256, sa_decode_workspace_size(batch, num_kv_heads, num_q_heads, head_dim, page_size,
+                                          sel_stride))
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def sa_sparse_decode(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_idx, sel_cnt,
+                     sel_stride: int, scale: float, out, lse=None, logits=None,
+                     logits_stride: int = 0, workspace=None, dev_status=None, stream=None):
+    lib = _lib.load()
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("sa_sparse_decode", lib.sa_sparse_decode(
+        ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads),
+        _p(sel_idx, torch.int32, "sel_idx"), _p(sel_cnt, torch.int32, "sel_cnt"), int(sel_stride),
+        float(scale), _p(out, name="out"), _p(lse, torch.float32, "lse"),
+        _p(logits, torch.float32, "logits"), int(logits_stride), _p(workspace, name="workspace"),
+        wbytes, _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_h2o_update(batch: SaBatch, num_kv_heads: int, num_q_heads: int, logits,
+                  logits_stride: int, lse, hh, num_slots: int, ret_pos, ret_cnt, ret_cap: int,
+                  budget: int, n_sink: int, grace: int, decay: float, evicted=None,
+                  evicted_cnt=None, dev_status=None, stream=None):
+    lib = _lib.load()
+    _check("sa_h2o_update", lib.sa_h2o_update(
+        ctypes.byref(batch), int(num_kv_heads), int(num_q_heads),
+        _p(logits, torch.float32, "logits"), int(logits_stride), _p(lse, torch.float32, "lse"),
+        _p(hh, torch.bfloat16, "hh"), int(num_slots), _p(ret_pos, torch.int32, "ret_pos"),
+        _p(ret_cnt, torch.int32, "ret_cnt"), int(ret_cap), int(budget), int(n_sink), int(grace),
+        float(decay), _p(evicted, torch.int32, "evicted"),
+        _p(evicted_cnt, torch.int32, "evicted_cnt"), _p(dev_status, torch.int32, "dev_status"),
+        _s(stream)))

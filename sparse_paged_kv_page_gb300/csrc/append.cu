@@ -1,0 +1,190 @@
+// sa_append_kv: write new keys / values into the paged pools and recompute
+// the element-wise statistics (k_min, k_max, k_mean) of every page touched.
+//
+// "flow: add H2O sparse attention" (vortex_torch PR 6), "Page-level variants"
+// and "Token-level variants" point 2: the statistics are overwriting
+// reductions over the written page, and the H2O score slots written in the
+// step are reset to zero because recycled pool pages keep stale contents.
+// "EntmaxKV" README, "How it works": per-page key statistics refreshed on
+// append.
+//
+// One CTA per (touched page, request). The CTA writes the page's new tokens
+// and recomputes its statistics in the same pass, taking new values from the
+// input rows and old values from the pool, so no other CTA's writes are read.
+// Slots past the page's new fill are stale and never touched. The mean is
+// summed in float64 (exact for bf16/fp16 keys of any practical range) and
+// rounded once to the cache dtype. A second one-block kernel advances the
+// lengths after every CTA has read the old ones.
+#include "common.cuh"
+#include "host.h"
+
+namespace sa {
+namespace {
+
+struct AppendArgs {
+  void* k;
+  void* v;
+  void* meta;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* new_cu;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  uint16_t* hh;
+  int32_t* ret_pos;
+  const int32_t* ret_cnt;
+  int32_t* status;
+  int H, D, ps, num_blocks, bt_stride, max_new, ret_cap;
+};
+
+constexpr int kAppendThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
+  using E = Elem<T>;
+  const int b = blockIdx.y;
+  const int i = blockIdx.x;
+  const int ps = a.ps, H = a.H, D = a.D;
+  const int L_old = a.seq_lens[b];
+  const int row0 = a.new_cu[b];
+  int n = a.new_cu[b + 1] - row0;
+  if (n > a.max_new) {
+    if (i == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
+    n = a.max_new;
+  }
+  const int64_t cap_tok = int64_t(a.bt_stride) * ps;
+  if (L_old < 0 || L_old > cap_tok) {
+    if (i == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
+    return;
+  }
+  if (L_old + int64_t(n) > cap_tok) {
+    if (i == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
+    n = int(cap_tok - L_old);
+  }
+  if (n <= 0) return;
+  const int L_new = L_old + n;
+  const int p = L_old / ps + i;
+  if (p > (L_new - 1) / ps) return;
+  const int blk = a.bt[int64_t(b) * a.bt_stride + p];
+  if (blk < 0 || blk >= a.num_blocks) {
+    if (threadIdx.x == 0) flag(a.status, SA_DEV_BAD_BLOCK);
+    return;
+  }
+  const int page_start = p * ps;
+  const int fill = min(ps, L_new - page_start);          // valid tokens after the append
+  const int s_new = max(0, L_old - page_start);          // first slot written here
+  const int DP = D / 2;
+  const uint32_t* kn = static_cast<const uint32_t*>(a.k_new);
+  const uint32_t* vn = static_cast<const uint32_t*>(a.v_new);
+  uint32_t* kp_all = static_cast<uint32_t*>(a.k);
+  uint32_t* vp_all = static_cast<uint32_t*>(a.v);
+
+  for (int idx = threadIdx.x; idx < H * DP; idx += kAppendThreads) {
+    const int h = idx / DP, dp = idx % DP;
+    const int64_t tile = (int64_t(blk) * H + h) * ps;    // first row of this (block, head)
+    float mn0 = INFINITY, mn1 = INFINITY, mx0 = -INFINITY, mx1 = -INFINITY;
+    double s0 = 0.0, s1 = 0.0;
+    for (int s = 0; s < fill; ++s) {
+      const int64_t dst = (tile + s) * DP + dp;
+      uint32_t u;
+      if (s >= s_new) {
+        const int64_t src = (int64_t(row0 + page_start + s - L_old) * H + h) * DP + dp;
+        u = kn[src];
+        kp_all[dst] = u;
+        vp_all[dst] = vn[src];
+      } else {
+        u = kp_all[dst];
+      }
+      const float x0 = E::lo(u), x1 = E::hi(u);
+      mn0 = fminf(mn0, x0); mn1 = fminf(mn1, x1);
+      mx0 = fmaxf(mx0, x0); mx1 = fmaxf(mx1, x1);
+      s0 += double(x0); s1 += double(x1);
+    }
+    if (a.meta) {
+      uint32_t* m = static_cast<uint32_t*>(a.meta) + (int64_t(blk) * H + h) * 3 * DP + dp;
+      const double inv = 1.0 / double(fill);
+      m[0] = E::pack(mn0, mn1);                          // exact: values are already dtype
+      m[DP] = E::pack(mx0, mx1);
+      const uint32_t me = uint32_t(E::from_f64(s0 * inv)) | (uint32_t(E::from_f64(s1 * inv)) << 16);
+      m[2 * DP] = me;
+    }
+  }
+  // H2O slots of the written tokens start at zero.
+  if (a.hh) {
+    for (int idx = threadIdx.x; idx < (fill - s_new) * H; idx += kAppendThreads) {
+      const int s = s_new + idx / H, h = idx % H;
+      a.hh[(int64_t(blk) * ps + s) * H + h] = 0;
+    }
+  }
+  // token-level retained lists: append the new positions, ascending
+  if (a.ret_pos) {
+    for (int idx = threadIdx.x; idx < (fill - s_new) * H; idx += kAppendThreads) {
+      const int s = s_new + idx / H, h = idx % H;
+      const int pos = page_start + s;
+      const int c = a.ret_cnt[b * H + h] + (pos - L_old);
+      if (c < 0 || c >= a.ret_cap) {
+        flag(a.status, SA_DEV_OVERFLOW);
+        continue;
+      }
+      a.ret_pos[(int64_t(b) * H + h) * a.ret_cap + c] = pos;
+    }
+  }
+}
+
+// Advances lengths (and retained counts) after the append kernel has read them.
+__global__ void advance_kernel(int32_t* seq_lens, const int32_t* new_cu, int32_t* ret_cnt, int B,
+                               int H, int max_new, int64_t cap_tok, int ret_cap) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int L = seq_lens[b];
+    if (L < 0 || L > cap_tok) continue;
+    int n = new_cu[b + 1] - new_cu[b];
+    n = max(0, min(n, max_new));
+    const int64_t Ln = min(int64_t(L) + n, cap_tok);
+    seq_lens[b] = int32_t(Ln);
+    if (ret_cnt) {
+      const int add = int(Ln - L);
+      for (int h = 0; h < H; ++h) {
+        const int c = ret_cnt[b * H + h] + add;
+        ret_cnt[b * H + h] = min(max(c, 0), ret_cap);
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace sa
+
+extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, const void* k_new,
+                                  const void* v_new, const int32_t* new_cu, int32_t max_new_per_req,
+                                  void* hh, int32_t* ret_pos, int32_t* ret_cnt, int32_t ret_cap,
+                                  int32_t* dev_status, void* stream) {
+  using namespace sa;
+  sa_status st = check_cache(cache, true, false);
+  if (st != SA_OK) return st;
+  if ((st = check_batch(batch)) != SA_OK) return st;
+  if (!k_new || !v_new || !new_cu || max_new_per_req < 0) return SA_ERR_INVALID_ARG;
+  if ((ret_pos == nullptr) != (ret_cnt == nullptr)) return SA_ERR_INVALID_ARG;
+  if (ret_pos && ret_cap <= 0) return SA_ERR_INVALID_ARG;
+  if (max_new_per_req == 0) return SA_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AppendArgs a;
+  a.k = cache->k; a.v = cache->v; a.meta = cache->meta;
+  a.k_new = k_new; a.v_new = v_new; a.new_cu = new_cu;
+  a.bt = batch->block_table; a.seq_lens = batch->seq_lens;
+  a.hh = static_cast<uint16_t*>(hh); a.ret_pos = ret_pos; a.ret_cnt = ret_cnt;
+  a.status = dev_status;
+  a.H = cache->num_kv_heads; a.D = cache->head_dim; a.ps = cache->page_size;
+  a.num_blocks = cache->num_blocks; a.bt_stride = batch->bt_stride;
+  a.max_new = max_new_per_req; a.ret_cap = ret_pos ? ret_cap : 0;
+  const int64_t pages = (int64_t(max_new_per_req) + a.ps - 1) / a.ps + 1;
+  if (pages > 0x7fffffff) return SA_ERR_INVALID_ARG;
+  dim3 grid(unsigned(pages), unsigned(batch->batch));
+  if (cache->dtype == SA_BF16)
+    append_kernel<__nv_bfloat16><<<grid, kAppendThreads, 0, s>>>(a);
+  else
+    append_kernel<__half><<<grid, kAppendThreads, 0, s>>>(a);
+  if ((st = launch_status()) != SA_OK) return st;
+  advance_kernel<<<1, 256, 0, s>>>(batch->seq_lens, new_cu, ret_cnt, batch->batch, a.H,
+                                   max_new_per_req, int64_t(batch->bt_stride) * a.ps, a.ret_cap);
+  return launch_status();
+}

@@ -1,0 +1,485 @@
+// sa_sparse_decode: exact softmax attention over the selected pages only,
+// split across CTAs, partials merged by their log-sum-exp.
+//
+// "EntmaxKV" README, "How it works": only the selected pages are attended and
+// the attention is exact over that selection. "flow: add H2O sparse
+// attention" (vortex_torch PR 6), "Token-level variants" point 1: softmax
+// scale head_dim ** -0.5 unless given. "test_ops_mla_chunked_context.cpp"
+// (vllm.cpp): chunked attention merged by log-sum-exp must equal single-shot
+// attention; an empty chunk carries lse = -inf.
+//
+// Work unit: a tile of 16 token rows of one (request, KV head) taken in
+// selection order (row i = entry i / page_size, slot i % page_size), so a
+// 16-token page is one tile and page_size 1 gathers 16 retained tokens.
+// Grid (nsplit, H_kv, B): CTA `split` of a unit takes an equal share of the
+// unit's tiles, counted on the device from sel_cnt. Its 4 warps take tiles
+// round robin, each with a private 3-stage cp.async ring (16-byte copies into
+// an XOR-swizzled tile so ldmatrix reads are bank-conflict free; rows past a
+// page's fill are zero-filled, never read). Per tile a warp computes
+// S = Q K^T with mma.sync m16n8k16 (rows = the G query heads, padded to 16;
+// columns = the 16 tokens), applies scale and mask, runs the online softmax in
+// float32 (exp2 domain), reuses P's accumulator registers as the A operand of
+// O += P V (second mma.sync), and at the end the 4 warps merge in shared
+// memory. Each CTA writes its partial (o_s, lse_s) to the workspace; the last
+// CTA of the unit to finish (atomic ticket) merges the partials exactly and
+// writes out / lse, then resets the ticket. No CTA waits on another.
+#include "common.cuh"
+#include "host.h"
+
+namespace sa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr int kMaxSplit = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct DecodeArgs {
+  const void* k;
+  const void* v;
+  const void* q;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  const int32_t* sel;
+  const int32_t* cnt;
+  void* out;
+  float* lse;
+  float* logits;
+  float* part_o;
+  float* part_lse;
+  int32_t* tickets;
+  int32_t* status;
+  int H_kv, H_q, G, ps, ps_shift, num_blocks, bt_stride, sel_stride, logits_stride, nsplit;
+  float scale, scale_log2;
+};
+
+template <int D>
+struct Tile {
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kBytes = 16 * kRowBytes;      // one 16-row K (or V) tile
+  static constexpr int kChunks = D / 8;              // 16-byte chunks per row
+  static constexpr int kRowsPerOp = 32 / kChunks;    // rows one warp-wide copy covers
+  static constexpr int kOps = 16 / kRowsPerOp;       // copies per lane per tile
+  static constexpr int kStageBytes = 2 * kBytes;     // K + V
+  static constexpr int kSmem = kWarps * kStages * kStageBytes;
+};
+
+// byte offset of (row, chunk) inside a swizzled tile
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return uint32_t(row * Tile<D>::kRowBytes + ((chunk ^ (row & 7)) << 4));
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
+  using E = Elem<T>;
+  using TL = Tile<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint32_t s_mask[kWarps][kStages];
+  __shared__ int s_last;
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = b * a.H_kv + h;
+  const int G = a.G, ps = a.ps, pss = a.ps_shift;
+  const int L = a.seq_lens[b];
+  int cnt = a.cnt[unit];
+  if (cnt < 0 || cnt > a.sel_stride) {
+    if (threadIdx.x == 0 && split == 0) flag(a.status, SA_DEV_BAD_COUNT);
+    cnt = cnt < 0 ? 0 : a.sel_stride;
+  }
+  const int n_rows = cnt << pss;
+  const int n_tiles = (n_rows + 15) >> 4;
+  const int per = (n_tiles + a.nsplit - 1) / a.nsplit;
+  const int t_begin = min(n_tiles, split * per), t_end = min(n_tiles, t_begin + per);
+  const int n_pages_req = L > 0 ? (L + ps - 1) >> pss : 0;
+  const int32_t* sel = a.sel + int64_t(unit) * a.sel_stride;
+  const int32_t* btb = a.bt + int64_t(b) * a.bt_stride;
+  const T* kbase = static_cast<const T*>(a.k);
+  const T* vbase = static_cast<const T*>(a.v);
+
+  // Q as the A operand (rows = query heads of this KV head, zero beyond G)
+  const int g = lane >> 2, tq = lane & 3;
+  uint32_t qa[D / 16][4];
+  {
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+        static_cast<const T*>(a.q) + (int64_t(b) * a.H_q + int64_t(h) * G) * D);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int c0 = (kk * 16 + 2 * tq) >> 1, c1 = c0 + 4;
+      qa[kk][0] = g < G ? qp[g * (D / 2) + c0] : 0u;
+      qa[kk][1] = g + 8 < G ? qp[(g + 8) * (D / 2) + c0] : 0u;
+      qa[kk][2] = g < G ? qp[g * (D / 2) + c1] : 0u;
+      qa[kk][3] = g + 8 < G ? qp[(g + 8) * (D / 2) + c1] : 0u;
+    }
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int x = 0; x < D / 8; ++x) o[x][0] = o[x][1] = o[x][2] = o[x][3] = 0.f;
+  float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+
+  uint8_t* wbuf = smem + warp * kStages * TL::kStageBytes;
+  const int nt = t_begin + warp < t_end ? (t_end - t_begin - warp + kWarps - 1) / kWarps : 0;
+
+  // Issue the copies of this warp's i-th tile into stage st.
+  auto issue = [&](int i, int st) {
+    const int t = t_begin + warp + i * kWarps;
+    int64_t off = 0;
+    bool valid = false;
+    if (lane < 16) {
+      const int j = (t << 4) + lane;
+      const int e = j >> pss, s = j & (ps - 1);
+      if (e < cnt) {
+        const int page = sel[e];
+        if (page < 0 || page >= n_pages_req || page >= a.bt_stride) {
+          flag(a.status, SA_DEV_BAD_BLOCK);
+        } else if (s < min(ps, L - (page << pss))) {
+          const int blk = btb[page];
+          if (blk < 0 || blk >= a.num_blocks) {
+            flag(a.status, SA_DEV_BAD_BLOCK);
+          } else {
+            valid = true;
+            off = ((int64_t(blk) * a.H_kv + h) * ps + s) * D;
+          }
+        }
+      }
+    }
+    const uint32_t vmask = __ballot_sync(kFull, valid) & 0xffffu;
+    if (lane == 0) s_mask[warp][st] = vmask;
+    const uint32_t sk = smem_u32(wbuf + st * TL::kStageBytes);
+    const uint32_t sv = sk + TL::kBytes;
+    const int chunk = lane % TL::kChunks;
+#pragma unroll
+    for (int r0 = 0; r0 < TL::kOps; ++r0) {
+      const int row = lane / TL::kChunks + r0 * TL::kRowsPerOp;
+      const int lo = __shfl_sync(kFull, int(uint64_t(off) & 0xffffffffu), row);
+      const int hi = __shfl_sync(kFull, int(uint64_t(off) >> 32), row);
+      const int64_t ro = int64_t((uint64_t(uint32_t(hi)) << 32) | uint32_t(lo));
+      const bool rv = (vmask >> row) & 1u;
+      const uint32_t d = swz<D>(row, chunk);
+      cp_async_16(sk + d, rv ? static_cast<const void*>(kbase + ro + chunk * 8) : a.k, rv ? 16 : 0);
+      cp_async_16(sv + d, rv ? static_cast<const void*>(vbase + ro + chunk * 8) : a.v, rv ? 16 : 0);
+    }
+  };
+
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) {
+    if (i < nt) issue(i, i);
+    cp_async_commit();
+  }
+  for (int i = 0; i < nt; ++i) {
+    const int nxt = i + kStages - 1;
+    if (nxt < nt) issue(nxt, nxt % kStages);
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const int st = i % kStages;
+    const int t = t_begin + warp + i * kWarps;
+    const uint32_t sk = smem_u32(wbuf + st * TL::kStageBytes);
+    const uint32_t sv = sk + TL::kBytes;
+    const uint32_t vmask = s_mask[warp][st];
+
+    // S = Q K^T   (c[ntile][.]: rows g / g+8, tokens ntile*8 + 2tq + {0,1})
+    float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int tok = (mi >> 1) * 8 + rr;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t r[4];
+        ldmatrix_x4(r, sk + swz<D>(tok, kk * 2 + (mi & 1)));
+        E::mma(c[0], qa[kk], r[0], r[1]);
+        E::mma(c[1], qa[kk], r[2], r[3]);
+      }
+    }
+    // scale, mask, logits, online softmax
+    float pmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt2 = 0; nt2 < 2; ++nt2) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = nt2 * 8 + 2 * tq + e;
+        const bool ok = (vmask >> tok) & 1u;
+        const int j = (t << 4) + tok;
+        if (a.logits && j < n_rows) {
+          float* lg = a.logits + (int64_t(b) * a.H_q + int64_t(h) * G) * a.logits_stride + j;
+          if (g < G) lg[int64_t(g) * a.logits_stride] = ok ? c[nt2][e] * a.scale : -INFINITY;
+          if (g + 8 < G) lg[int64_t(g + 8) * a.logits_stride] = ok ? c[nt2][2 + e] * a.scale : -INFINITY;
+        }
+        c[nt2][e] = ok ? c[nt2][e] * a.scale_log2 : -INFINITY;
+        c[nt2][2 + e] = ok ? c[nt2][2 + e] * a.scale_log2 : -INFINITY;
+        pmax[0] = fmaxf(pmax[0], c[nt2][e]);
+        pmax[1] = fmaxf(pmax[1], c[nt2][2 + e]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      pmax[r] = fmaxf(pmax[r], __shfl_xor_sync(kFull, pmax[r], 1));
+      pmax[r] = fmaxf(pmax[r], __shfl_xor_sync(kFull, pmax[r], 2));
+      const float m_new = fmaxf(m_r[r], pmax[r]);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(m_r[r] - m_use);
+      float rs = 0.f;
+#pragma unroll
+      for (int nt2 = 0; nt2 < 2; ++nt2) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float p = exp2f(c[nt2][2 * r + e] - m_use);
+          c[nt2][2 * r + e] = p;
+          rs += p;
+        }
+      }
+      l_r[r] = l_r[r] * alpha + rs;
+      m_r[r] = m_new;
+#pragma unroll
+      for (int x = 0; x < D / 8; ++x) { o[x][2 * r] *= alpha; o[x][2 * r + 1] *= alpha; }
+    }
+    // O += P V
+    const uint32_t pa[4] = {E::pack(c[0][0], c[0][1]), E::pack(c[0][2], c[0][3]),
+                            E::pack(c[1][0], c[1][1]), E::pack(c[1][2], c[1][3])};
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int tok = (mi & 1) * 8 + rr;
+#pragma unroll
+      for (int nd = 0; nd < D / 16; ++nd) {
+        uint32_t r[4];
+        ldmatrix_x4_trans(r, sv + swz<D>(tok, 2 * nd + (mi >> 1)));
+        E::mma(o[2 * nd], pa, r[0], r[1]);
+        E::mma(o[2 * nd + 1], pa, r[2], r[3]);
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l_r[r] += __shfl_xor_sync(kFull, l_r[r], 1);
+    l_r[r] += __shfl_xor_sync(kFull, l_r[r], 2);
+  }
+  __syncthreads();
+
+  // merge the 4 warps in shared memory (reusing the tile buffers)
+  float* wm = reinterpret_cast<float*>(smem);                 // [kWarps][16]
+  float* wl = wm + kWarps * 16;                                // [kWarps][16]
+  float* wo = wl + kWarps * 16;                                // [kWarps][G][D]
+  if (tq == 0) {
+    if (g < G) { wm[warp * 16 + g] = m_r[0]; wl[warp * 16 + g] = l_r[0]; }
+    if (g + 8 < G) { wm[warp * 16 + g + 8] = m_r[1]; wl[warp * 16 + g + 8] = l_r[1]; }
+  }
+#pragma unroll
+  for (int x = 0; x < D / 8; ++x) {
+    const int d = x * 8 + 2 * tq;
+    if (g < G) {
+      wo[(warp * G + g) * D + d] = o[x][0];
+      wo[(warp * G + g) * D + d + 1] = o[x][1];
+    }
+    if (g + 8 < G) {
+      wo[(warp * G + g + 8) * D + d] = o[x][2];
+      wo[(warp * G + g + 8) * D + d + 1] = o[x][3];
+    }
+  }
+  __syncthreads();
+  const bool single = a.nsplit == 1;
+  T* outp = static_cast<T*>(a.out) + (int64_t(b) * a.H_q + int64_t(h) * G) * D;
+  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+    const int row = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 16 + row]);
+    float acc = 0.f, tot = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = wm[w * 16 + row];
+        if (mw == -INFINITY) continue;
+        const float f = exp2f(mw - M);
+        acc += wo[(w * G + row) * D + d] * f;
+        tot += wl[w * 16 + row] * f;
+      }
+    }
+    const float os = tot > 0.f ? acc / tot : 0.f;
+    const float ls = tot > 0.f ? (M + log2f(tot)) * kLn2 : -INFINITY;
+    if (single) {
+      reinterpret_cast<uint16_t*>(outp)[row * D + d] = E::from_f(os);
+      if (a.lse && d == 0) a.lse[int64_t(b) * a.H_q + int64_t(h) * G + row] = ls;
+    } else {
+      const int64_t pi = (int64_t(unit) * a.nsplit + split) * G + row;
+      a.part_o[pi * D + d] = os;
+      if (d == 0) a.part_lse[pi] = ls;
+    }
+  }
+  if (single) return;
+
+  // last CTA of the unit merges the partials
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&a.tickets[unit], 1) == a.nsplit - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  float* wgt = reinterpret_cast<float*>(smem);                // [nsplit][G]
+  float* rmax = wgt + kMaxSplit * 16;                          // [G]
+  float* rtot = rmax + 16;                                     // [G]
+  const int64_t pbase = int64_t(unit) * a.nsplit * G;
+  for (int i = threadIdx.x; i < a.nsplit * G; i += kThreads) {
+    float v = __ldcg(a.part_lse + pbase + i);
+    if (isinf(v)) v = -INFINITY;
+    wgt[i] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int row = threadIdx.x;
+    float M = -INFINITY;
+    for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, wgt[s * G + row]);
+    rmax[row] = M;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < a.nsplit * G; i += kThreads) {
+    const float M = rmax[i % G];
+    const float v = wgt[i];
+    wgt[i] = (M == -INFINITY || v == -INFINITY) ? 0.f : expf(v - M);
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int row = threadIdx.x;
+    float t = 0.f;
+    for (int s = 0; s < a.nsplit; ++s) t += wgt[s * G + row];
+    rtot[row] = t;
+    if (a.lse)
+      a.lse[int64_t(b) * a.H_q + int64_t(h) * G + row] =
+          t > 0.f ? rmax[row] + logf(t) : -INFINITY;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+    const int row = idx / D, d = idx % D;
+    const float t = rtot[row];
+    float acc = 0.f;
+    if (t > 0.f) {
+      for (int s = 0; s < a.nsplit; ++s) {
+        const float w = wgt[s * G + row];
+        if (w != 0.f) acc += w * __ldcg(a.part_o + (pbase + int64_t(s) * G + row) * D + d);
+      }
+      acc /= t;
+    }
+    reinterpret_cast<uint16_t*>(outp)[row * D + d] = E::from_f(acc);
+  }
+  if (threadIdx.x == 0) a.tickets[unit] = 0;
+}
+
+int num_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!sms[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    sms[dev] = v;
+  }
+  return sms[dev];
+}
+
+// Splits per (request, KV head): enough CTAs for ~4 per SM, at most one per tile.
+int choose_nsplit(int units, int max_tiles, int sms) {
+  const int target = 4 * sms;
+  int s = (target + units - 1) / units;
+  if (s > max_tiles) s = max_tiles;
+  if (s > kMaxSplit) s = kMaxSplit;
+  return s < 1 ? 1 : s;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t tickets, part_lse, part_o, total;
+};
+
+WsLayout ws_layout(int units, int G, int D, int nsplit) {
+  WsLayout w;
+  w.tickets = 0;
+  w.part_lse = align256(size_t(units) * sizeof(int32_t));
+  w.part_o = w.part_lse + align256(size_t(units) * nsplit * G * sizeof(float));
+  w.total = w.part_o + align256(size_t(units) * nsplit * G * D * sizeof(float));
+  return w;
+}
+
+int g_dec_smem[4][64];
+
+template <typename T, int D>
+sa_status launch_decode(const DecodeArgs& a, dim3 grid, cudaStream_t s, int* cache) {
+  auto k = decode_kernel<T, D>;
+  if (!ensure_smem(k, Tile<D>::kSmem, cache)) return SA_ERR_CUDA;
+  k<<<grid, kThreads, Tile<D>::kSmem, s>>>(a);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace sa
+
+extern "C" size_t sa_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads,
+                                           int32_t head_dim, int32_t page_size, int32_t sel_stride) {
+  using namespace sa;
+  if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
+      sel_stride <= 0 || num_q_heads % num_kv_heads)
+    return 0;
+  const int units = batch * num_kv_heads;
+  const int64_t max_tiles = (int64_t(sel_stride) * page_size + 15) / 16;
+  const int ns = choose_nsplit(units, int(max_tiles > (1 << 30) ? (1 << 30) : max_tiles), num_sms());
+  return ws_layout(units, num_q_heads / num_kv_heads, head_dim, ns).total;
+}
+
+extern "C" sa_status sa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes == 0) return SA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
+}
+
+extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* batch, const void* q,
+                                      int32_t num_q_heads, const int32_t* sel_idx,
+                                      const int32_t* sel_cnt, int32_t sel_stride, float scale,
+                                      void* out, float* lse, float* logits, int32_t logits_stride,
+                                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream) {
+  using namespace sa;
+  sa_status st = check_cache(cache, true, false);
+  if (st != SA_OK) return st;
+  if ((st = check_batch(batch)) != SA_OK) return st;
+  if (!q || !sel_idx || !sel_cnt || !out || sel_stride <= 0) return SA_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
+  const int G = num_q_heads / cache->num_kv_heads;
+  if (G > 16) return SA_ERR_UNSUPPORTED;
+  const int64_t rows = int64_t(sel_stride) * cache->page_size;
+  if (rows > (int64_t(1) << 30)) return SA_ERR_UNSUPPORTED;
+  if (logits && logits_stride < rows) return SA_ERR_INVALID_ARG;
+  const int units = batch->batch * cache->num_kv_heads;
+  const int ns = choose_nsplit(units, int((rows + 15) / 16), num_sms());
+  const WsLayout w = ws_layout(units, G, cache->head_dim, ns);
+  if (ns > 1 && (!workspace || workspace_bytes < w.total)) return SA_ERR_WORKSPACE;
+  DecodeArgs a;
+  a.k = cache->k; a.v = cache->v; a.q = q; a.bt = batch->block_table; a.seq_lens = batch->seq_lens;
+  a.sel = sel_idx; a.cnt = sel_cnt; a.out = out; a.lse = lse; a.logits = logits;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.tickets = ns > 1 ? reinterpret_cast<int32_t*>(ws + w.tickets) : nullptr;
+  a.part_lse = ns > 1 ? reinterpret_cast<float*>(ws + w.part_lse) : nullptr;
+  a.part_o = ns > 1 ? reinterpret_cast<float*>(ws + w.part_o) : nullptr;
+  a.status = dev_status;
+  a.H_kv = cache->num_kv_heads; a.H_q = num_q_heads; a.G = G; a.ps = cache->page_size;
+  a.ps_shift = log2i(cache->page_size); a.num_blocks = cache->num_blocks;
+  a.bt_stride = batch->bt_stride; a.sel_stride = sel_stride;
+  a.logits_stride = logits ? logits_stride : 0; a.nsplit = ns;
+  a.scale = scale > 0.f ? scale : 1.0f / sqrtf(float(cache->head_dim));
+  a.scale_log2 = a.scale * kLog2e;
+  dim3 grid(unsigned(ns), unsigned(cache->num_kv_heads), unsigned(batch->batch));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf = cache->dtype == SA_BF16;
+  if (cache->head_dim == 128)
+    return bf ? launch_decode<__nv_bfloat16, 128>(a, grid, s, g_dec_smem[0])
+              : launch_decode<__half, 128>(a, grid, s, g_dec_smem[1]);
+  return bf ? launch_decode<__nv_bfloat16, 64>(a, grid, s, g_dec_smem[2])
+            : launch_decode<__half, 64>(a, grid, s, g_dec_smem[3]);
+}

@@ -1,0 +1,162 @@
+// sa_select_topk: the pages each (request, KV head) attends.
+//
+// "EntmaxKV" README, "How it works", "Top-k": keep topk pages, the budget
+// counting pages and including the always-attended tail page. With n pages:
+// n <= topk keeps all; otherwise the tail n-1 plus the topk-1 best of pages
+// 0..n-2 by (score descending, index ascending); -0 == +0; NaN ranks last.
+//
+// One 1024-thread CTA per (KV head, request). Scores become order-preserving
+// 32-bit keys in shared memory; a most-significant-digit radix select
+// (4 passes of 8 bits, early exit once a digit bin is taken whole) finds the
+// key K of the (topk-1)-th best candidate and how many candidates equal to K
+// to keep; those are the lowest-indexed ones. Two block-wide prefix sums in
+// page order then give each kept page its slot, so the output is ascending
+// without sorting and the result is deterministic.
+#include "common.cuh"
+#include "host.h"
+
+namespace sa {
+namespace {
+
+constexpr int kSelThreads = 1024;
+constexpr int kSelMaxPages = 49152;
+
+struct SelArgs {
+  const float* scores;
+  const int32_t* seq_lens;
+  int32_t* sel_idx;
+  int32_t* sel_cnt;
+  int32_t* status;
+  int H, ps, max_pages, topk;
+};
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
+  extern __shared__ uint32_t keys[];
+  __shared__ int hist[256];
+  __shared__ int scan_tmp[32];
+  __shared__ int s_digit, s_above;
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int unit = b * a.H + h;
+  const int L = a.seq_lens[b];
+  int n = L > 0 ? (L + a.ps - 1) / a.ps : 0;
+  if (n > a.max_pages) {
+    if (tid == 0) flag(a.status, SA_DEV_OVERFLOW);
+    n = a.max_pages;
+  }
+  int32_t* out = a.sel_idx + int64_t(unit) * a.topk;
+  if (n <= a.topk) {
+    for (int i = tid; i < n; i += kSelThreads) out[i] = i;
+    if (tid == 0) a.sel_cnt[unit] = n;
+    return;
+  }
+  const int kprime = a.topk - 1;                 // best candidates besides the tail
+  const int nc = n - 1;                          // candidates 0 .. n-2
+  if (kprime == 0) {
+    if (tid == 0) { out[0] = n - 1; a.sel_cnt[unit] = 1; }
+    return;
+  }
+  const float* sc = a.scores + int64_t(unit) * a.max_pages;
+  for (int i = tid; i < nc; i += kSelThreads) keys[i] = f32_key(sc[i]);
+
+  uint32_t prefix = 0, mask = 0;
+  int remaining = kprime;                        // still to take among keys matching prefix
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+    for (int i = tid; i < nc; i += kSelThreads) {
+      const uint32_t k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // lane l owns digits 255-8l .. 248-8l, scanned from the largest digit down
+      int c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { c[j] = hist[255 - 8 * tid - j]; sum += c[j]; }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (tid >= o) incl += y;
+      }
+      int run = incl - sum, found = -1, above = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (found < 0 && run < remaining && remaining <= run + c[j]) { found = 255 - 8 * tid - j; above = run; }
+        run += c[j];
+      }
+      const unsigned m = __ballot_sync(kFull, found >= 0);
+      const int src = m ? __ffs(m) - 1 : 0;
+      const int d = __shfl_sync(kFull, found, src), ab = __shfl_sync(kFull, above, src);
+      if (tid == 0) { s_digit = d; s_above = ab; }
+    }
+    __syncthreads();
+    const int d = s_digit;
+    remaining -= s_above;
+    prefix |= uint32_t(d) << shift;
+    mask |= 255u << shift;
+    const bool whole = hist[d] == remaining;
+    __syncthreads();                             // everyone has read hist before it is reset
+    if (whole) break;
+  }
+
+  // keep: (key & mask) > prefix, or == prefix among the first `remaining` in page order
+  const int per = (nc + kSelThreads - 1) / kSelThreads;
+  const int c0 = min(nc, tid * per), c1 = min(nc, c0 + per);
+  int eq_local = 0;
+  for (int i = c0; i < c1; ++i) eq_local += (keys[i] & mask) == prefix;
+  int total;
+  const int eq_before = block_exclusive_scan<kSelThreads>(eq_local, scan_tmp, &total);
+  int take_local = 0;
+  {
+    int e = eq_before;
+    for (int i = c0; i < c1; ++i) {
+      const uint32_t k = keys[i] & mask;
+      if (k > prefix) ++take_local;
+      else if (k == prefix) { take_local += e < remaining; ++e; }
+    }
+  }
+  const int take_before = block_exclusive_scan<kSelThreads>(take_local, scan_tmp, &total);
+  {
+    int e = eq_before, o = take_before;
+    for (int i = c0; i < c1; ++i) {
+      const uint32_t k = keys[i] & mask;
+      bool take = false;
+      if (k > prefix) take = true;
+      else if (k == prefix) { take = e < remaining; ++e; }
+      if (take && o < kprime) out[o++] = i;
+    }
+  }
+  if (tid == 0) {
+    out[kprime] = n - 1;                         // the tail is the largest index
+    a.sel_cnt[unit] = a.topk;
+  }
+}
+
+int g_sel_smem[64];
+
+}  // namespace
+}  // namespace sa
+
+extern "C" sa_status sa_select_topk(const float* scores, int32_t max_pages, const sa_batch* batch,
+                                    int32_t page_size, int32_t num_kv_heads, int32_t topk,
+                                    int32_t* sel_idx, int32_t* sel_cnt, int32_t* dev_status,
+                                    void* stream) {
+  using namespace sa;
+  sa_status st = check_batch(batch);
+  if (st != SA_OK) return st;
+  if (!scores || !sel_idx || !sel_cnt || max_pages <= 0 || num_kv_heads <= 0 || topk <= 0)
+    return SA_ERR_INVALID_ARG;
+  if (!is_pow2(page_size) || page_size > 128) return SA_ERR_UNSUPPORTED;
+  if (max_pages > kSelMaxPages) return SA_ERR_UNSUPPORTED;
+  SelArgs a;
+  a.scores = scores; a.seq_lens = batch->seq_lens; a.sel_idx = sel_idx; a.sel_cnt = sel_cnt;
+  a.status = dev_status; a.H = num_kv_heads; a.ps = page_size; a.max_pages = max_pages;
+  a.topk = topk;
+  const int smem = max_pages * int(sizeof(uint32_t));
+  if (smem > 48 * 1024 && !ensure_smem(select_kernel, smem, g_sel_smem)) return SA_ERR_CUDA;
+  dim3 grid(unsigned(num_kv_heads), unsigned(batch->batch));
+  select_kernel<<<grid, kSelThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
+  return launch_status();
+}

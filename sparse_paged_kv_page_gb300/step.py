@@ -1,0 +1,136 @@
+"""Decode-step driver: device buffers plus the per-step chain of C-ABI calls.
+
+Page level (page_size > 1):  append -> score -> select -> sparse decode.
+Token level (page_size 1):   append (+ retained list) -> sparse decode over
+                             the retained tokens (logits + lse) -> H2O update.
+
+PyTorch only allocates the buffers and supplies the stream; every step runs in
+the native kernels. ``capture()`` records one step into a CUDA graph whose
+replay needs only the persistent input buffers ``q_buf`` / ``k_buf`` /
+``v_buf`` to be refreshed.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from .api import (PagedKVCache, alloc_decode_workspace, make_batch, sa_append_kv,
+                  sa_h2o_update, sa_score_pages, sa_select_topk, sa_sparse_decode)
+
+
+class SparseDecoder:
+    def __init__(self, *, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 page_size: int, num_blocks: int, bt_stride: int, dtype=torch.bfloat16,
+                 topk: int = 0, w_avg: float = 1.0, w_peak: float = 0.25, scale: float = 0.0,
+                 budget: int = 0, n_sink: int = 0, grace: int = 0, decay: float = 1.0,
+                 ret_cap: int = 0, device="cuda"):
+        self.B, self.H_q, self.H_kv, self.D = batch, num_q_heads, num_kv_heads, head_dim
+        self.ps, self.dtype, self.device = page_size, dtype, torch.device(device)
+        self.token_level = page_size == 1 and ret_cap > 0
+        self.topk, self.w_avg, self.w_peak, self.scale = topk, w_avg, w_peak, scale
+        self.budget, self.n_sink, self.grace, self.decay = budget, n_sink, grace, decay
+        self.cache = PagedKVCache(num_blocks, num_kv_heads, page_size, head_dim, dtype, device,
+                                  with_meta=not self.token_level, with_hh=self.token_level)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.block_table = torch.zeros((batch, bt_stride), **i32)
+        self.seq_lens = torch.zeros((batch,), **i32)
+        self.batch = make_batch(self.block_table, self.seq_lens)
+        self.bt_stride = bt_stride
+        self.max_pages = bt_stride
+        if self.token_level:
+            self.ret_cap = ret_cap
+            self.ret_pos = torch.zeros((batch, num_kv_heads, ret_cap), **i32)
+            self.ret_cnt = torch.zeros((batch, num_kv_heads), **i32)
+            self.logits = torch.empty((batch, num_q_heads, ret_cap), dtype=torch.float32,
+                                      device=device)
+            self.evicted = torch.zeros((batch, num_kv_heads, ret_cap), **i32)
+            self.evicted_cnt = torch.zeros((batch, num_kv_heads), **i32)
+            self.sel_stride = ret_cap
+        else:
+            if topk <= 0:
+                raise ValueError("page-level decoding needs topk >= 1")
+            self.scores = torch.empty((batch, num_kv_heads, bt_stride), dtype=torch.float32,
+                                      device=device)
+            self.sel_idx = torch.zeros((batch, num_kv_heads, topk), **i32)
+            self.sel_cnt = torch.zeros((batch, num_kv_heads), **i32)
+            self.sel_stride = topk
+        self.out = torch.empty((batch, num_q_heads, head_dim), dtype=dtype, device=device)
+        self.lse = torch.empty((batch, num_q_heads), dtype=torch.float32, device=device)
+        self.workspace = alloc_decode_workspace(batch, num_kv_heads, num_q_heads, head_dim,
+                                                page_size, self.sel_stride, device)
+        self.dev_status = torch.zeros((1,), **i32)
+        self.decode_cu = torch.arange(batch + 1, **i32)
+        self.q_buf = torch.zeros((batch, num_q_heads, head_dim), dtype=dtype, device=device)
+        self.k_buf = torch.zeros((batch, num_kv_heads, head_dim), dtype=dtype, device=device)
+        self.v_buf = torch.zeros((batch, num_kv_heads, head_dim), dtype=dtype, device=device)
+        self.graph = None
+
+    # ------------------------------------------------------------------
+    def set_block_table(self, bt: torch.Tensor):
+        self.block_table.copy_(bt.to(device=self.device, dtype=torch.int32))
+
+    def prefill(self, k: torch.Tensor, v: torch.Tensor, lens: Sequence[int]):
+        """Append lens[b] tokens per request: k, v [sum(lens), H_kv, D] in request order."""
+        cu = [0]
+        for n in lens:
+            cu.append(cu[-1] + int(n))
+        new_cu = torch.tensor(cu, dtype=torch.int32, device=self.device)
+        self._append(k, v, new_cu, max(int(n) for n in lens))
+
+    def _append(self, k, v, new_cu, max_new):
+        if self.token_level:
+            sa_append_kv(self.cache.struct, self.batch, k, v, new_cu, max_new, hh=self.cache.hh,
+                         ret_pos=self.ret_pos, ret_cnt=self.ret_cnt, ret_cap=self.ret_cap,
+                         dev_status=self.dev_status)
+        else:
+            sa_append_kv(self.cache.struct, self.batch, k, v, new_cu, max_new,
+                         hh=self.cache.hh, dev_status=self.dev_status)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor):
+        """One new token per request: k_new, v_new [B, H_kv, D]."""
+        self._append(k_new, v_new, self.decode_cu, 1)
+
+    def attend(self, q: torch.Tensor):
+        """Attention of q [B, H_q, D] over the current cache (no append)."""
+        if self.token_level:
+            sa_sparse_decode(self.cache.struct, self.batch, q, self.H_q, self.ret_pos, self.ret_cnt,
+                             self.ret_cap, self.scale, self.out, lse=self.lse, logits=self.logits,
+                             logits_stride=self.ret_cap, workspace=self.workspace,
+                             dev_status=self.dev_status)
+            sa_h2o_update(self.batch, self.H_kv, self.H_q, self.logits, self.ret_cap, self.lse,
+                          self.cache.hh, self.cache.hh.shape[0], self.ret_pos, self.ret_cnt,
+                          self.ret_cap, self.budget, self.n_sink, self.grace, self.decay,
+                          evicted=self.evicted, evicted_cnt=self.evicted_cnt,
+                          dev_status=self.dev_status)
+        else:
+            sa_score_pages(self.cache.struct, self.batch, q, self.H_q, self.w_avg, self.w_peak,
+                           self.scores, self.max_pages, dev_status=self.dev_status)
+            sa_select_topk(self.scores, self.max_pages, self.batch, self.ps, self.H_kv, self.topk,
+                           self.sel_idx, self.sel_cnt, dev_status=self.dev_status)
+            sa_sparse_decode(self.cache.struct, self.batch, q, self.H_q, self.sel_idx,
+                             self.sel_cnt, self.topk, self.scale, self.out, lse=self.lse,
+                             workspace=self.workspace, dev_status=self.dev_status)
+        return self.out
+
+    def step(self, q: torch.Tensor, k_new: Optional[torch.Tensor] = None,
+             v_new: Optional[torch.Tensor] = None):
+        if k_new is not None:
+            self.append(k_new, v_new)
+        return self.attend(q)
+
+    # ------------------------------------------------------------------
+    def capture(self, append: bool = True):
+        """Record one step (reading q_buf / k_buf / v_buf) into a CUDA graph."""
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self.step(self.q_buf, self.k_buf if append else None, self.v_buf if append else None)
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+        return self.out

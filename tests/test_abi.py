@@ -1,0 +1,55 @@
+"""CPU checks of the native library: it loads and exports every entry point the
+public header declares, with matching binding signatures. No compute call is
+made (there may be no GPU)."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "sparse_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sa_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_paged_kv_page_gb300 import build as B
+    B.build()
+    from sparse_paged_kv_page_gb300 import _lib
+    return _lib.load()
+
+
+def test_header_declares_the_five_steps():
+    names = _declared()
+    for n in ("sa_append_kv", "sa_score_pages", "sa_select_topk", "sa_sparse_decode",
+              "sa_h2o_update"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    from sparse_paged_kv_page_gb300 import _lib
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, name
+
+
+def test_host_only_calls(lib):
+    import sparse_paged_kv_page_gb300 as S
+    assert S.sa_version() == "0.1.0"
+    assert S.sa_status_string(0) == "SA_OK" and S.sa_status_string(3) == "SA_ERR_WORKSPACE"
+    assert S.sa_decode_workspace_size(0, 8, 64, 128, 16, 256) == 0
+    assert S.sa_decode_workspace_size(4, 8, 64, 128, 16, 256) > 4 * 8 * 4
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "sparse_paged_kv_page_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", txt, re.M), f
+                assert "sa_synth" not in txt, f

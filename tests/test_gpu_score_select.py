@@ -1,0 +1,134 @@
+"""sa_score_pages and sa_select_topk on the GPU against the oracle.
+
+Scores: within 1e-4 of the oracle's float64 plain-form scores, norm-wise.
+Selection: bit-exact against the oracle's selector applied to the same
+generator-drawn float32 scores (ties, signed zeros, NaN, -inf included); in the
+chained path the GPU's selection must be a valid top-k for scores within the
+float32 error bound of the oracle's.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from sa_synth import config, make_workload
+from gpu_util import (make_decoder, step_inputs, dev_status, host_bits, score_norm, assert_scores,
+                      score_error_bound, assert_selection_valid)
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_scores(wl, b, h, steps_done, q_bits):
+    c = wl.cfg
+    L = wl.seq_len(b, steps_done)
+    mn, mx, me = O.head_meta(wl.k_seq(b, steps_done)[:, h, :], L, c.ps, c.dtype)
+    q = O.decode_kdt(q_bits[h * c.G:(h + 1) * c.G], c.dtype)
+    S = O.score_pages(mn, mx, me, q, c.w_avg, c.w_peak)
+    return S, score_norm(mn, mx, me, q, c.w_avg, c.w_peak), L
+
+
+def _run_scores(dec, wl, t):
+    q, _, _ = step_inputs(wl, t)
+    from sparse_paged_kv_page_gb300 import sa_score_pages, sa_select_topk
+    sa_score_pages(dec.cache.struct, dec.batch, q, wl.cfg.H_q, wl.cfg.w_avg, wl.cfg.w_peak,
+                   dec.scores, dec.max_pages, dev_status=dec.dev_status)
+    sa_select_topk(dec.scores, dec.max_pages, dec.batch, wl.cfg.ps, wl.cfg.H_kv, wl.cfg.topk,
+                   dec.sel_idx, dec.sel_cnt, dev_status=dec.dev_status)
+    torch.cuda.synchronize()
+    return wl.q(t)
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3, 5])
+def test_scores_and_selection_small_configs(cid):
+    wl = make_workload(config(cid, small=True))
+    dec = make_decoder(wl)
+    qb = _run_scores(dec, wl, 0)
+    scores = dec.scores.cpu().numpy()
+    sel = dec.sel_idx.cpu().numpy()
+    cnt = dec.sel_cnt.cpu().numpy()
+    c = wl.cfg
+    for b in range(c.B):
+        for h in range(c.H_kv):
+            S, A, L = _oracle_scores(wl, b, h, 0, qb[b])
+            n = O.num_pages(L, c.ps)
+            assert_scores(scores[b, h, :n], S, A)
+            assert cnt[b, h] == min(c.topk, n)
+            eps = score_error_bound(A, c.D, c.G)
+            assert_selection_valid(sel[b, h, :cnt[b, h]], S, eps, n, c.topk)
+    assert dev_status(dec) == 0
+
+
+@pytest.mark.parametrize("G", [1, 3, 4, 7, 8, 16])
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "fp16")])
+def test_scores_group_sizes(G, D, dtype):
+    cfg = config(3, small=True).replace(H_q=2 * G, H_kv=2, D=D, dtype=dtype, len_range=(5, 400),
+                                        w_avg=0.7, w_peak=0.3)
+    wl = make_workload(cfg)
+    dec = make_decoder(wl)
+    qb = _run_scores(dec, wl, 0)
+    scores = dec.scores.cpu().numpy()
+    for b in range(cfg.B):
+        for h in range(cfg.H_kv):
+            S, A, L = _oracle_scores(wl, b, h, 0, qb[b])
+            assert_scores(scores[b, h, :O.num_pages(L, cfg.ps)], S, A)
+
+
+def _run_select(scores_np, lens, ps, topk, H):
+    from sparse_paged_kv_page_gb300 import make_batch, sa_select_topk
+    B, _, maxp = scores_np.shape
+    sc = torch.from_numpy(scores_np.astype(np.float32)).cuda()
+    bt = torch.zeros((B, maxp), dtype=torch.int32, device="cuda")
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    batch = make_batch(bt, sl)
+    sel = torch.full((B, H, topk), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, H), -7, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sa_select_topk(sc, maxp, batch, ps, H, topk, sel, cnt, dev_status=st)
+    torch.cuda.synchronize()
+    return sel.cpu().numpy(), cnt.cpu().numpy(), int(st.item())
+
+
+@pytest.mark.parametrize("kind", ["continuous", "ties", "specials"])
+@pytest.mark.parametrize("topk", [1, 2, 7, 64, 256])
+def test_select_bit_exact_on_generated_scores(kind, topk):
+    rng = np.random.default_rng([77, topk, len(kind)])
+    B, H, maxp, ps = 3, 4, 3000, 16
+    if kind == "continuous":
+        s = rng.standard_normal((B, H, maxp)).astype(np.float32)
+    elif kind == "ties":
+        s = rng.integers(-3, 4, size=(B, H, maxp)).astype(np.float32) * 0.5
+    else:
+        pool = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 1e-30, -1e-30, 3.0],
+                        dtype=np.float32)
+        s = rng.choice(pool, size=(B, H, maxp))
+    lens = [maxp * ps, int(rng.integers(1, 200)) * ps - 3, 0]
+    sel, cnt, st = _run_select(s, lens, ps, topk, H)
+    assert st == 0
+    for b in range(B):
+        n = O.num_pages(lens[b], ps)
+        for h in range(H):
+            want = O.select_pages(s[b, h], n, topk)
+            assert cnt[b, h] == len(want)
+            assert np.array_equal(sel[b, h, :cnt[b, h]], want), (b, h)
+            assert np.all(sel[b, h, cnt[b, h]:] == -7)
+
+
+def test_select_large_candidate_count():
+    rng = np.random.default_rng(5)
+    B, H, maxp, ps = 1, 2, 49152, 16
+    s = rng.standard_normal((B, H, maxp)).astype(np.float32)
+    s[0, 1, 100:5000] = 0.25                          # a huge tie block at the boundary
+    sel, cnt, st = _run_select(s, [maxp * ps], ps, 3000, H)
+    for h in range(H):
+        assert np.array_equal(sel[0, h, :cnt[0, h]], O.select_pages(s[0, h], maxp, 3000))
+
+
+def test_bad_block_scores_nan_and_flags():
+    wl = make_workload(config(1))
+    dec = make_decoder(wl)
+    bt = torch.from_numpy(wl.block_table.copy())
+    bt[0, 3] = 1000                                   # out of range
+    dec.set_block_table(bt)
+    _run_scores(dec, wl, 0)
+    assert dev_status(dec) & 1
+    assert torch.isnan(dec.scores[0, 0, 3])
