@@ -179,7 +179,7 @@ class Workload:
         c = self.cfg
         s = {}
         ps, B = c.ps, c.B
-        cap_pages = int(((self.prefill_lens.max() + max(c.decode_steps, 0) + 4096) + ps - 1) // ps)
+        cap_pages = int(((self.prefill_lens.max() + self.total_steps + 4096) + ps - 1) // ps)
         if c.structure == "page_unit_offset":
             s["u_page"] = _unit(rng, B, cap_pages, c.D).astype(np.float32)
         elif c.structure == "page_normal_offset":

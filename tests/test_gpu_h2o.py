@@ -45,7 +45,7 @@ def _run_update(hh_bits, logits, lse, ret, cnt, bt, G, budget, n_sink, grace, de
 
 def _inputs(rng, B, H, G, n, cap, L, zero_probs=False, tie_vals=None):
     nslots = B * L + 7
-    bt = np.stack([rng.permutation(nslots)[:L] for _ in range(B)]).astype(np.int32)
+    bt = rng.permutation(nslots)[:B * L].reshape(B, L).astype(np.int32)   # disjoint slots
     ret = np.zeros((B, H, cap), dtype=np.int64)
     cnt = np.full((B, H), n, dtype=np.int64)
     for b in range(B):
