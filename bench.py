@@ -151,19 +151,16 @@ def _worker_init(spec):
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[v] = "1"
     import numpy as np
-    from multiprocessing import shared_memory
-    for name, (shm_name, shape) in spec.items():
-        shm = shared_memory.SharedMemory(name=shm_name)
-        _W[name + "_shm"] = shm
-        _W[name] = np.ndarray(shape, dtype=np.uint16, buffer=shm.buf)
+    for name, path in spec.items():
+        _W[name] = np.load(path, mmap_mode="r")
 
 
 def _worker_task(task):
     import numpy as np
     import oracle as O
     b, h, lo, hi, extra_k, extra_v, L, qg, kind, kw, hh, pos = task
-    ks = _W["k"][lo:hi, h]
-    vs = _W["v"][lo:hi, h]
+    ks = np.ascontiguousarray(_W["k"][lo:hi, h])
+    vs = np.ascontiguousarray(_W["v"][lo:hi, h])
     if extra_k is not None:
         ks = np.concatenate([ks, extra_k], 0)
         vs = np.concatenate([vs, extra_v], 0)
@@ -180,16 +177,15 @@ class OracleRunner:
 
     def __init__(self, wl, workers):
         import multiprocessing as mp
-        from multiprocessing import shared_memory
+        import tempfile
         import numpy as np
         self.wl, self.workers = wl, workers
-        self.shms = []
+        self.dir = tempfile.mkdtemp(prefix="sa_oracle_")
         spec = {}
         for name, arr in (("k", wl.k_pre), ("v", wl.v_pre)):
-            shm = shared_memory.SharedMemory(create=True, size=max(1, arr.nbytes))
-            np.ndarray(arr.shape, dtype=np.uint16, buffer=shm.buf)[...] = arr
-            self.shms.append(shm)
-            spec[name] = (shm.name, arr.shape)
+            path = os.path.join(self.dir, name + ".npy")
+            np.save(path, arr)
+            spec[name] = path
         self.pool = mp.get_context("spawn").Pool(workers, initializer=_worker_init,
                                                  initargs=(spec,))
 
@@ -224,11 +220,10 @@ class OracleRunner:
         return time.perf_counter() - t0
 
     def close(self):
+        import shutil
         self.pool.close()
         self.pool.join()
-        for s in self.shms:
-            s.close()
-            s.unlink()
+        shutil.rmtree(self.dir, ignore_errors=True)
 
 
 def units_of(cfg):
