@@ -73,6 +73,7 @@ typedef enum sa_dtype { SA_BF16 = 0, SA_FP16 = 1 } sa_dtype;
 #define SA_DEV_BAD_BLOCK 1  /* block-table entry outside [0, num_blocks), or page index out of range */
 #define SA_DEV_OVERFLOW 2   /* table or retained-list capacity exceeded; the excess was dropped */
 #define SA_DEV_BAD_COUNT 4  /* a selection / retained count outside [0, stride] (clamped) */
+#define SA_DEV_TIMEOUT 8    /* a bounded wait inside a kernel gave up (the kernel stopped early) */
 
 /* The paged cache: pools plus per-page statistics. */
 typedef struct sa_cache {
@@ -147,7 +148,7 @@ sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, const void*
  *   max_pages  host: row length of scores, >= every request's page count
  *            (else SA_DEV_OVERFLOW for that request)
  * A page whose block id is out of range scores NaN and sets SA_DEV_BAD_BLOCK.
- * Needs cache->meta. Arithmetic: float32, using the exact identity
+ * Needs cache->meta. Limits: batch <= 1024 (else SA_ERR_UNSUPPORTED). Arithmetic: float32, using the exact identity
  * max(q*M, q*m) = max(q,0)*M + min(q,0)*m (M >= m) so the cost per page does
  * not grow with G.
  */

@@ -16,7 +16,7 @@ c_f32 = ctypes.c_float
 c_size = ctypes.c_size_t
 
 SA_BF16, SA_FP16 = 0, 1
-SA_DEV_BAD_BLOCK, SA_DEV_OVERFLOW, SA_DEV_BAD_COUNT = 1, 2, 4
+SA_DEV_BAD_BLOCK, SA_DEV_OVERFLOW, SA_DEV_BAD_COUNT, SA_DEV_TIMEOUT = 1, 2, 4, 8
 
 
 class SaCache(ctypes.Structure):

@@ -38,7 +38,11 @@ struct AppendArgs {
 };
 
 constexpr int kAppendThreads = 128;
+constexpr int kRowBatch = 16;     // rows of a page loaded per batch (independent 16-byte loads)
 
+// One CTA per (touched page, request); thread (h, c) owns 8 columns
+// [8c, 8c+8) of KV head h. All rows of a batch are loaded before any is
+// used, so a page costs one memory round trip per 16 rows.
 template <typename T>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
   using E = Elem<T>;
@@ -73,40 +77,72 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
   const int page_start = p * ps;
   const int fill = min(ps, L_new - page_start);          // valid tokens after the append
   const int s_new = max(0, L_old - page_start);          // first slot written here
-  const int DP = D / 2;
-  const uint32_t* kn = static_cast<const uint32_t*>(a.k_new);
-  const uint32_t* vn = static_cast<const uint32_t*>(a.v_new);
-  uint32_t* kp_all = static_cast<uint32_t*>(a.k);
-  uint32_t* vp_all = static_cast<uint32_t*>(a.v);
+  const int C = D / 8;                                    // 16-byte chunks per row
+  const uint4* kn = static_cast<const uint4*>(a.k_new);
+  const uint4* vn = static_cast<const uint4*>(a.v_new);
+  uint4* kp = static_cast<uint4*>(a.k);
+  uint4* vp = static_cast<uint4*>(a.v);
 
-  for (int idx = threadIdx.x; idx < H * DP; idx += kAppendThreads) {
-    const int h = idx / DP, dp = idx % DP;
+  for (int idx = threadIdx.x; idx < H * C; idx += kAppendThreads) {
+    const int h = idx / C, c = idx % C;
     const int64_t tile = (int64_t(blk) * H + h) * ps;    // first row of this (block, head)
-    float mn0 = INFINITY, mn1 = INFINITY, mx0 = -INFINITY, mx1 = -INFINITY;
-    double s0 = 0.0, s1 = 0.0;
-    for (int s = 0; s < fill; ++s) {
-      const int64_t dst = (tile + s) * DP + dp;
-      uint32_t u;
-      if (s >= s_new) {
-        const int64_t src = (int64_t(row0 + page_start + s - L_old) * H + h) * DP + dp;
-        u = kn[src];
-        kp_all[dst] = u;
-        vp_all[dst] = vn[src];
-      } else {
-        u = kp_all[dst];
+    float mn[8], mx[8];
+    double sm[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) { mn[e] = INFINITY; mx[e] = -INFINITY; sm[e] = 0.0; }
+    for (int s0 = 0; s0 < fill; s0 += kRowBatch) {
+      uint4 r[kRowBatch];
+#pragma unroll
+      for (int j = 0; j < kRowBatch; ++j) {
+        const int s = s0 + j;
+        if (s < fill) {
+          if (s >= s_new) {
+            const int64_t src = (int64_t(row0 + page_start + s - L_old) * H + h) * C + c;
+            r[j] = kn[src];
+          } else {
+            r[j] = kp[(tile + s) * C + c];
+          }
+        }
       }
-      const float x0 = E::lo(u), x1 = E::hi(u);
-      mn0 = fminf(mn0, x0); mn1 = fminf(mn1, x1);
-      mx0 = fmaxf(mx0, x0); mx1 = fmaxf(mx1, x1);
-      s0 += double(x0); s1 += double(x1);
+#pragma unroll
+      for (int j = 0; j < kRowBatch; ++j) {
+        const int s = s0 + j;
+        if (s < fill) {
+          const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = E::lo(w[e]), x1 = E::hi(w[e]);
+            mn[2 * e] = fminf(mn[2 * e], x0); mn[2 * e + 1] = fminf(mn[2 * e + 1], x1);
+            mx[2 * e] = fmaxf(mx[2 * e], x0); mx[2 * e + 1] = fmaxf(mx[2 * e + 1], x1);
+            sm[2 * e] += double(x0); sm[2 * e + 1] += double(x1);
+          }
+        }
+      }
+      // write the new rows (keys from registers, values copied)
+#pragma unroll
+      for (int j = 0; j < kRowBatch; ++j) {
+        const int s = s0 + j;
+        if (s < fill && s >= s_new) {
+          const int64_t src = (int64_t(row0 + page_start + s - L_old) * H + h) * C + c;
+          kp[(tile + s) * C + c] = r[j];
+          vp[(tile + s) * C + c] = vn[src];
+        }
+      }
     }
     if (a.meta) {
-      uint32_t* m = static_cast<uint32_t*>(a.meta) + (int64_t(blk) * H + h) * 3 * DP + dp;
-      const double inv = 1.0 / double(fill);
-      m[0] = E::pack(mn0, mn1);                          // exact: values are already dtype
-      m[DP] = E::pack(mx0, mx1);
-      const uint32_t me = uint32_t(E::from_f64(s0 * inv)) | (uint32_t(E::from_f64(s1 * inv)) << 16);
-      m[2 * DP] = me;
+      uint4* m = static_cast<uint4*>(a.meta) + (int64_t(blk) * H + h) * 3 * C + c;
+      const double f = double(fill);
+      uint32_t w0[4], w1[4], w2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        w0[e] = E::pack(mn[2 * e], mn[2 * e + 1]);       // exact: values are already dtype
+        w1[e] = E::pack(mx[2 * e], mx[2 * e + 1]);
+        w2[e] = uint32_t(E::from_f64(sm[2 * e] / f)) |
+                (uint32_t(E::from_f64(sm[2 * e + 1] / f)) << 16);
+      }
+      m[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+      m[C] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+      m[2 * C] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
     }
   }
   // H2O slots of the written tokens start at zero.

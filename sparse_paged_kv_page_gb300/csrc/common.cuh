@@ -149,6 +149,60 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, uint32_t addr) {
 }
 
 // ---------------------------------------------------------------------------
+// mbarrier + bulk (TMA engine) copies
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for phase `parity` of an mbarrier, giving up after ~1 s of wall time
+// (sets SA_DEV_TIMEOUT and returns false). Correct code never times out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > 1000000000ull) {
+      flag(status, SA_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// Bulk copy global -> this CTA's shared memory, completion counted in bytes on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // order-preserving keys
 // ---------------------------------------------------------------------------
 // float32 -> uint32 whose unsigned order is the float order, -0 == +0, NaN
@@ -165,6 +219,15 @@ __device__ __forceinline__ uint32_t bf16_key(uint16_t u) {
   if ((u & 0x7fffu) > 0x7f80u) return 0xffffu;
   if (u == 0x8000u) u = 0;
   return (u & 0x8000u) ? (~uint32_t(u) & 0xffffu) : (uint32_t(u) | 0x8000u);
+}
+
+// Histogram increment aggregated across the warp: lanes holding the same bin
+// add once (one shared-memory atomic per distinct bin per warp). Every lane of
+// the warp must call it; `bin` < 0 means "no key on this lane".
+__device__ __forceinline__ void warp_hist_add(int* hist, int bin) {
+  const unsigned peers = __match_any_sync(kFull, bin);
+  const int leader = __ffs(peers) - 1;
+  if (bin >= 0 && (threadIdx.x & 31) == leader) atomicAdd(&hist[bin], __popc(peers));
 }
 
 // ---------------------------------------------------------------------------

@@ -33,6 +33,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 3;
 constexpr int kMaxSplit = 64;
+constexpr int kMaxEnt = 4096;          // (block, fill) entries staged per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -52,6 +53,7 @@ struct DecodeArgs {
   int32_t* tickets;
   int32_t* status;
   int H_kv, H_q, G, ps, ps_shift, num_blocks, bt_stride, sel_stride, logits_stride, nsplit;
+  int ent_max;      // entries of the selection one CTA can touch
   float scale, scale_log2;
 };
 
@@ -100,6 +102,28 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   const T* kbase = static_cast<const T*>(a.k);
   const T* vbase = static_cast<const T*>(a.v);
 
+  // Prologue: resolve the selection entries this CTA touches to (block, fill)
+  // once, in parallel, so the copy loop never waits on sel -> block table.
+  int2* s_ent = reinterpret_cast<int2*>(smem + TL::kSmem);
+  const int row_begin = t_begin << 4, row_end = min(t_end << 4, n_rows);
+  const int e_begin = row_begin >> pss;
+  const int e_cnt = row_end > row_begin ? min(((row_end - 1) >> pss) - e_begin + 1, a.ent_max) : 0;
+  for (int i = threadIdx.x; i < e_cnt; i += kThreads) {
+    const int e = e_begin + i;
+    int blk = -1, fill = 0;
+    const int page = sel[e];
+    if (page < 0 || page >= n_pages_req || page >= a.bt_stride) {
+      flag(a.status, SA_DEV_BAD_BLOCK);
+    } else {
+      fill = min(ps, L - (page << pss));
+      const int x = btb[page];
+      if (x < 0 || x >= a.num_blocks) flag(a.status, SA_DEV_BAD_BLOCK);
+      else blk = x;
+    }
+    s_ent[i] = make_int2(blk, fill);
+  }
+  __syncthreads();
+
   // Q as the A operand (rows = query heads of this KV head, zero beyond G)
   const int g = lane >> 2, tq = lane & 3;
   uint32_t qa[D / 16][4];
@@ -131,19 +155,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
     bool valid = false;
     if (lane < 16) {
       const int j = (t << 4) + lane;
-      const int e = j >> pss, s = j & (ps - 1);
-      if (e < cnt) {
-        const int page = sel[e];
-        if (page < 0 || page >= n_pages_req || page >= a.bt_stride) {
-          flag(a.status, SA_DEV_BAD_BLOCK);
-        } else if (s < min(ps, L - (page << pss))) {
-          const int blk = btb[page];
-          if (blk < 0 || blk >= a.num_blocks) {
-            flag(a.status, SA_DEV_BAD_BLOCK);
-          } else {
-            valid = true;
-            off = ((int64_t(blk) * a.H_kv + h) * ps + s) * D;
-          }
+      const int ei = (j >> pss) - e_begin, s = j & (ps - 1);
+      if (j < row_end && ei < e_cnt) {
+        const int2 en = s_ent[ei];
+        if (en.x >= 0 && s < en.y) {
+          valid = true;
+          off = ((int64_t(en.x) * a.H_kv + h) * ps + s) * D;
         }
       }
     }
@@ -264,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   // merge the 4 warps in shared memory (reusing the tile buffers)
   float* wm = reinterpret_cast<float*>(smem);                 // [kWarps][16]
   float* wl = wm + kWarps * 16;                                // [kWarps][16]
-  float* wo = wl + kWarps * 16;                                // [kWarps][G][D]
+  float* wo = wl + kWarps * 16;                                // [kWarps][G][D + 4]
+  constexpr int WS = D + 4;                                    // padded row: no bank conflicts
   if (tq == 0) {
     if (g < G) { wm[warp * 16 + g] = m_r[0]; wl[warp * 16 + g] = l_r[0]; }
     if (g + 8 < G) { wm[warp * 16 + g + 8] = m_r[1]; wl[warp * 16 + g + 8] = l_r[1]; }
@@ -273,12 +291,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   for (int x = 0; x < D / 8; ++x) {
     const int d = x * 8 + 2 * tq;
     if (g < G) {
-      wo[(warp * G + g) * D + d] = o[x][0];
-      wo[(warp * G + g) * D + d + 1] = o[x][1];
+      wo[(warp * G + g) * WS + d] = o[x][0];
+      wo[(warp * G + g) * WS + d + 1] = o[x][1];
     }
     if (g + 8 < G) {
-      wo[(warp * G + g + 8) * D + d] = o[x][2];
-      wo[(warp * G + g + 8) * D + d + 1] = o[x][3];
+      wo[(warp * G + g + 8) * WS + d] = o[x][2];
+      wo[(warp * G + g + 8) * WS + d + 1] = o[x][3];
     }
   }
   __syncthreads();
@@ -296,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
         const float mw = wm[w * 16 + row];
         if (mw == -INFINITY) continue;
         const float f = exp2f(mw - M);
-        acc += wo[(w * G + row) * D + d] * f;
+        acc += wo[(w * G + row) * WS + d] * f;
         tot += wl[w * 16 + row] * f;
       }
     }
@@ -382,13 +400,22 @@ int num_sms() {
   return sms[dev];
 }
 
-// Splits per (request, KV head): enough CTAs for ~4 per SM, at most one per tile.
-int choose_nsplit(int units, int max_tiles, int sms) {
-  const int target = 4 * sms;
+// Splits per (request, KV head): one wave of two CTAs per SM, at most one
+// split per tile, and enough splits that a CTA's entry table stays small.
+int choose_nsplit(int units, int max_tiles, int ps, int sms) {
+  const int target = 2 * sms;
   int s = (target + units - 1) / units;
+  const int64_t ent_total = (int64_t(max_tiles) * 16 + ps - 1) / ps;
+  const int need = int((ent_total + kMaxEnt - 1) / kMaxEnt);
+  if (s < need) s = need;
   if (s > max_tiles) s = max_tiles;
   if (s > kMaxSplit) s = kMaxSplit;
   return s < 1 ? 1 : s;
+}
+
+int ent_max_for(int max_tiles, int nsplit, int ps) {
+  const int per = (max_tiles + nsplit - 1) / nsplit;
+  return (per * 16 + ps - 1) / ps + 1;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -411,8 +438,9 @@ int g_dec_smem[4][64];
 template <typename T, int D>
 sa_status launch_decode(const DecodeArgs& a, dim3 grid, cudaStream_t s, int* cache) {
   auto k = decode_kernel<T, D>;
-  if (!ensure_smem(k, Tile<D>::kSmem, cache)) return SA_ERR_CUDA;
-  k<<<grid, kThreads, Tile<D>::kSmem, s>>>(a);
+  const int smem = Tile<D>::kSmem + a.ent_max * int(sizeof(int2));
+  if (!ensure_smem(k, smem, cache)) return SA_ERR_CUDA;
+  k<<<grid, kThreads, smem, s>>>(a);
   return launch_status();
 }
 
@@ -427,7 +455,8 @@ extern "C" size_t sa_decode_workspace_size(int32_t batch, int32_t num_kv_heads, 
     return 0;
   const int units = batch * num_kv_heads;
   const int64_t max_tiles = (int64_t(sel_stride) * page_size + 15) / 16;
-  const int ns = choose_nsplit(units, int(max_tiles > (1 << 30) ? (1 << 30) : max_tiles), num_sms());
+  const int ns = choose_nsplit(units, int(max_tiles > (1 << 30) ? (1 << 30) : max_tiles), page_size,
+                               num_sms());
   return ws_layout(units, num_q_heads / num_kv_heads, head_dim, ns).total;
 }
 
@@ -457,7 +486,8 @@ extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* bat
   if (rows > (int64_t(1) << 30)) return SA_ERR_UNSUPPORTED;
   if (logits && logits_stride < rows) return SA_ERR_INVALID_ARG;
   const int units = batch->batch * cache->num_kv_heads;
-  const int ns = choose_nsplit(units, int((rows + 15) / 16), num_sms());
+  const int max_tiles = int((rows + 15) / 16);
+  const int ns = choose_nsplit(units, max_tiles, cache->page_size, num_sms());
   const WsLayout w = ws_layout(units, G, cache->head_dim, ns);
   if (ns > 1 && (!workspace || workspace_bytes < w.total)) return SA_ERR_WORKSPACE;
   DecodeArgs a;
@@ -472,6 +502,7 @@ extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* bat
   a.ps_shift = log2i(cache->page_size); a.num_blocks = cache->num_blocks;
   a.bt_stride = batch->bt_stride; a.sel_stride = sel_stride;
   a.logits_stride = logits ? logits_stride : 0; a.nsplit = ns;
+  a.ent_max = ent_max_for(max_tiles, ns, cache->page_size);
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf(float(cache->head_dim));
   a.scale_log2 = a.scale * kLog2e;
   dim3 grid(unsigned(ns), unsigned(cache->num_kv_heads), unsigned(batch->batch));

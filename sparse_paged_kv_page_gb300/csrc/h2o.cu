@@ -103,9 +103,14 @@ __global__ void __launch_bounds__(kH2oThreads) h2o_kernel(H2oArgs a) {
     const int shift = 8 - 8 * pass;
     if (tid < 256) hist[tid] = 0;
     __syncthreads();
-    for (int j = lo + tid; j < hi; j += kH2oThreads) {
-      const uint32_t k = s_key[j];
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    for (int j0 = lo; j0 < hi; j0 += kH2oThreads) {           // warp-uniform trip count
+      const int j = j0 + tid;
+      int bin = -1;
+      if (j < hi) {
+        const uint32_t k = s_key[j];
+        if ((k & mask) == prefix) bin = int((k >> shift) & 255u);
+      }
+      warp_hist_add(hist, bin);
     }
     __syncthreads();
     if (tid < 32) {

@@ -11,20 +11,31 @@
 //   max(q max_d, q min_d) = q+ max_d + q- min_d,
 // so the group-mean score is
 //   S(p) = sum_d [ w_avg qbar_d mean_pd + w_peak (P_d max_pd + N_d min_pd) ]
-// with qbar, P, N the group means of q, q+, q-. Each CTA folds the G queries
-// of its KV head into those three coefficient vectors once; the page loop is
-// then 3 FMAs per element whatever G is, and the kernel is a gather of
-// 3 * head_dim * 2 bytes of statistics per page, bounded by HBM bandwidth.
+// with qbar, P, N the group means of q, q+, q-: 3 FMAs per element whatever
+// G is. The kernel is then a gather of 3 * head_dim * 2 bytes of statistics
+// per (page, KV head) through the block table, bounded by HBM bandwidth.
 //
-// Mapping: a group of head_dim / 8 lanes owns one page; each lane loads the
-// 16-byte slice of the page's min, max and mean rows (non-coherent, L1
-// bypass), so every 16-lane group reads three contiguous 256-byte rows. Four
-// pages per lane group are in flight per iteration.
+// Design: persistent CTAs (two per SM), the batch's pages cut into chunks of
+// 32 pages of one (request, KV head) and the chunk list split evenly across
+// CTAs (a device-side prefix over request lengths, so ragged batches
+// balance). In each CTA one producer warp resolves a chunk's block ids and has
+// the TMA engine gather every page's contiguous statistics rows with one
+// cp.async.bulk per page into a 4-stage shared-memory ring, completion counted
+// in bytes on the stage's mbarrier; four consumer warps score from shared
+// memory (16 lanes per page, one 16-byte slice of each row per lane, shuffle
+// reduction) and release the stage. Block ids of the next chunk are loaded
+// before waiting for a free stage, so the table lookup overlaps the copies.
 #include "common.cuh"
 #include "host.h"
 
 namespace sa {
 namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kScThreads = 32 * (kConsumerWarps + 1);
+constexpr int kChunk = 32;                 // pages per stage (one per producer lane)
+constexpr int kStages = 4;
+constexpr int kMaxBatch = 1024;
 
 struct ScoreArgs {
   const void* meta;
@@ -33,104 +44,217 @@ struct ScoreArgs {
   const int32_t* seq_lens;
   float* scores;
   int32_t* status;
-  int H_kv, H_q, G, ps, num_blocks, bt_stride, max_pages;
+  int B, H_kv, H_q, G, ps, num_blocks, bt_stride, max_pages;
   float w_avg, w_peak;
 };
 
-constexpr int kScoreThreads = 256;
-constexpr int kScoreUnroll = 4;
-constexpr int kPagesPerCta = 256;
+template <int D>
+struct ScoreTile {
+  static constexpr int kPageBytes = 3 * D * 2;             // min, max, mean rows
+  static constexpr int kStageBytes = kChunk * kPageBytes;
+  static constexpr int kSmem = kStages * kStageBytes;
+};
+
+struct ChunkHdr {
+  int b, h, p0, count;
+  uint32_t valid;                                          // bit j: page p0+j has a good block
+};
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kScThreads, 2) score_kernel(ScoreArgs a) {
   using E = Elem<T>;
-  constexpr int LPP = D / 8;                    // lanes per page
-  constexpr int PPP = kScoreThreads / LPP;      // pages per pass
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int L = a.seq_lens[b];
-  int n = (L + a.ps - 1) / a.ps;
-  if (n > a.max_pages || n > a.bt_stride) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
-    n = min(a.max_pages, a.bt_stride);
-  }
-  const int p_begin = blockIdx.x * kPagesPerCta;
-  if (p_begin >= n) return;
-  const int p_end = min(n, p_begin + kPagesPerCta);
-  const int grp = threadIdx.x / LPP, l = threadIdx.x % LPP;
+  using TL = ScoreTile<D>;
+  constexpr int LPP = D / 8;                               // lanes per page
+  constexpr int PPP = 32 * kConsumerWarps / LPP;           // pages per consumer pass
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ ChunkHdr hdr[kStages];
+  __shared__ int s_prefix[kMaxBatch + 1];                  // chunks before request b
+  __shared__ int scan_tmp[32];
 
-  // group-mean coefficients of this lane's 8 dimensions
-  float ca[8], cp[8], cn[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) ca[e] = cp[e] = cn[e] = 0.f;
-  const T* qh = static_cast<const T*>(a.q) + (int64_t(b) * a.H_q + int64_t(h) * a.G) * D + l * 8;
-  for (int g = 0; g < a.G; ++g) {
-    const uint4 v = *reinterpret_cast<const uint4*>(qh + int64_t(g) * D);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float x0 = E::lo(w[e]), x1 = E::hi(w[e]);
-      ca[2 * e] += x0; ca[2 * e + 1] += x1;
-      cp[2 * e] += fmaxf(x0, 0.f); cp[2 * e + 1] += fmaxf(x1, 0.f);
-      cn[2 * e] += fminf(x0, 0.f); cn[2 * e + 1] += fminf(x1, 0.f);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // chunk prefix over requests: request b owns H_kv * ceil(n_b / kChunk) chunks
+  {
+    const int per = (a.B + kScThreads - 1) / kScThreads;
+    const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+      int n = (a.seq_lens[b] + a.ps - 1) / a.ps;
+      n = max(0, min(n, min(a.max_pages, a.bt_stride)));
+      local += a.H_kv * ((n + kChunk - 1) / kChunk);
     }
-  }
-  const float ia = a.w_avg / float(a.G), ip = a.w_peak / float(a.G);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) { ca[e] *= ia; cp[e] *= ip; cn[e] *= ip; }
-
-  const int32_t* btb = a.bt + int64_t(b) * a.bt_stride;
-  float* out = a.scores + (int64_t(b) * a.H_kv + h) * a.max_pages;
-  const uint8_t* meta = static_cast<const uint8_t*>(a.meta);
-  for (int p0 = p_begin; p0 < p_end; p0 += PPP * kScoreUnroll) {
-    uint4 vmn[kScoreUnroll], vmx[kScoreUnroll], vme[kScoreUnroll];
-    int state[kScoreUnroll];                     // 0 = no page, 1 = ok, 2 = bad block
-#pragma unroll
-    for (int u = 0; u < kScoreUnroll; ++u) {
-      const int p = p0 + u * PPP + grp;
-      state[u] = 0;
-      vmn[u] = vmx[u] = vme[u] = make_uint4(0, 0, 0, 0);
-      if (p < p_end) {
-        const int blk = btb[p];
-        if (blk < 0 || blk >= a.num_blocks) {
-          state[u] = 2;
-        } else {
-          state[u] = 1;
-          const uint8_t* base =
-              meta + ((int64_t(blk) * a.H_kv + h) * 3 * D + l * 8) * int64_t(sizeof(T));
-          vmn[u] = ld_nc_v4(base);
-          vmx[u] = ld_nc_v4(base + D * sizeof(T));
-          vme[u] = ld_nc_v4(base + 2 * D * sizeof(T));
+    int total;
+    int run = block_exclusive_scan<kScThreads>(local, scan_tmp, &total);
+    for (int b = b0; b < b1; ++b) {
+      s_prefix[b] = run;
+      int n = (a.seq_lens[b] + a.ps - 1) / a.ps;
+      n = max(0, min(n, min(a.max_pages, a.bt_stride)));
+      run += a.H_kv * ((n + kChunk - 1) / kChunk);
+    }
+    if (tid == 0) s_prefix[a.B] = total;
+    if (tid == 0 && blockIdx.x == 0)
+      for (int b = 0; b < a.B; ++b)
+        if ((a.seq_lens[b] + a.ps - 1) / a.ps > min(a.max_pages, a.bt_stride)) {
+          flag(a.status, SA_DEV_OVERFLOW);
+          break;
         }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kConsumerWarps);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const int total = s_prefix[a.B];
+  const int c_begin = int((int64_t(total) * blockIdx.x) / gridDim.x);
+  const int c_end = int((int64_t(total) * (blockIdx.x + 1)) / gridDim.x);
+  if (c_begin >= c_end) return;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    auto locate = [&](int ci, int& b, int& h, int& p0, int& count) {
+      int lo = 0, hi = a.B;                                // largest b with prefix[b] <= ci
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_prefix[mid] <= ci) lo = mid; else hi = mid;
+      }
+      while (lo + 1 <= a.B && s_prefix[lo + 1] <= ci) ++lo;   // skip requests with no chunks
+      b = lo;
+      int n = (a.seq_lens[b] + a.ps - 1) / a.ps;
+      n = max(0, min(n, min(a.max_pages, a.bt_stride)));
+      const int kb = (n + kChunk - 1) / kChunk;
+      const int r = ci - s_prefix[b];
+      h = r / kb;
+      p0 = (r % kb) * kChunk;
+      count = min(kChunk, n - p0);
+    };
+    int nb, nh, np0, ncount, nblk;
+    locate(c_begin, nb, nh, np0, ncount);
+    nblk = lane < ncount ? a.bt[int64_t(nb) * a.bt_stride + np0 + lane] : -1;
+    bool ok = true;
+    for (int ci = c_begin, it = 0; ci < c_end; ++ci, ++it) {
+      const int b = nb, h = nh, p0 = np0, count = ncount, blk = nblk;
+      if (ci + 1 < c_end) {                                // prefetch the next chunk's block ids
+        locate(ci + 1, nb, nh, np0, ncount);
+        nblk = lane < ncount ? a.bt[int64_t(nb) * a.bt_stride + np0 + lane] : -1;
+      }
+      const int s = it % kStages;
+      if (it >= kStages && !mbar_wait(smem_u32(&empty_bar[s]), ((it / kStages) - 1) & 1, a.status)) {
+        ok = false;
+        break;
+      }
+      const bool good = lane < count && blk >= 0 && blk < a.num_blocks;
+      if (lane < count && !good) flag(a.status, SA_DEV_BAD_BLOCK);
+      const uint32_t valid = __ballot_sync(kFull, good);
+      if (lane == 0) {
+        hdr[s] = ChunkHdr{b, h, p0, count, valid};
+        mbar_arrive_expect_tx(smem_u32(&full_bar[s]), uint32_t(__popc(valid)) * TL::kPageBytes);
+      }
+      __syncwarp();
+      if (good) {
+        const uint8_t* src = static_cast<const uint8_t*>(a.meta) +
+                             (int64_t(blk) * a.H_kv + h) * int64_t(TL::kPageBytes);
+        bulk_g2s(smem_u32(smem + s * TL::kStageBytes + lane * TL::kPageBytes), src,
+                 TL::kPageBytes, smem_u32(&full_bar[s]));
       }
     }
+    // never leave with copies in flight: wait (bounded) for the last stages
+    if (lane == 0) {
+      const int n_it = c_end - c_begin;
+      for (int it = max(0, n_it - kStages); it < n_it && ok; ++it)
+        ok = mbar_wait(smem_u32(&full_bar[it % kStages]), (it / kStages) & 1, a.status);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int grp = tid / LPP, l = tid % LPP;
+  float ca[8], cp[8], cn[8];
+  int cur_b = -1, cur_h = -1;
+  for (int ci = c_begin, it = 0; ci < c_end; ++ci, ++it) {
+    const int s = it % kStages;
+    if (!mbar_wait(smem_u32(&full_bar[s]), (it / kStages) & 1, a.status)) break;
+    const ChunkHdr hd = hdr[s];
+    if (hd.b != cur_b || hd.h != cur_h) {
+      cur_b = hd.b;
+      cur_h = hd.h;
 #pragma unroll
-    for (int u = 0; u < kScoreUnroll; ++u) {
-      const uint32_t m0[4] = {vmn[u].x, vmn[u].y, vmn[u].z, vmn[u].w};
-      const uint32_t m1[4] = {vmx[u].x, vmx[u].y, vmx[u].z, vmx[u].w};
-      const uint32_t m2[4] = {vme[u].x, vme[u].y, vme[u].z, vme[u].w};
+      for (int e = 0; e < 8; ++e) ca[e] = cp[e] = cn[e] = 0.f;
+      const T* qh = static_cast<const T*>(a.q) + (int64_t(cur_b) * a.H_q + int64_t(cur_h) * a.G) * D + l * 8;
+      for (int g = 0; g < a.G; ++g) {
+        const uint4 v = *reinterpret_cast<const uint4*>(qh + int64_t(g) * D);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = E::lo(w[e]), x1 = E::hi(w[e]);
+          ca[2 * e] += x0; ca[2 * e + 1] += x1;
+          cp[2 * e] += fmaxf(x0, 0.f); cp[2 * e + 1] += fmaxf(x1, 0.f);
+          cn[2 * e] += fminf(x0, 0.f); cn[2 * e + 1] += fminf(x1, 0.f);
+        }
+      }
+      const float ia = a.w_avg / float(a.G), ip = a.w_peak / float(a.G);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) { ca[e] *= ia; cp[e] *= ip; cn[e] *= ip; }
+    }
+    float* out = a.scores + (int64_t(hd.b) * a.H_kv + hd.h) * a.max_pages + hd.p0;
+    const uint8_t* st = smem + s * TL::kStageBytes;
+#pragma unroll
+    for (int pass = 0; pass < kChunk / PPP; ++pass) {
+      const int j = pass * PPP + grp;
+      const bool here = j < hd.count && ((hd.valid >> j) & 1u);
       float acc = 0.f;
+      if (here) {
+        const uint8_t* pg = st + j * TL::kPageBytes + l * 16;
+        const uint4 vmn = *reinterpret_cast<const uint4*>(pg);
+        const uint4 vmx = *reinterpret_cast<const uint4*>(pg + D * 2);
+        const uint4 vme = *reinterpret_cast<const uint4*>(pg + 2 * D * 2);
+        const uint32_t m0[4] = {vmn.x, vmn.y, vmn.z, vmn.w};
+        const uint32_t m1[4] = {vmx.x, vmx.y, vmx.z, vmx.w};
+        const uint32_t m2[4] = {vme.x, vme.y, vme.z, vme.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(ca[2 * e], E::lo(m2[e]), acc);
-        acc = fmaf(ca[2 * e + 1], E::hi(m2[e]), acc);
-        acc = fmaf(cp[2 * e], E::lo(m1[e]), acc);
-        acc = fmaf(cp[2 * e + 1], E::hi(m1[e]), acc);
-        acc = fmaf(cn[2 * e], E::lo(m0[e]), acc);
-        acc = fmaf(cn[2 * e + 1], E::hi(m0[e]), acc);
+        for (int e = 0; e < 4; ++e) {
+          acc = fmaf(ca[2 * e], E::lo(m2[e]), acc);
+          acc = fmaf(ca[2 * e + 1], E::hi(m2[e]), acc);
+          acc = fmaf(cp[2 * e], E::lo(m1[e]), acc);
+          acc = fmaf(cp[2 * e + 1], E::hi(m1[e]), acc);
+          acc = fmaf(cn[2 * e], E::lo(m0[e]), acc);
+          acc = fmaf(cn[2 * e + 1], E::hi(m0[e]), acc);
+        }
       }
 #pragma unroll
       for (int o = LPP / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
-      if (l == 0 && state[u] != 0) {
-        const int p = p0 + u * PPP + grp;
-        if (state[u] == 2) {
-          flag(a.status, SA_DEV_BAD_BLOCK);
-          out[p] = __int_as_float(0x7fc00000);
-        } else {
-          out[p] = acc;
-        }
-      }
+      if (l == 0 && j < hd.count) out[j] = here ? acc : __int_as_float(0x7fc00000);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
   }
+}
+
+int g_sc_smem[4][64];
+
+template <typename T, int D>
+sa_status launch_score(const ScoreArgs& a, int grid, cudaStream_t s, int* cache) {
+  auto k = score_kernel<T, D>;
+  if (!ensure_smem(k, ScoreTile<D>::kSmem, cache)) return SA_ERR_CUDA;
+  k<<<grid, kScThreads, ScoreTile<D>::kSmem, s>>>(a);
+  return launch_status();
+}
+
+int sm_count() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!sms[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    sms[dev] = v;
+  }
+  return sms[dev];
 }
 
 }  // namespace
@@ -147,23 +271,22 @@ extern "C" sa_status sa_score_pages(const sa_cache* cache, const sa_batch* batch
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
   const int G = num_q_heads / cache->num_kv_heads;
   if (G > 16) return SA_ERR_UNSUPPORTED;
+  if (batch->batch > kMaxBatch) return SA_ERR_UNSUPPORTED;
   ScoreArgs a;
   a.meta = cache->meta; a.q = q; a.bt = batch->block_table; a.seq_lens = batch->seq_lens;
   a.scores = scores; a.status = dev_status;
-  a.H_kv = cache->num_kv_heads; a.H_q = num_q_heads; a.G = G; a.ps = cache->page_size;
-  a.num_blocks = cache->num_blocks; a.bt_stride = batch->bt_stride; a.max_pages = max_pages;
-  a.w_avg = w_avg; a.w_peak = w_peak;
+  a.B = batch->batch; a.H_kv = cache->num_kv_heads; a.H_q = num_q_heads; a.G = G;
+  a.ps = cache->page_size; a.num_blocks = cache->num_blocks; a.bt_stride = batch->bt_stride;
+  a.max_pages = max_pages; a.w_avg = w_avg; a.w_peak = w_peak;
+  // enough persistent CTAs for two per SM, never more than chunks could exist
   const int cap = max_pages < batch->bt_stride ? max_pages : batch->bt_stride;
-  dim3 grid(unsigned((cap + kPagesPerCta - 1) / kPagesPerCta), unsigned(a.H_kv),
-            unsigned(batch->batch));
+  const int64_t max_chunks = int64_t(batch->batch) * a.H_kv * ((cap + kChunk - 1) / kChunk);
+  const int grid = int(max_chunks < 2 * sm_count() ? max_chunks : 2 * sm_count());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = cache->dtype == SA_BF16;
-  if (cache->head_dim == 128) {
-    if (bf) score_kernel<__nv_bfloat16, 128><<<grid, kScoreThreads, 0, s>>>(a);
-    else score_kernel<__half, 128><<<grid, kScoreThreads, 0, s>>>(a);
-  } else {
-    if (bf) score_kernel<__nv_bfloat16, 64><<<grid, kScoreThreads, 0, s>>>(a);
-    else score_kernel<__half, 64><<<grid, kScoreThreads, 0, s>>>(a);
-  }
-  return launch_status();
+  if (cache->head_dim == 128)
+    return bf ? launch_score<__nv_bfloat16, 128>(a, grid, s, g_sc_smem[0])
+              : launch_score<__half, 128>(a, grid, s, g_sc_smem[1]);
+  return bf ? launch_score<__nv_bfloat16, 64>(a, grid, s, g_sc_smem[2])
+            : launch_score<__half, 64>(a, grid, s, g_sc_smem[3]);
 }

@@ -64,9 +64,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     const int shift = 24 - 8 * pass;
     if (tid < 256) hist[tid] = 0;
     __syncthreads();
-    for (int i = tid; i < nc; i += kSelThreads) {
-      const uint32_t k = keys[i];
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    for (int i0 = 0; i0 < nc; i0 += kSelThreads) {           // warp-uniform trip count
+      const int i = i0 + tid;
+      int bin = -1;
+      if (i < nc) {
+        const uint32_t k = keys[i];
+        if ((k & mask) == prefix) bin = int((k >> shift) & 255u);
+      }
+      warp_hist_add(hist, bin);
     }
     __syncthreads();
     if (tid < 32) {
