@@ -8,13 +8,25 @@
 // "EntmaxKV" README, "How it works": per-page key statistics refreshed on
 // append.
 //
-// One CTA per (touched page, request). The CTA writes the page's new tokens
-// and recomputes its statistics in the same pass, taking new values from the
-// input rows and old values from the pool, so no other CTA's writes are read.
-// Slots past the page's new fill are stale and never touched. The mean is
-// summed in float64 (exact for bf16/fp16 keys of any practical range) and
-// rounded once to the cache dtype. A second one-block kernel advances the
-// lengths after every CTA has read the old ones.
+// One CTA per (touched page, request); thread (h, c) owns the 8 columns
+// [8c, 8c+8) of KV head h and loads all of the page's rows before using any,
+// taking new rows from the input and old ones from the pool, so no other
+// CTA's writes are read and a page costs one memory round trip per 16 rows.
+// Slots past the page's new fill are stale and never touched.
+//
+// k_mean is the float64 mean rounded once to the cache dtype. GB300's float64
+// rate is low, so the kernel computes it in float32 and proves the result
+// exact: each running sum carries a TwoSum error term (zero => the float32
+// sum is the exact sum S); S / f in float32 is correctly rounded, and
+// rounding it to the dtype equals rounding S / f itself unless the float32
+// quotient lands exactly on a dtype midpoint, which is then settled by the
+// exact product midpoint * f against S. Columns where any of this does not
+// hold (an inexact running sum, float32 underflow, fp16 subnormals) recompute
+// in float64 from the pool.
+//
+// When every request touches at most two pages (decode), one CTA per request
+// handles its pages and then advances the request's length itself; otherwise
+// a second one-block kernel advances the lengths after all CTAs have read them.
 #include "common.cuh"
 #include "host.h"
 
@@ -29,10 +41,10 @@ struct AppendArgs {
   const void* v_new;
   const int32_t* new_cu;
   const int32_t* bt;
-  const int32_t* seq_lens;
+  int32_t* seq_lens;
   uint16_t* hh;
   int32_t* ret_pos;
-  const int32_t* ret_cnt;
+  int32_t* ret_cnt;
   int32_t* status;
   int H, D, ps, num_blocks, bt_stride, max_new, ret_cap;
 };
@@ -40,35 +52,46 @@ struct AppendArgs {
 constexpr int kAppendThreads = 128;
 constexpr int kRowBatch = 16;     // rows of a page loaded per batch (independent 16-byte loads)
 
-// One CTA per (touched page, request); thread (h, c) owns 8 columns
-// [8c, 8c+8) of KV head h. All rows of a batch are loaded before any is
-// used, so a page costs one memory round trip per 16 rows.
+// exact float32 sum step: s += x, clears `exact` if the addition rounded
+__device__ __forceinline__ void two_sum(float& s, float x, bool& exact) {
+  const float t = s + x;
+  const float bb = t - s;
+  const float err = (s - (t - bb)) + (x - bb);
+  exact &= (err == 0.f);
+  s = t;
+}
+
+// Round S / f (S exact) once to the element type; false if float32 cannot decide.
 template <typename T>
-__global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
+__device__ __forceinline__ bool mean_f32(float S, int f, uint16_t& out) {
   using E = Elem<T>;
-  const int b = blockIdx.y;
-  const int i = blockIdx.x;
+  const float aS = fabsf(S);
+  if (S == 0.f) { out = E::from_f(S); return true; }
+  if (!(aS >= 0x1p-100f)) return false;                       // float32 underflow risk
+  if ((f & (f - 1)) == 0) {                                    // power of two: exact scaling
+    const float q = S * (1.0f / float(f));
+    if (E::midpoint(q) < 0) return false;
+    out = E::from_f(q);
+    return true;
+  }
+  const float q = S / float(f);                                // correctly rounded
+  const int mid = E::midpoint(q);
+  if (mid < 0) return false;
+  if (mid == 0) { out = E::from_f(q); return true; }
+  const float prod = q * float(f);                             // exact: few significant bits
+  if (S == prod) { out = E::from_f(q); return true; }          // a true tie: to even
+  const uint16_t lo = E::from_f_rz(fabsf(q));                  // smaller-magnitude neighbour
+  const uint16_t mag = fabsf(S) > fabsf(prod) ? uint16_t(lo + 1) : lo;
+  out = uint16_t(mag | (S < 0.f ? 0x8000u : 0u));
+  return true;
+}
+
+// Recompute statistics of page p of request b (all heads) and write the new rows.
+template <typename T>
+__device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, int L_old, int L_new,
+                                             int row0) {
+  using E = Elem<T>;
   const int ps = a.ps, H = a.H, D = a.D;
-  const int L_old = a.seq_lens[b];
-  const int row0 = a.new_cu[b];
-  int n = a.new_cu[b + 1] - row0;
-  if (n > a.max_new) {
-    if (i == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
-    n = a.max_new;
-  }
-  const int64_t cap_tok = int64_t(a.bt_stride) * ps;
-  if (L_old < 0 || L_old > cap_tok) {
-    if (i == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
-    return;
-  }
-  if (L_old + int64_t(n) > cap_tok) {
-    if (i == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
-    n = int(cap_tok - L_old);
-  }
-  if (n <= 0) return;
-  const int L_new = L_old + n;
-  const int p = L_old / ps + i;
-  if (p > (L_new - 1) / ps) return;
   const int blk = a.bt[int64_t(b) * a.bt_stride + p];
   if (blk < 0 || blk >= a.num_blocks) {
     if (threadIdx.x == 0) flag(a.status, SA_DEV_BAD_BLOCK);
@@ -86,41 +109,36 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
   for (int idx = threadIdx.x; idx < H * C; idx += kAppendThreads) {
     const int h = idx / C, c = idx % C;
     const int64_t tile = (int64_t(blk) * H + h) * ps;    // first row of this (block, head)
-    float mn[8], mx[8];
-    double sm[8];
+    float mn[8], mx[8], sm[8];
+    bool exact[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) { mn[e] = INFINITY; mx[e] = -INFINITY; sm[e] = 0.0; }
+    for (int e = 0; e < 8; ++e) { mn[e] = INFINITY; mx[e] = -INFINITY; sm[e] = 0.f; exact[e] = true; }
     for (int s0 = 0; s0 < fill; s0 += kRowBatch) {
       uint4 r[kRowBatch];
 #pragma unroll
       for (int j = 0; j < kRowBatch; ++j) {
         const int s = s0 + j;
         if (s < fill) {
-          if (s >= s_new) {
-            const int64_t src = (int64_t(row0 + page_start + s - L_old) * H + h) * C + c;
-            r[j] = kn[src];
-          } else {
-            r[j] = kp[(tile + s) * C + c];
-          }
+          if (s >= s_new) r[j] = kn[(int64_t(row0 + page_start + s - L_old) * H + h) * C + c];
+          else r[j] = kp[(tile + s) * C + c];
         }
       }
 #pragma unroll
       for (int j = 0; j < kRowBatch; ++j) {
-        const int s = s0 + j;
-        if (s < fill) {
+        if (s0 + j < fill) {
           const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float x0 = E::lo(w[e]), x1 = E::hi(w[e]);
             mn[2 * e] = fminf(mn[2 * e], x0); mn[2 * e + 1] = fminf(mn[2 * e + 1], x1);
             mx[2 * e] = fmaxf(mx[2 * e], x0); mx[2 * e + 1] = fmaxf(mx[2 * e + 1], x1);
-            sm[2 * e] += double(x0); sm[2 * e + 1] += double(x1);
+            two_sum(sm[2 * e], x0, exact[2 * e]);
+            two_sum(sm[2 * e + 1], x1, exact[2 * e + 1]);
           }
         }
       }
-      // write the new rows (keys from registers, values copied)
 #pragma unroll
-      for (int j = 0; j < kRowBatch; ++j) {
+      for (int j = 0; j < kRowBatch; ++j) {                // the new rows go to the pool
         const int s = s0 + j;
         if (s < fill && s >= s_new) {
           const int64_t src = (int64_t(row0 + page_start + s - L_old) * H + h) * C + c;
@@ -129,23 +147,40 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
         }
       }
     }
-    if (a.meta) {
-      uint4* m = static_cast<uint4*>(a.meta) + (int64_t(blk) * H + h) * 3 * C + c;
-      const double f = double(fill);
-      uint32_t w0[4], w1[4], w2[4];
+    if (!a.meta) continue;
+    uint16_t me[8];
+    bool slow = false;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        w0[e] = E::pack(mn[2 * e], mn[2 * e + 1]);       // exact: values are already dtype
-        w1[e] = E::pack(mx[2 * e], mx[2 * e + 1]);
-        w2[e] = uint32_t(E::from_f64(sm[2 * e] / f)) |
-                (uint32_t(E::from_f64(sm[2 * e + 1] / f)) << 16);
-      }
-      m[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-      m[C] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-      m[2 * C] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+    for (int e = 0; e < 8; ++e) {
+      if (!exact[e] || !mean_f32<T>(sm[e], fill, me[e])) { exact[e] = false; slow = true; }
     }
+    if (slow) {                                           // rare: float64 from the pool rows
+      double sd[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sd[e] = 0.0;
+      for (int s = 0; s < fill; ++s) {
+        const uint4 x = kp[(tile + s) * C + c];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { sd[2 * e] += double(E::lo(w[e])); sd[2 * e + 1] += double(E::hi(w[e])); }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (!exact[e]) me[e] = E::from_f64(sd[e] / double(fill));
+    }
+    uint4* m = static_cast<uint4*>(a.meta) + (int64_t(blk) * H + h) * 3 * C + c;
+    uint32_t w0[4], w1[4], w2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      w0[e] = E::pack(mn[2 * e], mn[2 * e + 1]);         // exact: values are already dtype
+      w1[e] = E::pack(mx[2 * e], mx[2 * e + 1]);
+      w2[e] = uint32_t(me[2 * e]) | (uint32_t(me[2 * e + 1]) << 16);
+    }
+    m[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+    m[C] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+    m[2 * C] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
   }
-  // H2O slots of the written tokens start at zero.
+  // H2O slots of the written tokens start at zero
   if (a.hh) {
     for (int idx = threadIdx.x; idx < (fill - s_new) * H; idx += kAppendThreads) {
       const int s = s_new + idx / H, h = idx % H;
@@ -157,13 +192,65 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
     for (int idx = threadIdx.x; idx < (fill - s_new) * H; idx += kAppendThreads) {
       const int s = s_new + idx / H, h = idx % H;
       const int pos = page_start + s;
-      const int c = a.ret_cnt[b * H + h] + (pos - L_old);
-      if (c < 0 || c >= a.ret_cap) {
+      const int cpos = a.ret_cnt[b * H + h] + (pos - L_old);
+      if (cpos < 0 || cpos >= a.ret_cap) {
         flag(a.status, SA_DEV_OVERFLOW);
         continue;
       }
-      a.ret_pos[(int64_t(b) * H + h) * a.ret_cap + c] = pos;
+      a.ret_pos[(int64_t(b) * H + h) * a.ret_cap + cpos] = pos;
     }
+  }
+}
+
+// Clamp request b's new-token count; returns false if nothing is appended.
+__device__ __forceinline__ bool plan(const AppendArgs& a, int b, bool report, int& L_old, int& n,
+                                     int& row0) {
+  L_old = a.seq_lens[b];
+  row0 = a.new_cu[b];
+  n = a.new_cu[b + 1] - row0;
+  if (n > a.max_new) {
+    if (report) flag(a.status, SA_DEV_OVERFLOW);
+    n = a.max_new;
+  }
+  const int64_t cap_tok = int64_t(a.bt_stride) * a.ps;
+  if (L_old < 0 || L_old > cap_tok) {
+    if (report) flag(a.status, SA_DEV_OVERFLOW);
+    return false;
+  }
+  if (L_old + int64_t(n) > cap_tok) {
+    if (report) flag(a.status, SA_DEV_OVERFLOW);
+    n = int(cap_tok - L_old);
+  }
+  return n > 0;
+}
+
+// Grid (touched pages, B); lengths advanced by advance_kernel afterwards.
+template <typename T>
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
+  const int b = blockIdx.y, i = blockIdx.x;
+  int L_old, n, row0;
+  if (!plan(a, b, i == 0 && threadIdx.x == 0, L_old, n, row0)) return;
+  const int p = L_old / a.ps + i;
+  if (p > (L_old + n - 1) / a.ps) return;
+  refresh_page<T>(a, b, p, L_old, L_old + n, row0);
+}
+
+// Grid (B): a request's (at most two) pages, then its length, in one CTA.
+template <typename T>
+__global__ void __launch_bounds__(kAppendThreads) append_fused_kernel(AppendArgs a) {
+  const int b = blockIdx.x;
+  int L_old, n, row0;
+  const bool any = plan(a, b, threadIdx.x == 0, L_old, n, row0);
+  if (any)
+    for (int p = L_old / a.ps; p <= (L_old + n - 1) / a.ps; ++p)
+      refresh_page<T>(a, b, p, L_old, L_old + n, row0);
+  __syncthreads();                                          // every read of the old length is done
+  if (any && threadIdx.x < a.H) {
+    if (a.ret_cnt) {
+      const int c = a.ret_cnt[b * a.H + threadIdx.x] + n;
+      a.ret_cnt[b * a.H + threadIdx.x] = min(max(c, 0), a.ret_cap);
+    }
+    if (threadIdx.x == 0) a.seq_lens[b] = L_old + n;
   }
 }
 
@@ -201,6 +288,7 @@ extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, 
   if (!k_new || !v_new || !new_cu || max_new_per_req < 0) return SA_ERR_INVALID_ARG;
   if ((ret_pos == nullptr) != (ret_cnt == nullptr)) return SA_ERR_INVALID_ARG;
   if (ret_pos && ret_cap <= 0) return SA_ERR_INVALID_ARG;
+  if (cache->num_kv_heads > kAppendThreads) return SA_ERR_UNSUPPORTED;
   if (max_new_per_req == 0) return SA_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   AppendArgs a;
@@ -212,13 +300,17 @@ extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, 
   a.H = cache->num_kv_heads; a.D = cache->head_dim; a.ps = cache->page_size;
   a.num_blocks = cache->num_blocks; a.bt_stride = batch->bt_stride;
   a.max_new = max_new_per_req; a.ret_cap = ret_pos ? ret_cap : 0;
+  const bool bf = cache->dtype == SA_BF16;
+  if (max_new_per_req <= a.ps) {                            // touches at most two pages per request
+    if (bf) append_fused_kernel<__nv_bfloat16><<<batch->batch, kAppendThreads, 0, s>>>(a);
+    else append_fused_kernel<__half><<<batch->batch, kAppendThreads, 0, s>>>(a);
+    return launch_status();
+  }
   const int64_t pages = (int64_t(max_new_per_req) + a.ps - 1) / a.ps + 1;
   if (pages > 0x7fffffff) return SA_ERR_INVALID_ARG;
   dim3 grid(unsigned(pages), unsigned(batch->batch));
-  if (cache->dtype == SA_BF16)
-    append_kernel<__nv_bfloat16><<<grid, kAppendThreads, 0, s>>>(a);
-  else
-    append_kernel<__half><<<grid, kAppendThreads, 0, s>>>(a);
+  if (bf) append_kernel<__nv_bfloat16><<<grid, kAppendThreads, 0, s>>>(a);
+  else append_kernel<__half><<<grid, kAppendThreads, 0, s>>>(a);
   if ((st = launch_status()) != SA_OK) return st;
   advance_kernel<<<1, 256, 0, s>>>(batch->seq_lens, new_cu, ret_cnt, batch->batch, a.H,
                                    max_new_per_req, int64_t(batch->bt_stride) * a.ps, a.ret_cap);

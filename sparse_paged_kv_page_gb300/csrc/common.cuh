@@ -75,6 +75,14 @@ struct Elem<__nv_bfloat16> {
     return __bfloat16_as_ushort(__float2bfloat16_rn(a));
   }
   static __device__ __forceinline__ uint16_t from_f64(double x) { return round_f64<8, -126, 127>(x); }
+  static __device__ __forceinline__ uint16_t from_f_rz(float a) {
+    return __bfloat16_as_ushort(__float2bfloat16_rz(a));
+  }
+  // 1: a float32 q lies exactly half-way between two bf16 values; 0: it does not;
+  // -1: not decidable here (outside the range handled in float32).
+  static __device__ __forceinline__ int midpoint(float q) {
+    return (__float_as_uint(q) & 0xffffu) == 0x8000u ? 1 : 0;
+  }
   static __device__ __forceinline__ void mma(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
@@ -102,6 +110,14 @@ struct Elem<__half> {
     return __half_as_ushort(__float2half_rn(a));
   }
   static __device__ __forceinline__ uint16_t from_f64(double x) { return round_f64<11, -14, 15>(x); }
+  static __device__ __forceinline__ uint16_t from_f_rz(float a) {
+    return __half_as_ushort(__float2half_rz(a));
+  }
+  static __device__ __forceinline__ int midpoint(float q) {
+    const float aq = fabsf(q);
+    if (!(aq >= 0x1p-14f && aq <= 65504.f)) return -1;          // fp16 subnormal / overflow range
+    return (__float_as_uint(q) & 0x1fffu) == 0x1000u ? 1 : 0;
+  }
   static __device__ __forceinline__ void mma(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
@@ -200,6 +216,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// 2-D tiled TMA load (tensor map in kernel-parameter space), completion on `bar`.
+// x (innermost coordinate) * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// Order this thread's generic-proxy shared-memory accesses before later async-proxy (TMA) ones.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------

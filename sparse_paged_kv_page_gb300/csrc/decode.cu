@@ -12,26 +12,42 @@
 // selection order (row i = entry i / page_size, slot i % page_size), so a
 // 16-token page is one tile and page_size 1 gathers 16 retained tokens.
 // Grid (nsplit, H_kv, B): CTA `split` of a unit takes an equal share of the
-// unit's tiles, counted on the device from sel_cnt. Its 4 warps take tiles
-// round robin, each with a private 3-stage cp.async ring (16-byte copies into
-// an XOR-swizzled tile so ldmatrix reads are bank-conflict free; rows past a
-// page's fill are zero-filled, never read). Per tile a warp computes
-// S = Q K^T with mma.sync m16n8k16 (rows = the G query heads, padded to 16;
-// columns = the 16 tokens), applies scale and mask, runs the online softmax in
-// float32 (exp2 domain), reuses P's accumulator registers as the A operand of
-// O += P V (second mma.sync), and at the end the 4 warps merge in shared
-// memory. Each CTA writes its partial (o_s, lse_s) to the workspace; the last
-// CTA of the unit to finish (atomic ticket) merges the partials exactly and
-// writes out / lse, then resets the ticket. No CTA waits on another.
+// unit's tiles, counted on the device from sel_cnt, and first resolves the
+// selection entries it touches to (block, fill) in shared memory. Its 4 warps
+// take tiles round robin, each with a private ring of stages:
+//  * page_size >= 16: a tile is 16 contiguous rows of one (block, head), so
+//    the TMA engine fetches it through a 2-D tensor map over all pool rows
+//    (cp.async.bulk.tensor, 64-column boxes, 128-byte swizzle), completion
+//    on the stage's mbarrier; slots past a page's fill are masked, and the
+//    stale V rows of a partial page are zeroed in shared memory;
+//  * page_size < 16: rows come from different pages, gathered with 16-byte
+//    cp.async (zero-fill for invalid rows) into the same swizzled layout.
+// Per tile a warp computes S = Q K^T with mma.sync m16n8k16 (rows = the G
+// query heads, padded to 16; columns = the 16 tokens), applies scale and mask,
+// runs the online softmax in float32 (exp2 domain), reuses P's accumulator
+// registers as the A operand of O += P V, and at the end the 4 warps merge in
+// shared memory. Each CTA writes its partial (o_s, lse_s) to the workspace; the
+// last CTA of the unit to finish (atomic ticket) merges the partials exactly,
+// writes out / lse and resets the ticket. No CTA waits on another; every
+// mbarrier wait is time-bounded.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "host.h"
 
 namespace sa {
 namespace {
 
+#ifndef SA_DECODE_STAGES
+#define SA_DECODE_STAGES 3
+#endif
+#ifndef SA_DECODE_CTAS_PER_SM
+#define SA_DECODE_CTAS_PER_SM 2
+#endif
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = SA_DECODE_STAGES;
+constexpr int kCtasPerSm = SA_DECODE_CTAS_PER_SM;
 constexpr int kMaxSplit = 64;
 constexpr int kMaxEnt = 4096;          // (block, fill) entries staged per CTA
 constexpr float kLog2e = 1.4426950408889634f;
@@ -57,30 +73,38 @@ struct DecodeArgs {
   float scale, scale_log2;
 };
 
+// Shared-memory tile of 16 rows x D columns (2-byte elements): 64-column
+// halves of 16 x 128 bytes, each 16-byte chunk c of row r stored at chunk
+// position c ^ (r & 7) -- the TMA 128-byte swizzle, so 8 rows read at one
+// column hit 8 different bank groups.
 template <int D>
 struct Tile {
-  static constexpr int kRowBytes = D * 2;
-  static constexpr int kBytes = 16 * kRowBytes;      // one 16-row K (or V) tile
+  static constexpr int kHalves = D / 64;
+  static constexpr int kBytes = 16 * D * 2;          // one K (or V) tile
   static constexpr int kChunks = D / 8;              // 16-byte chunks per row
-  static constexpr int kRowsPerOp = 32 / kChunks;    // rows one warp-wide copy covers
-  static constexpr int kOps = 16 / kRowsPerOp;       // copies per lane per tile
+  static constexpr int kRowsPerOp = 32 / kChunks;    // rows one warp-wide cp.async covers
+  static constexpr int kOps = 16 / kRowsPerOp;       // cp.async per lane per tile
   static constexpr int kStageBytes = 2 * kBytes;     // K + V
-  static constexpr int kSmem = kWarps * kStages * kStageBytes;
+  static constexpr int kSmem = kWarps * kStages * kStageBytes + 1024;   // + alignment slack
 };
 
-// byte offset of (row, chunk) inside a swizzled tile
 template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return uint32_t(row * Tile<D>::kRowBytes + ((chunk ^ (row & 7)) << 4));
+  return uint32_t((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
+template <typename T, int D, bool kTma>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv) {
   using E = Elem<T>;
   using TL = Tile<D>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ uint32_t s_mask[kWarps][kStages];
+  __shared__ __align__(8) uint64_t s_bar[kWarps][kStages];
   __shared__ int s_last;
+  // 1024-byte aligned base for the swizzled tiles
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -99,12 +123,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   const int n_pages_req = L > 0 ? (L + ps - 1) >> pss : 0;
   const int32_t* sel = a.sel + int64_t(unit) * a.sel_stride;
   const int32_t* btb = a.bt + int64_t(b) * a.bt_stride;
-  const T* kbase = static_cast<const T*>(a.k);
-  const T* vbase = static_cast<const T*>(a.v);
 
   // Prologue: resolve the selection entries this CTA touches to (block, fill)
   // once, in parallel, so the copy loop never waits on sel -> block table.
-  int2* s_ent = reinterpret_cast<int2*>(smem + TL::kSmem);
+  int2* s_ent = reinterpret_cast<int2*>(smem_raw + TL::kSmem);
   const int row_begin = t_begin << 4, row_end = min(t_end << 4, n_rows);
   const int e_begin = row_begin >> pss;
   const int e_cnt = row_end > row_begin ? min(((row_end - 1) >> pss) - e_begin + 1, a.ent_max) : 0;
@@ -121,6 +143,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
       else blk = x;
     }
     s_ent[i] = make_int2(blk, fill);
+  }
+  if (kTma && threadIdx.x == 0) {
+    for (int w = 0; w < kWarps; ++w)
+      for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&s_bar[w][s]), 1);
+    mbar_init_fence();
   }
   __syncthreads();
 
@@ -148,56 +175,104 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   uint8_t* wbuf = smem + warp * kStages * TL::kStageBytes;
   const int nt = t_begin + warp < t_end ? (t_end - t_begin - warp + kWarps - 1) / kWarps : 0;
 
-  // Issue the copies of this warp's i-th tile into stage st.
+  // Start the copies of this warp's i-th tile into stage st.
   auto issue = [&](int i, int st) {
     const int t = t_begin + warp + i * kWarps;
-    int64_t off = 0;
-    bool valid = false;
-    if (lane < 16) {
-      const int j = (t << 4) + lane;
-      const int ei = (j >> pss) - e_begin, s = j & (ps - 1);
-      if (j < row_end && ei < e_cnt) {
-        const int2 en = s_ent[ei];
-        if (en.x >= 0 && s < en.y) {
-          valid = true;
-          off = ((int64_t(en.x) * a.H_kv + h) * ps + s) * D;
-        }
-      }
-    }
-    const uint32_t vmask = __ballot_sync(kFull, valid) & 0xffffu;
-    if (lane == 0) s_mask[warp][st] = vmask;
     const uint32_t sk = smem_u32(wbuf + st * TL::kStageBytes);
     const uint32_t sv = sk + TL::kBytes;
-    const int chunk = lane % TL::kChunks;
+    if constexpr (kTma) {
+      // one (block, head) row range: 16 rows starting at slot s0 of entry e
+      const int j0 = t << 4;
+      const int ei = (j0 >> pss) - e_begin, s0 = j0 & (ps - 1);
+      int y = 0, nvalid = 0;
+      if (j0 < row_end && ei < e_cnt) {
+        const int2 en = s_ent[ei];
+        if (en.x >= 0 && s0 < en.y) {
+          nvalid = min(16, en.y - s0);
+          y = int((int64_t(en.x) * a.H_kv + h) * ps + s0);
+        }
+      }
+      const uint32_t vmask = nvalid >= 16 ? 0xffffu : ((1u << nvalid) - 1u);
+      if (lane == 0) {
+        s_mask[warp][st] = vmask;
+        const uint32_t bar = smem_u32(&s_bar[warp][st]);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, vmask ? uint32_t(2 * TL::kBytes) : 0u);
+        if (vmask) {
 #pragma unroll
-    for (int r0 = 0; r0 < TL::kOps; ++r0) {
-      const int row = lane / TL::kChunks + r0 * TL::kRowsPerOp;
-      const int lo = __shfl_sync(kFull, int(uint64_t(off) & 0xffffffffu), row);
-      const int hi = __shfl_sync(kFull, int(uint64_t(off) >> 32), row);
-      const int64_t ro = int64_t((uint64_t(uint32_t(hi)) << 32) | uint32_t(lo));
-      const bool rv = (vmask >> row) & 1u;
-      const uint32_t d = swz<D>(row, chunk);
-      cp_async_16(sk + d, rv ? static_cast<const void*>(kbase + ro + chunk * 8) : a.k, rv ? 16 : 0);
-      cp_async_16(sv + d, rv ? static_cast<const void*>(vbase + ro + chunk * 8) : a.v, rv ? 16 : 0);
+          for (int hf = 0; hf < TL::kHalves; ++hf) {
+            tma_load_2d(sk + hf * 2048, &tmk, hf * 64, y, bar);
+            tma_load_2d(sv + hf * 2048, &tmv, hf * 64, y, bar);
+          }
+        }
+      }
+    } else {
+      int64_t off = 0;
+      bool valid = false;
+      if (lane < 16) {
+        const int j = (t << 4) + lane;
+        const int ei = (j >> pss) - e_begin, s = j & (ps - 1);
+        if (j < row_end && ei < e_cnt) {
+          const int2 en = s_ent[ei];
+          if (en.x >= 0 && s < en.y) {
+            valid = true;
+            off = ((int64_t(en.x) * a.H_kv + h) * ps + s) * D;
+          }
+        }
+      }
+      const uint32_t vmask = __ballot_sync(kFull, valid) & 0xffffu;
+      if (lane == 0) s_mask[warp][st] = vmask;
+      const T* kbase = static_cast<const T*>(a.k);
+      const T* vbase = static_cast<const T*>(a.v);
+      const int chunk = lane % TL::kChunks;
+#pragma unroll
+      for (int r0 = 0; r0 < TL::kOps; ++r0) {
+        const int row = lane / TL::kChunks + r0 * TL::kRowsPerOp;
+        const int lo = __shfl_sync(kFull, int(uint64_t(off) & 0xffffffffu), row);
+        const int hi = __shfl_sync(kFull, int(uint64_t(off) >> 32), row);
+        const int64_t ro = int64_t((uint64_t(uint32_t(hi)) << 32) | uint32_t(lo));
+        const bool rv = (vmask >> row) & 1u;
+        const uint32_t d = swz<D>(row, chunk);
+        cp_async_16(sk + d, rv ? static_cast<const void*>(kbase + ro + chunk * 8) : a.k, rv ? 16 : 0);
+        cp_async_16(sv + d, rv ? static_cast<const void*>(vbase + ro + chunk * 8) : a.v, rv ? 16 : 0);
+      }
     }
   };
 
+  bool alive = true;
 #pragma unroll
   for (int i = 0; i < kStages - 1; ++i) {
     if (i < nt) issue(i, i);
-    cp_async_commit();
+    if constexpr (!kTma) cp_async_commit();
   }
-  for (int i = 0; i < nt; ++i) {
+  for (int i = 0; i < nt && alive; ++i) {
     const int nxt = i + kStages - 1;
-    if (nxt < nt) issue(nxt, nxt % kStages);
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
     __syncwarp();
+    if (nxt < nt) issue(nxt, nxt % kStages);
     const int st = i % kStages;
+    if constexpr (kTma) {
+      if (!mbar_wait(smem_u32(&s_bar[warp][st]), (i / kStages) & 1, a.status)) { alive = false; break; }
+    } else {
+      cp_async_commit();
+      cp_async_wait<kStages - 1>();
+    }
+    __syncwarp();
     const int t = t_begin + warp + i * kWarps;
     const uint32_t sk = smem_u32(wbuf + st * TL::kStageBytes);
     const uint32_t sv = sk + TL::kBytes;
     const uint32_t vmask = s_mask[warp][st];
+    if (vmask == 0) continue;
+    if (kTma && vmask != 0xffffu) {
+      // a partial page: its stale V rows could hold anything (NaN) -- zero them
+      for (int idx = lane; idx < 16 * TL::kChunks; idx += 32) {
+        const int row = idx / TL::kChunks, chunk = idx % TL::kChunks;
+        if (!((vmask >> row) & 1u))
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(sv + swz<D>(row, chunk)), "r"(0u)
+                       : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
 
     // S = Q K^T   (c[ntile][.]: rows g / g+8, tokens ntile*8 + 2tq + {0,1})
     float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -268,9 +343,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
         E::mma(o[2 * nd + 1], pa, r[2], r[3]);
       }
     }
-    __syncwarp();
   }
-  cp_async_wait<0>();
+  if constexpr (kTma) {
+    // never leave with copies in flight (bounded): drain this warp's issued stages
+    if (lane == 0 && !alive) {
+      for (int i = 0; i < nt; ++i)
+        if (!mbar_wait(smem_u32(&s_bar[warp][i % kStages]), (i / kStages) & 1, a.status)) break;
+    }
+  } else {
+    cp_async_wait<0>();
+  }
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     l_r[r] += __shfl_xor_sync(kFull, l_r[r], 1);
@@ -279,10 +361,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   __syncthreads();
 
   // merge the 4 warps in shared memory (reusing the tile buffers)
+  constexpr int WS = D + 4;                                    // padded row: no bank conflicts
   float* wm = reinterpret_cast<float*>(smem);                 // [kWarps][16]
   float* wl = wm + kWarps * 16;                                // [kWarps][16]
-  float* wo = wl + kWarps * 16;                                // [kWarps][G][D + 4]
-  constexpr int WS = D + 4;                                    // padded row: no bank conflicts
+  float* wo = wl + kWarps * 16;                                // [kWarps][G][WS]
   if (tq == 0) {
     if (g < G) { wm[warp * 16 + g] = m_r[0]; wl[warp * 16 + g] = l_r[0]; }
     if (g + 8 < G) { wm[warp * 16 + g + 8] = m_r[1]; wl[warp * 16 + g + 8] = l_r[1]; }
@@ -400,11 +482,11 @@ int num_sms() {
   return sms[dev];
 }
 
-// Splits per (request, KV head): one wave of two CTAs per SM, at most one
-// split per tile, and enough splits that a CTA's entry table stays small.
+// Splits per (request, KV head): one wave of resident CTAs, at most one split
+// per tile, and enough splits that a CTA's entry table stays small.
 int choose_nsplit(int units, int max_tiles, int ps, int sms) {
-  const int target = 2 * sms;
-  int s = (target + units - 1) / units;
+  const int target = kCtasPerSm * sms;
+  int s = target / units;
   const int64_t ent_total = (int64_t(max_tiles) * 16 + ps - 1) / ps;
   const int need = int((ent_total + kMaxEnt - 1) / kMaxEnt);
   if (s < need) s = need;
@@ -433,15 +515,61 @@ WsLayout ws_layout(int units, int G, int D, int nsplit) {
   return w;
 }
 
-int g_dec_smem[4][64];
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
 
-template <typename T, int D>
-sa_status launch_decode(const DecodeArgs& a, dim3 grid, cudaStream_t s, int* cache) {
-  auto k = decode_kernel<T, D>;
+// Tensor map over every pool row: [rows = num_blocks * H * page_size, D], box 16 x 64, 128-byte swizzle.
+bool make_pool_map(CUtensorMap* m, const void* base, const sa_cache* c) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t rows = cuuint64_t(c->num_blocks) * c->num_kv_heads * c->page_size;
+  if (rows >= (cuuint64_t(1) << 31)) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(c->head_dim), rows};
+  const cuuint64_t strides[1] = {cuuint64_t(c->head_dim) * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_dec_smem[8][64];
+
+template <typename T, int D, bool kTma>
+sa_status launch_decode(const DecodeArgs& a, dim3 grid, cudaStream_t s, const CUtensorMap& mk,
+                        const CUtensorMap& mv, int* cache) {
+  auto k = decode_kernel<T, D, kTma>;
   const int smem = Tile<D>::kSmem + a.ent_max * int(sizeof(int2));
   if (!ensure_smem(k, smem, cache)) return SA_ERR_CUDA;
-  k<<<grid, kThreads, smem, s>>>(a);
+  k<<<grid, kThreads, smem, s>>>(a, mk, mv);
   return launch_status();
+}
+
+template <typename T, int D>
+sa_status dispatch_tma(const DecodeArgs& a, dim3 grid, cudaStream_t s, const sa_cache* c, int slot) {
+  CUtensorMap mk, mv;
+  if (c->page_size >= 16 && make_pool_map(&mk, c->k, c) && make_pool_map(&mv, c->v, c))
+    return launch_decode<T, D, true>(a, grid, s, mk, mv, g_dec_smem[2 * slot]);
+  memset(&mk, 0, sizeof(mk));
+  memset(&mv, 0, sizeof(mv));
+  return launch_decode<T, D, false>(a, grid, s, mk, mv, g_dec_smem[2 * slot + 1]);
 }
 
 }  // namespace
@@ -509,8 +637,8 @@ extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* bat
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = cache->dtype == SA_BF16;
   if (cache->head_dim == 128)
-    return bf ? launch_decode<__nv_bfloat16, 128>(a, grid, s, g_dec_smem[0])
-              : launch_decode<__half, 128>(a, grid, s, g_dec_smem[1]);
-  return bf ? launch_decode<__nv_bfloat16, 64>(a, grid, s, g_dec_smem[2])
-            : launch_decode<__half, 64>(a, grid, s, g_dec_smem[3]);
+    return bf ? dispatch_tma<__nv_bfloat16, 128>(a, grid, s, cache, 0)
+              : dispatch_tma<__half, 128>(a, grid, s, cache, 1);
+  return bf ? dispatch_tma<__nv_bfloat16, 64>(a, grid, s, cache, 2)
+            : dispatch_tma<__half, 64>(a, grid, s, cache, 3);
 }

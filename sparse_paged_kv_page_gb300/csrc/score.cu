@@ -31,10 +31,20 @@
 namespace sa {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+#ifndef SA_SCORE_CONSUMER_WARPS
+#define SA_SCORE_CONSUMER_WARPS 4
+#endif
+#ifndef SA_SCORE_STAGES
+#define SA_SCORE_STAGES 4
+#endif
+#ifndef SA_SCORE_CTAS_PER_SM
+#define SA_SCORE_CTAS_PER_SM 2
+#endif
+constexpr int kConsumerWarps = SA_SCORE_CONSUMER_WARPS;
 constexpr int kScThreads = 32 * (kConsumerWarps + 1);
 constexpr int kChunk = 32;                 // pages per stage (one per producer lane)
-constexpr int kStages = 4;
+constexpr int kStages = SA_SCORE_STAGES;
+constexpr int kCtasPerSm = SA_SCORE_CTAS_PER_SM;
 constexpr int kMaxBatch = 1024;
 
 struct ScoreArgs {
@@ -61,7 +71,7 @@ struct ChunkHdr {
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kScThreads, 2) score_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs a) {
   using E = Elem<T>;
   using TL = ScoreTile<D>;
   constexpr int LPP = D / 8;                               // lanes per page
@@ -71,6 +81,7 @@ __global__ void __launch_bounds__(kScThreads, 2) score_kernel(ScoreArgs a) {
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ ChunkHdr hdr[kStages];
   __shared__ int s_prefix[kMaxBatch + 1];                  // chunks before request b
+  __shared__ int s_pages[kMaxBatch];                       // pages of request b (clamped)
   __shared__ int scan_tmp[32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -91,6 +102,7 @@ __global__ void __launch_bounds__(kScThreads, 2) score_kernel(ScoreArgs a) {
       s_prefix[b] = run;
       int n = (a.seq_lens[b] + a.ps - 1) / a.ps;
       n = max(0, min(n, min(a.max_pages, a.bt_stride)));
+      s_pages[b] = n;
       run += a.H_kv * ((n + kChunk - 1) / kChunk);
     }
     if (tid == 0) s_prefix[a.B] = total;
@@ -122,25 +134,29 @@ __global__ void __launch_bounds__(kScThreads, 2) score_kernel(ScoreArgs a) {
         const int mid = (lo + hi) >> 1;
         if (s_prefix[mid] <= ci) lo = mid; else hi = mid;
       }
-      while (lo + 1 <= a.B && s_prefix[lo + 1] <= ci) ++lo;   // skip requests with no chunks
       b = lo;
-      int n = (a.seq_lens[b] + a.ps - 1) / a.ps;
-      n = max(0, min(n, min(a.max_pages, a.bt_stride)));
+      const int n = s_pages[b];
       const int kb = (n + kChunk - 1) / kChunk;
       const int r = ci - s_prefix[b];
       h = r / kb;
       p0 = (r % kb) * kChunk;
       count = min(kChunk, n - p0);
     };
-    int nb, nh, np0, ncount, nblk;
-    locate(c_begin, nb, nh, np0, ncount);
-    nblk = lane < ncount ? a.bt[int64_t(nb) * a.bt_stride + np0 + lane] : -1;
+    // block ids of the next two chunks are in flight while a stage is waited for
+    int b1, h1, p01, c1, k1 = -1, b2 = 0, h2 = 0, p02 = 0, c2 = 0, k2 = -1;
+    locate(c_begin, b1, h1, p01, c1);
+    k1 = lane < c1 ? a.bt[int64_t(b1) * a.bt_stride + p01 + lane] : -1;
+    if (c_begin + 1 < c_end) {
+      locate(c_begin + 1, b2, h2, p02, c2);
+      k2 = lane < c2 ? a.bt[int64_t(b2) * a.bt_stride + p02 + lane] : -1;
+    }
     bool ok = true;
     for (int ci = c_begin, it = 0; ci < c_end; ++ci, ++it) {
-      const int b = nb, h = nh, p0 = np0, count = ncount, blk = nblk;
-      if (ci + 1 < c_end) {                                // prefetch the next chunk's block ids
-        locate(ci + 1, nb, nh, np0, ncount);
-        nblk = lane < ncount ? a.bt[int64_t(nb) * a.bt_stride + np0 + lane] : -1;
+      const int b = b1, h = h1, p0 = p01, count = c1, blk = k1;
+      b1 = b2; h1 = h2; p01 = p02; c1 = c2; k1 = k2;
+      if (ci + 2 < c_end) {
+        locate(ci + 2, b2, h2, p02, c2);
+        k2 = lane < c2 ? a.bt[int64_t(b2) * a.bt_stride + p02 + lane] : -1;
       }
       const int s = it % kStages;
       if (it >= kStages && !mbar_wait(smem_u32(&empty_bar[s]), ((it / kStages) - 1) & 1, a.status)) {
@@ -281,7 +297,8 @@ extern "C" sa_status sa_score_pages(const sa_cache* cache, const sa_batch* batch
   // enough persistent CTAs for two per SM, never more than chunks could exist
   const int cap = max_pages < batch->bt_stride ? max_pages : batch->bt_stride;
   const int64_t max_chunks = int64_t(batch->batch) * a.H_kv * ((cap + kChunk - 1) / kChunk);
-  const int grid = int(max_chunks < 2 * sm_count() ? max_chunks : 2 * sm_count());
+  const int full = kCtasPerSm * sm_count();
+  const int grid = int(max_chunks < full ? max_chunks : full);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = cache->dtype == SA_BF16;
   if (cache->head_dim == 128)

@@ -18,7 +18,10 @@
 namespace sa {
 namespace {
 
-constexpr int kSelThreads = 1024;
+#ifndef SA_SELECT_THREADS
+#define SA_SELECT_THREADS 1024
+#endif
+constexpr int kSelThreads = SA_SELECT_THREADS;
 constexpr int kSelMaxPages = 49152;
 
 struct SelArgs {
@@ -62,7 +65,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   int remaining = kprime;                        // still to take among keys matching prefix
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    if (tid < 256) hist[tid] = 0;
+    for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
     __syncthreads();
     for (int i0 = 0; i0 < nc; i0 += kSelThreads) {           // warp-uniform trip count
       const int i = i0 + tid;
