@@ -167,7 +167,7 @@ sa_status sa_score_pages(const sa_cache* cache, const sa_batch* batch, const voi
  *   scores   [batch, num_kv_heads, max_pages] float32 (from sa_score_pages)
  *   sel_idx  [batch, num_kv_heads, topk] int32; entries past sel_cnt untouched
  *   sel_cnt  [batch, num_kv_heads] int32 = min(topk, n)
- * Limits: max_pages <= 49152 (the candidate keys of one (request, KV head)
+ * Limits: max_pages <= 45056 (the candidate keys of one (request, KV head)
  * are held in shared memory), else SA_ERR_UNSUPPORTED.
  */
 sa_status sa_select_topk(const float* scores, int32_t max_pages, const sa_batch* batch,

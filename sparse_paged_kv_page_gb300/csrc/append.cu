@@ -8,8 +8,8 @@
 // "EntmaxKV" README, "How it works": per-page key statistics refreshed on
 // append.
 //
-// One CTA per (touched page, request); thread (h, c) owns the 8 columns
-// [8c, 8c+8) of KV head h and loads all of the page's rows before using any,
+// One CTA per (touched page, request); thread (h, c) owns the column pair
+// [2c, 2c+1] of KV head h and loads all of the page's rows before using any,
 // taking new rows from the input and old ones from the pool, so no other
 // CTA's writes are read and a page costs one memory round trip per 16 rows.
 // Slots past the page's new fill are stale and never touched.
@@ -49,8 +49,8 @@ struct AppendArgs {
   int H, D, ps, num_blocks, bt_stride, max_new, ret_cap;
 };
 
-constexpr int kAppendThreads = 128;
-constexpr int kRowBatch = 16;     // rows of a page loaded per batch (independent 16-byte loads)
+constexpr int kAppendThreads = 512;
+constexpr int kRowBatch = 16;     // rows of a page loaded per batch (independent loads)
 
 // exact float32 sum step: s += x, clears `exact` if the addition rounded
 __device__ __forceinline__ void two_sum(float& s, float x, bool& exact) {
@@ -87,6 +87,7 @@ __device__ __forceinline__ bool mean_f32(float S, int f, uint16_t& out) {
 }
 
 // Recompute statistics of page p of request b (all heads) and write the new rows.
+// Thread (h, c) owns the column pair [2c, 2c+1] of KV head h.
 template <typename T>
 __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, int L_old, int L_new,
                                              int row0) {
@@ -100,24 +101,23 @@ __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, 
   const int page_start = p * ps;
   const int fill = min(ps, L_new - page_start);          // valid tokens after the append
   const int s_new = max(0, L_old - page_start);          // first slot written here
-  const int C = D / 8;                                    // 16-byte chunks per row
-  const uint4* kn = static_cast<const uint4*>(a.k_new);
-  const uint4* vn = static_cast<const uint4*>(a.v_new);
-  uint4* kp = static_cast<uint4*>(a.k);
-  uint4* vp = static_cast<uint4*>(a.v);
+  const int C = D / 2;                                    // column pairs per row
+  const uint32_t* kn = static_cast<const uint32_t*>(a.k_new);
+  const uint32_t* vn = static_cast<const uint32_t*>(a.v_new);
+  uint32_t* kp = static_cast<uint32_t*>(a.k);
+  uint32_t* vp = static_cast<uint32_t*>(a.v);
 
   for (int idx = threadIdx.x; idx < H * C; idx += kAppendThreads) {
     const int h = idx / C, c = idx % C;
     const int64_t tile = (int64_t(blk) * H + h) * ps;    // first row of this (block, head)
-    float mn[8], mx[8], sm[8];
-    bool exact[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) { mn[e] = INFINITY; mx[e] = -INFINITY; sm[e] = 0.f; exact[e] = true; }
+    float mn0 = INFINITY, mn1 = INFINITY, mx0 = -INFINITY, mx1 = -INFINITY, sm0 = 0.f, sm1 = 0.f;
+    bool ex0 = true, ex1 = true;
+    uint32_t r[kRowBatch];
     for (int s0 = 0; s0 < fill; s0 += kRowBatch) {
-      uint4 r[kRowBatch];
 #pragma unroll
       for (int j = 0; j < kRowBatch; ++j) {
         const int s = s0 + j;
+        r[j] = 0u;
         if (s < fill) {
           if (s >= s_new) r[j] = kn[(int64_t(row0 + page_start + s - L_old) * H + h) * C + c];
           else r[j] = kp[(tile + s) * C + c];
@@ -126,15 +126,11 @@ __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, 
 #pragma unroll
       for (int j = 0; j < kRowBatch; ++j) {
         if (s0 + j < fill) {
-          const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = E::lo(w[e]), x1 = E::hi(w[e]);
-            mn[2 * e] = fminf(mn[2 * e], x0); mn[2 * e + 1] = fminf(mn[2 * e + 1], x1);
-            mx[2 * e] = fmaxf(mx[2 * e], x0); mx[2 * e + 1] = fmaxf(mx[2 * e + 1], x1);
-            two_sum(sm[2 * e], x0, exact[2 * e]);
-            two_sum(sm[2 * e + 1], x1, exact[2 * e + 1]);
-          }
+          const float x0 = E::lo(r[j]), x1 = E::hi(r[j]);
+          mn0 = fminf(mn0, x0); mn1 = fminf(mn1, x1);
+          mx0 = fmaxf(mx0, x0); mx1 = fmaxf(mx1, x1);
+          two_sum(sm0, x0, ex0);
+          two_sum(sm1, x1, ex1);
         }
       }
 #pragma unroll
@@ -148,37 +144,29 @@ __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, 
       }
     }
     if (!a.meta) continue;
-    uint16_t me[8];
-    bool slow = false;
+    uint16_t me0 = 0, me1 = 0;
+    ex0 = ex0 && mean_f32<T>(sm0, fill, me0);
+    ex1 = ex1 && mean_f32<T>(sm1, fill, me1);
+    if (!ex0 || !ex1) {                                   // rare: float64
+      double d0 = 0.0, d1 = 0.0;
+      if (fill <= kRowBatch) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      if (!exact[e] || !mean_f32<T>(sm[e], fill, me[e])) { exact[e] = false; slow = true; }
-    }
-    if (slow) {                                           // rare: float64 from the pool rows
-      double sd[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sd[e] = 0.0;
-      for (int s = 0; s < fill; ++s) {
-        const uint4 x = kp[(tile + s) * C + c];
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) { sd[2 * e] += double(E::lo(w[e])); sd[2 * e + 1] += double(E::hi(w[e])); }
+        for (int j = 0; j < kRowBatch; ++j)
+          if (j < fill) { d0 += double(E::lo(r[j])); d1 += double(E::hi(r[j])); }
+      } else {
+        for (int s = 0; s < fill; ++s) {
+          const uint32_t x = kp[(tile + s) * C + c];
+          d0 += double(E::lo(x));
+          d1 += double(E::hi(x));
+        }
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (!exact[e]) me[e] = E::from_f64(sd[e] / double(fill));
+      if (!ex0) me0 = E::from_f64(d0 / double(fill));
+      if (!ex1) me1 = E::from_f64(d1 / double(fill));
     }
-    uint4* m = static_cast<uint4*>(a.meta) + (int64_t(blk) * H + h) * 3 * C + c;
-    uint32_t w0[4], w1[4], w2[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      w0[e] = E::pack(mn[2 * e], mn[2 * e + 1]);         // exact: values are already dtype
-      w1[e] = E::pack(mx[2 * e], mx[2 * e + 1]);
-      w2[e] = uint32_t(me[2 * e]) | (uint32_t(me[2 * e + 1]) << 16);
-    }
-    m[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-    m[C] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-    m[2 * C] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+    uint32_t* m = static_cast<uint32_t*>(a.meta) + (int64_t(blk) * H + h) * 3 * C + c;
+    m[0] = E::pack(mn0, mn1);                             // exact: values are already dtype
+    m[C] = E::pack(mx0, mx1);
+    m[2 * C] = uint32_t(me0) | (uint32_t(me1) << 16);
   }
   // H2O slots of the written tokens start at zero
   if (a.hh) {
@@ -288,7 +276,7 @@ extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, 
   if (!k_new || !v_new || !new_cu || max_new_per_req < 0) return SA_ERR_INVALID_ARG;
   if ((ret_pos == nullptr) != (ret_cnt == nullptr)) return SA_ERR_INVALID_ARG;
   if (ret_pos && ret_cap <= 0) return SA_ERR_INVALID_ARG;
-  if (cache->num_kv_heads > kAppendThreads) return SA_ERR_UNSUPPORTED;
+  if (cache->num_kv_heads > kAppendThreads) return SA_ERR_UNSUPPORTED;   // one thread per head for lengths
   if (max_new_per_req == 0) return SA_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   AppendArgs a;

@@ -124,6 +124,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int32_t* sel = a.sel + int64_t(unit) * a.sel_stride;
   const int32_t* btb = a.bt + int64_t(b) * a.bt_stride;
 
+  // Q as the A operand (rows = query heads of this KV head, zero beyond G)
+  const int g = lane >> 2, tq = lane & 3;
+  uint32_t qa[D / 16][4];
+  {
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+        static_cast<const T*>(a.q) + (int64_t(b) * a.H_q + int64_t(h) * G) * D);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int c0 = (kk * 16 + 2 * tq) >> 1, c1 = c0 + 4;
+      qa[kk][0] = g < G ? qp[g * (D / 2) + c0] : 0u;
+      qa[kk][1] = g + 8 < G ? qp[(g + 8) * (D / 2) + c0] : 0u;
+      qa[kk][2] = g < G ? qp[g * (D / 2) + c1] : 0u;
+      qa[kk][3] = g + 8 < G ? qp[(g + 8) * (D / 2) + c1] : 0u;
+    }
+  }
+
   // Prologue: resolve the selection entries this CTA touches to (block, fill)
   // once, in parallel, so the copy loop never waits on sel -> block table.
   int2* s_ent = reinterpret_cast<int2*>(smem_raw + TL::kSmem);
@@ -150,22 +166,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mbar_init_fence();
   }
   __syncthreads();
-
-  // Q as the A operand (rows = query heads of this KV head, zero beyond G)
-  const int g = lane >> 2, tq = lane & 3;
-  uint32_t qa[D / 16][4];
-  {
-    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
-        static_cast<const T*>(a.q) + (int64_t(b) * a.H_q + int64_t(h) * G) * D);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int c0 = (kk * 16 + 2 * tq) >> 1, c1 = c0 + 4;
-      qa[kk][0] = g < G ? qp[g * (D / 2) + c0] : 0u;
-      qa[kk][1] = g + 8 < G ? qp[(g + 8) * (D / 2) + c0] : 0u;
-      qa[kk][2] = g < G ? qp[g * (D / 2) + c1] : 0u;
-      qa[kk][3] = g + 8 < G ? qp[(g + 8) * (D / 2) + c1] : 0u;
-    }
-  }
 
   float o[D / 8][4];
 #pragma unroll
@@ -453,18 +453,45 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           t > 0.f ? rmax[row] + logf(t) : -INFINITY;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
-    const int row = idx / D, d = idx % D;
-    const float t = rtot[row];
-    float acc = 0.f;
-    if (t > 0.f) {
-      for (int s = 0; s < a.nsplit; ++s) {
-        const float w = wgt[s * G + row];
-        if (w != 0.f) acc += w * __ldcg(a.part_o + (pbase + int64_t(s) * G + row) * D + d);
-      }
-      acc /= t;
+  // every output element of the unit: sum over splits, loads issued 4 splits
+  // at a time for all of this thread's elements before any is used
+  constexpr int kOut = (16 * D) / kThreads;                    // elements per thread (G <= 16)
+  const int n_el = G * D;
+  float acc[kOut];
+#pragma unroll
+  for (int k = 0; k < kOut; ++k) acc[k] = 0.f;
+  for (int s0 = 0; s0 < a.nsplit; s0 += 4) {
+    float v[kOut][4];
+#pragma unroll
+    for (int k = 0; k < kOut; ++k) {
+      const int idx = threadIdx.x + k * kThreads;
+      const int row = idx / D, d = idx % D;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[k][u] = (idx < n_el && s0 + u < a.nsplit)
+                      ? __ldcg(a.part_o + (pbase + int64_t(s0 + u) * G + row) * D + d)
+                      : 0.f;
     }
-    reinterpret_cast<uint16_t*>(outp)[row * D + d] = E::from_f(acc);
+#pragma unroll
+    for (int k = 0; k < kOut; ++k) {
+      const int idx = threadIdx.x + k * kThreads;
+      const int row = (idx < n_el ? idx : 0) / D;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (s0 + u < a.nsplit) {
+          const float w = wgt[(s0 + u) * G + row];
+          if (w != 0.f) acc[k] += w * v[k][u];
+        }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kOut; ++k) {
+    const int idx = threadIdx.x + k * kThreads;
+    if (idx < n_el) {
+      const int row = idx / D, d = idx % D;
+      const float t = rtot[row];
+      reinterpret_cast<uint16_t*>(outp)[row * D + d] = E::from_f(t > 0.f ? acc[k] / t : 0.f);
+    }
   }
   if (threadIdx.x == 0) a.tickets[unit] = 0;
 }

@@ -201,8 +201,14 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
 #pragma unroll
       for (int e = 0; e < 8; ++e) ca[e] = cp[e] = cn[e] = 0.f;
       const T* qh = static_cast<const T*>(a.q) + (int64_t(cur_b) * a.H_q + int64_t(cur_h) * a.G) * D + l * 8;
-      for (int g = 0; g < a.G; ++g) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qh + int64_t(g) * D);
+      uint4 qv[16];
+#pragma unroll
+      for (int g = 0; g < 16; ++g)
+        qv[g] = g < a.G ? *reinterpret_cast<const uint4*>(qh + int64_t(g) * D) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int g = 0; g < 16; ++g) {
+        if (g >= a.G) break;
+        const uint4 v = qv[g];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

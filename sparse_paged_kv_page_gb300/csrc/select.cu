@@ -7,7 +7,7 @@
 //
 // One 1024-thread CTA per (KV head, request). Scores become order-preserving
 // 32-bit keys in shared memory; a most-significant-digit radix select
-// (4 passes of 8 bits, early exit once a digit bin is taken whole) finds the
+// (12-, 12- and 8-bit digits, early exit once a digit bin is taken whole) finds the
 // key K of the (topk-1)-th best candidate and how many candidates equal to K
 // to keep; those are the lowest-indexed ones. Two block-wide prefix sums in
 // page order then give each kept page its slot, so the output is ascending
@@ -22,7 +22,9 @@ namespace {
 #define SA_SELECT_THREADS 1024
 #endif
 constexpr int kSelThreads = SA_SELECT_THREADS;
-constexpr int kSelMaxPages = 49152;
+constexpr int kBpt = 4096 / kSelThreads;   // histogram bins owned per thread in the digit search
+static_assert(4096 % kSelThreads == 0, "threads must divide the 4096 bins");
+constexpr int kSelMaxPages = 45056;      // keys in shared memory next to a 16 KB histogram
 
 struct SelArgs {
   const float* scores;
@@ -35,7 +37,7 @@ struct SelArgs {
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   extern __shared__ uint32_t keys[];
-  __shared__ int hist[256];
+  __shared__ int hist[4096];
   __shared__ int scan_tmp[32];
   __shared__ int s_digit, s_above;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
@@ -59,51 +61,57 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     return;
   }
   const float* sc = a.scores + int64_t(unit) * a.max_pages;
-  for (int i = tid; i < nc; i += kSelThreads) keys[i] = f32_key(sc[i]);
+  for (int i0 = 0; i0 < nc; i0 += 8 * kSelThreads) {      // 8 independent loads per thread
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kSelThreads + tid;
+      v[u] = i < nc ? sc[i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kSelThreads + tid;
+      if (i < nc) keys[i] = f32_key(v[u]);
+    }
+  }
 
+  // Radix select from the most significant digit: 12, 12 and 8 bits. (The top
+  // byte of a float key is the sign and high exponent bits -- a 12-bit first
+  // digit also takes three mantissa bits, so the first pass already splits
+  // typical score distributions into many bins.)
   uint32_t prefix = 0, mask = 0;
   int remaining = kprime;                        // still to take among keys matching prefix
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+  for (int pass = 0; pass < 3; ++pass) {
+    const int width = pass < 2 ? 12 : 8;
+    const int shift = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
+    const int nbins = 1 << width;
+    for (int i = tid; i < nbins; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (int i0 = 0; i0 < nc; i0 += kSelThreads) {           // warp-uniform trip count
-      const int i = i0 + tid;
-      int bin = -1;
-      if (i < nc) {
-        const uint32_t k = keys[i];
-        if ((k & mask) == prefix) bin = int((k >> shift) & 255u);
-      }
-      warp_hist_add(hist, bin);
+    for (int i = tid; i < nc; i += kSelThreads) {
+      const uint32_t k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & uint32_t(nbins - 1)], 1);
     }
     __syncthreads();
-    if (tid < 32) {
-      // lane l owns digits 255-8l .. 248-8l, scanned from the largest digit down
-      int c[8], sum = 0;
+    // thread t owns bins nbins-1-kBpt*t-j (j < kBpt), i.e. scanned from the top
+    int c[kBpt], sum = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) { c[j] = hist[255 - 8 * tid - j]; sum += c[j]; }
-      int incl = sum;
+    for (int j = 0; j < kBpt; ++j) {
+      const int bin = nbins - 1 - kBpt * tid - j;
+      c[j] = bin >= 0 ? hist[bin] : 0;
+      sum += c[j];
+    }
+    int total;
+    int run = block_exclusive_scan<kSelThreads>(sum, scan_tmp, &total);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, incl, o);
-        if (tid >= o) incl += y;
-      }
-      int run = incl - sum, found = -1, above = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (found < 0 && run < remaining && remaining <= run + c[j]) { found = 255 - 8 * tid - j; above = run; }
-        run += c[j];
-      }
-      const unsigned m = __ballot_sync(kFull, found >= 0);
-      const int src = m ? __ffs(m) - 1 : 0;
-      const int d = __shfl_sync(kFull, found, src), ab = __shfl_sync(kFull, above, src);
-      if (tid == 0) { s_digit = d; s_above = ab; }
+    for (int j = 0; j < kBpt; ++j) {
+      if (run < remaining && remaining <= run + c[j]) { s_digit = nbins - 1 - kBpt * tid - j; s_above = run; }
+      run += c[j];
     }
     __syncthreads();
     const int d = s_digit;
     remaining -= s_above;
     prefix |= uint32_t(d) << shift;
-    mask |= 255u << shift;
+    mask |= uint32_t(nbins - 1) << shift;
     const bool whole = hist[d] == remaining;
     __syncthreads();                             // everyone has read hist before it is reset
     if (whole) break;

@@ -115,7 +115,7 @@ def test_select_bit_exact_on_generated_scores(kind, topk):
 
 def test_select_large_candidate_count():
     rng = np.random.default_rng(5)
-    B, H, maxp, ps = 1, 2, 49152, 16
+    B, H, maxp, ps = 1, 2, 45056, 16
     s = rng.standard_normal((B, H, maxp)).astype(np.float32)
     s[0, 1, 100:5000] = 0.25                          # a huge tie block at the boundary
     sel, cnt, st = _run_select(s, [maxp * ps], ps, 3000, H)
