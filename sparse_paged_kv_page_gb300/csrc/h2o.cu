@@ -217,7 +217,7 @@ extern "C" sa_status sa_h2o_update(const sa_batch* batch, int32_t num_kv_heads, 
   a.bt_stride = batch->bt_stride; a.logits_stride = logits_stride; a.num_slots = num_slots;
   a.cap = ret_cap; a.budget = budget; a.n_sink = n_sink; a.grace = grace; a.decay = decay;
   const int smem = ret_cap * 6 + 16;
-  if (smem > 48 * 1024 && !ensure_smem(h2o_kernel, smem, g_h2o_smem)) return SA_ERR_CUDA;
+  if (!ensure_smem(h2o_kernel, smem, g_h2o_smem)) return SA_ERR_CUDA;
   dim3 grid(unsigned(num_kv_heads), unsigned(batch->batch));
   h2o_kernel<<<grid, kH2oThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
   return launch_status();

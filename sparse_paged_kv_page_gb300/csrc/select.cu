@@ -171,7 +171,8 @@ extern "C" sa_status sa_select_topk(const float* scores, int32_t max_pages, cons
   a.status = dev_status; a.H = num_kv_heads; a.ps = page_size; a.max_pages = max_pages;
   a.topk = topk;
   const int smem = max_pages * int(sizeof(uint32_t));
-  if (smem > 48 * 1024 && !ensure_smem(select_kernel, smem, g_sel_smem)) return SA_ERR_CUDA;
+  // static shared memory (the 16 KB histogram) plus the keys may pass the 48 KB default
+  if (!ensure_smem(select_kernel, smem, g_sel_smem)) return SA_ERR_CUDA;
   dim3 grid(unsigned(num_kv_heads), unsigned(batch->batch));
   select_kernel<<<grid, kSelThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
   return launch_status();
