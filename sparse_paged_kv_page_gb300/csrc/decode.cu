@@ -277,15 +277,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // S = Q K^T   (c[ntile][.]: rows g / g+8, tokens ntile*8 + 2tq + {0,1})
     float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     {
+      // even and odd k-steps accumulate separately: two dependency chains of D/32
+      float c2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       const int mi = lane >> 3, rr = lane & 7;
       const int tok = (mi >> 1) * 8 + rr;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t r[4];
+      for (int kk = 0; kk < D / 16; kk += 2) {
+        uint32_t r[4], r2[4];
         ldmatrix_x4(r, sk + swz<D>(tok, kk * 2 + (mi & 1)));
+        ldmatrix_x4(r2, sk + swz<D>(tok, (kk + 1) * 2 + (mi & 1)));
         E::mma(c[0], qa[kk], r[0], r[1]);
         E::mma(c[1], qa[kk], r[2], r[3]);
+        E::mma(c2[0], qa[kk + 1], r2[0], r2[1]);
+        E::mma(c2[1], qa[kk + 1], r2[2], r2[3]);
       }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) { c[0][x] += c2[0][x]; c[1][x] += c2[1][x]; }
     }
     // scale, mask, logits, online softmax
     float pmax[2] = {-INFINITY, -INFINITY};
@@ -669,3 +676,4 @@ extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* bat
   return bf ? dispatch_tma<__nv_bfloat16, 64>(a, grid, s, cache, 2)
             : dispatch_tma<__half, 64>(a, grid, s, cache, 3);
 }
+
