@@ -225,6 +225,36 @@ sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* batch, const v
                            size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * sa_sparse_decode_noalloc -- sa_sparse_decode without a caller workspace.
+ *
+ * No counterpart on the pages: this is an integration convenience. Some
+ * callers cannot allocate device memory where they call the decode -- a plugin
+ * handed fixed buffers by a host engine, a runtime whose memory plan is frozen
+ * after start-up, a real-time loop that must never enter the allocator. This
+ * entry point allocates nothing: the split partials and tickets live in one
+ * fixed device array inside the library, of sa_sparse_decode_noalloc_capacity()
+ * bytes (4 MiB), which every GPU that loads the library keeps until the
+ * process exits. Arguments, layouts and results are those of
+ * sa_sparse_decode; the caller still passes every input and output.
+ *   - A call whose sizes need more scratch than the capacity (see
+ *     sa_decode_workspace_size) returns SA_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call resets the tickets it uses with cudaMemsetAsync on `stream`.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race and corrupt each other's results; order
+ *     them on one stream.
+ */
+sa_status sa_sparse_decode_noalloc(const sa_cache* cache, const sa_batch* batch, const void* q,
+                                   int32_t num_q_heads, const int32_t* sel_idx,
+                                   const int32_t* sel_cnt, int32_t sel_stride, float scale,
+                                   void* out, float* lse, float* logits, int32_t logits_stride,
+                                   int32_t* dev_status, void* stream);
+
+/* Bytes of the fixed scratch array sa_sparse_decode_noalloc uses (host function). */
+size_t sa_sparse_decode_noalloc_capacity(void);
+
+/*
  * sa_h2o_update -- token-level H2O: fold this step's attention probabilities
  * into the bf16 heavy-hitter scores and evict above budget (page_size 1).
  *

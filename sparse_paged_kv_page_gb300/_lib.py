@@ -45,6 +45,9 @@ SIGNATURES = {
     "sa_decode_workspace_init": (c_i32, [c_ptr, c_size, c_ptr]),
     "sa_sparse_decode": (c_i32, [P_CACHE, P_BATCH, c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_f32,
                                  c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_size, c_ptr, c_ptr]),
+    "sa_sparse_decode_noalloc": (c_i32, [P_CACHE, P_BATCH, c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_f32,
+                                         c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr]),
+    "sa_sparse_decode_noalloc_capacity": (c_size, []),
     "sa_h2o_update": (c_i32, [P_BATCH, c_i32, c_i32, c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_ptr,
                               c_ptr, c_i32, c_i32, c_i32, c_i32, c_f32, c_ptr, c_ptr, c_ptr,
                               c_ptr]),

@@ -17,7 +17,8 @@ from ._lib import SaBatch, SaCache
 
 __all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKVCache",
            "sa_append_kv", "sa_score_pages", "sa_select_topk", "sa_decode_workspace_size",
-           "sa_decode_workspace_init", "sa_sparse_decode", "sa_h2o_update", "sa_status_string",
+           "sa_decode_workspace_init", "sa_sparse_decode", "sa_sparse_decode_noalloc",
+           "sa_sparse_decode_noalloc_capacity", "sa_h2o_update", "sa_status_string",
            "sa_version", "alloc_decode_workspace"]
 
 _DT = {torch.bfloat16: _lib.SA_BF16, torch.float16: _lib.SA_FP16}
@@ -161,6 +162,24 @@ def sa_sparse_decode(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_id
         float(scale), _p(out, name="out"), _p(lse, torch.float32, "lse"),
         _p(logits, torch.float32, "logits"), int(logits_stride), _p(workspace, name="workspace"),
         wbytes, _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_sparse_decode_noalloc(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_idx,
+                             sel_cnt, sel_stride: int, scale: float, out, lse=None, logits=None,
+                             logits_stride: int = 0, dev_status=None, stream=None):
+    """sa_sparse_decode with the library's fixed scratch instead of a workspace
+    (for callers that cannot allocate; calls must not overlap on the GPU)."""
+    lib = _lib.load()
+    _check("sa_sparse_decode_noalloc", lib.sa_sparse_decode_noalloc(
+        ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads),
+        _p(sel_idx, torch.int32, "sel_idx"), _p(sel_cnt, torch.int32, "sel_cnt"), int(sel_stride),
+        float(scale), _p(out, name="out"), _p(lse, torch.float32, "lse"),
+        _p(logits, torch.float32, "logits"), int(logits_stride),
+        _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_sparse_decode_noalloc_capacity() -> int:
+    return int(_lib.load().sa_sparse_decode_noalloc_capacity())
 
 
 def sa_h2o_update(batch: SaBatch, num_kv_heads: int, num_q_heads: int, logits,

@@ -677,3 +677,54 @@ extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* bat
             : dispatch_tma<__half, 64>(a, grid, s, cache, 3);
 }
 
+// ---------------------------------------------------------------------------
+// sa_sparse_decode_noalloc: the same split-K decode, with its scratch (split
+// partials and per-(request, KV head) tickets) in a fixed device array of this
+// library instead of a caller workspace, for callers that cannot allocate.
+// ---------------------------------------------------------------------------
+#ifndef SA_NOALLOC_SCRATCH_BYTES
+#define SA_NOALLOC_SCRATCH_BYTES (4u << 20)
+#endif
+
+// Lives in every GPU that loads the library until the process exits. In host
+// code this name is only a stand-in: the device address comes from
+// cudaGetSymbolAddress, taken once per device with that device current.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void* g_noalloc_addr[64];   // device address of g_noalloc_scratch, per device ordinal
+}  // namespace
+
+extern "C" size_t sa_sparse_decode_noalloc_capacity(void) { return SA_NOALLOC_SCRATCH_BYTES; }
+
+extern "C" sa_status sa_sparse_decode_noalloc(const sa_cache* cache, const sa_batch* batch,
+                                              const void* q, int32_t num_q_heads,
+                                              const int32_t* sel_idx, const int32_t* sel_cnt,
+                                              int32_t sel_stride, float scale, void* out, float* lse,
+                                              float* logits, int32_t logits_stride,
+                                              int32_t* dev_status, void* stream) {
+  using namespace sa;
+  if (!cache || !batch || cache->num_kv_heads <= 0 || num_q_heads <= 0 || sel_stride <= 0 ||
+      num_q_heads % cache->num_kv_heads || cache->head_dim <= 0 || cache->page_size <= 0 ||
+      batch->batch <= 0)
+    return SA_ERR_INVALID_ARG;
+  const size_t need = sa_decode_workspace_size(batch->batch, cache->num_kv_heads, num_q_heads,
+                                               cache->head_dim, cache->page_size, sel_stride);
+  if (need == 0) return SA_ERR_INVALID_ARG;
+  if (need > SA_NOALLOC_SCRATCH_BYTES) return SA_ERR_WORKSPACE;   // beyond the fixed scratch
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SA_ERR_CUDA;
+  if (!g_noalloc_addr[dev]) {
+    // set-up on this device's first call (do it before any stream capture)
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SA_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  void* ws = g_noalloc_addr[dev];
+  // the tickets must start at zero on every call (a call cut short could leave them set)
+  const size_t ticket_bytes = size_t(batch->batch) * cache->num_kv_heads * sizeof(int32_t);
+  if (cudaMemsetAsync(ws, 0, ticket_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SA_ERR_CUDA;
+  return sa_sparse_decode(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
+                          logits, logits_stride, ws, SA_NOALLOC_SCRATCH_BYTES, dev_status, stream);
+}
