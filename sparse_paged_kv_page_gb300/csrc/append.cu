@@ -49,7 +49,8 @@ struct AppendArgs {
   int H, D, ps, num_blocks, bt_stride, max_new, ret_cap;
 };
 
-constexpr int kAppendThreads = 512;
+constexpr int kAppendThreads = 512;   // prefill path
+constexpr int kFusedThreads = 128;    // decode path: small enough to run beside the page scorer
 constexpr int kRowBatch = 16;     // rows of a page loaded per batch (independent loads)
 
 // exact float32 sum step: s += x, clears `exact` if the addition rounded
@@ -87,8 +88,8 @@ __device__ __forceinline__ bool mean_f32(float S, int f, uint16_t& out) {
 }
 
 // Recompute statistics of page p of request b (all heads) and write the new rows.
-// Thread (h, c) owns the column pair [2c, 2c+1] of KV head h.
-template <typename T>
+// Thread (h, c) owns the column pair [2c, 2c+1] of KV head h (NT threads loop).
+template <typename T, int NT>
 __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, int L_old, int L_new,
                                              int row0) {
   using E = Elem<T>;
@@ -107,7 +108,7 @@ __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, 
   uint32_t* kp = static_cast<uint32_t*>(a.k);
   uint32_t* vp = static_cast<uint32_t*>(a.v);
 
-  for (int idx = threadIdx.x; idx < H * C; idx += kAppendThreads) {
+  for (int idx = threadIdx.x; idx < H * C; idx += NT) {
     const int h = idx / C, c = idx % C;
     const int64_t tile = (int64_t(blk) * H + h) * ps;    // first row of this (block, head)
     float mn0 = INFINITY, mn1 = INFINITY, mx0 = -INFINITY, mx1 = -INFINITY, sm0 = 0.f, sm1 = 0.f;
@@ -170,14 +171,14 @@ __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, 
   }
   // H2O slots of the written tokens start at zero
   if (a.hh) {
-    for (int idx = threadIdx.x; idx < (fill - s_new) * H; idx += kAppendThreads) {
+    for (int idx = threadIdx.x; idx < (fill - s_new) * H; idx += NT) {
       const int s = s_new + idx / H, h = idx % H;
       a.hh[(int64_t(blk) * ps + s) * H + h] = 0;
     }
   }
   // token-level retained lists: append the new positions, ascending
   if (a.ret_pos) {
-    for (int idx = threadIdx.x; idx < (fill - s_new) * H; idx += kAppendThreads) {
+    for (int idx = threadIdx.x; idx < (fill - s_new) * H; idx += NT) {
       const int s = s_new + idx / H, h = idx % H;
       const int pos = page_start + s;
       const int cpos = a.ret_cnt[b * H + h] + (pos - L_old);
@@ -220,23 +221,23 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
   if (!plan(a, b, i == 0 && threadIdx.x == 0, L_old, n, row0)) return;
   const int p = L_old / a.ps + i;
   if (p > (L_old + n - 1) / a.ps) return;
-  refresh_page<T>(a, b, p, L_old, L_old + n, row0);
+  refresh_page<T, kAppendThreads>(a, b, p, L_old, L_old + n, row0);
 }
 
 // Grid (B): a request's (at most two) pages, then its length, in one CTA.
 template <typename T>
-__global__ void __launch_bounds__(kAppendThreads) append_fused_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kFusedThreads) append_fused_kernel(AppendArgs a) {
   const int b = blockIdx.x;
   int L_old, n, row0;
   const bool any = plan(a, b, threadIdx.x == 0, L_old, n, row0);
   if (any)
     for (int p = L_old / a.ps; p <= (L_old + n - 1) / a.ps; ++p)
-      refresh_page<T>(a, b, p, L_old, L_old + n, row0);
+      refresh_page<T, kFusedThreads>(a, b, p, L_old, L_old + n, row0);
   __syncthreads();                                          // every read of the old length is done
-  if (any && threadIdx.x < a.H) {
-    if (a.ret_cnt) {
-      const int c = a.ret_cnt[b * a.H + threadIdx.x] + n;
-      a.ret_cnt[b * a.H + threadIdx.x] = min(max(c, 0), a.ret_cap);
+  if (any) {
+    for (int h = threadIdx.x; h < a.H && a.ret_cnt; h += kFusedThreads) {
+      const int c = a.ret_cnt[b * a.H + h] + n;
+      a.ret_cnt[b * a.H + h] = min(max(c, 0), a.ret_cap);
     }
     if (threadIdx.x == 0) a.seq_lens[b] = L_old + n;
   }
@@ -276,7 +277,6 @@ extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, 
   if (!k_new || !v_new || !new_cu || max_new_per_req < 0) return SA_ERR_INVALID_ARG;
   if ((ret_pos == nullptr) != (ret_cnt == nullptr)) return SA_ERR_INVALID_ARG;
   if (ret_pos && ret_cap <= 0) return SA_ERR_INVALID_ARG;
-  if (cache->num_kv_heads > kAppendThreads) return SA_ERR_UNSUPPORTED;   // one thread per head for lengths
   if (max_new_per_req == 0) return SA_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   AppendArgs a;
@@ -290,8 +290,8 @@ extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, 
   a.max_new = max_new_per_req; a.ret_cap = ret_pos ? ret_cap : 0;
   const bool bf = cache->dtype == SA_BF16;
   if (max_new_per_req <= a.ps) {                            // touches at most two pages per request
-    if (bf) append_fused_kernel<__nv_bfloat16><<<batch->batch, kAppendThreads, 0, s>>>(a);
-    else append_fused_kernel<__half><<<batch->batch, kAppendThreads, 0, s>>>(a);
+    if (bf) append_fused_kernel<__nv_bfloat16><<<batch->batch, kFusedThreads, 0, s>>>(a);
+    else append_fused_kernel<__half><<<batch->batch, kFusedThreads, 0, s>>>(a);
     return launch_status();
   }
   const int64_t pages = (int64_t(max_new_per_req) + a.ps - 1) / a.ps + 1;

@@ -232,6 +232,40 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch (no-ops unless the launch asked for it)
+// ---------------------------------------------------------------------------
+// Let the next kernel in the stream, if launched programmatically, start now.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+// Wait until the grids this one depends on have completed and their memory is visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// thread-block clusters: rank, distributed shared memory, barrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// All threads of all CTAs of the cluster; release our shared-memory writes, acquire the others'.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // order-preserving keys
 // ---------------------------------------------------------------------------
 // float32 -> uint32 whose unsigned order is the float order, -0 == +0, NaN

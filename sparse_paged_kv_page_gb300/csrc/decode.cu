@@ -49,6 +49,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kStages = SA_DECODE_STAGES;
 constexpr int kCtasPerSm = SA_DECODE_CTAS_PER_SM;
 constexpr int kMaxSplit = 64;
+constexpr int kMaxCluster = 8;         // portable cluster size: splits merged through DSMEM
 constexpr int kMaxEnt = 4096;          // (block, fill) entries staged per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -88,17 +89,24 @@ struct Tile {
   static constexpr int kSmem = kWarps * kStages * kStageBytes + 1024;   // + alignment slack
 };
 
+// Byte offset (from the 1024-aligned base) of a CTA's cluster partial, past the
+// warp-merge scratch (<= 4 warps x 16 rows x (D + 4) floats + 512 bytes).
+constexpr int kClusterOff = 36 * 1024;
+
 template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return uint32_t((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-template <typename T, int D, bool kTma>
+template <typename T, int D, bool kTma, bool kCluster>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
   using E = Elem<T>;
   using TL = Tile<D>;
+  static_assert(kClusterOff >= 4 * (kWarps * 32 + kWarps * 16 * (D + 4)), "warp-merge scratch overlaps");
+  static_assert(kClusterOff + 4 * (16 * D + 16) <= kWarps * kStages * TL::kStageBytes,
+                "cluster partial must fit in the stage area");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ uint32_t s_mask[kWarps][kStages];
   __shared__ __align__(8) uint64_t s_bar[kWarps][kStages];
@@ -391,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   __syncthreads();
   const bool single = a.nsplit == 1;
   T* outp = static_cast<T*>(a.out) + (int64_t(b) * a.H_q + int64_t(h) * G) * D;
-  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < G * D && !(kCluster && !single); idx += kThreads) {
     const int row = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
@@ -419,6 +427,66 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   }
   if (single) return;
+
+  if constexpr (kCluster) {
+    // The unit's nsplit CTAs form one cluster. Each leaves its partial in its
+    // own shared memory; after a cluster barrier each CTA merges a 1/nsplit
+    // slice of the unit's G*D outputs from every peer's partial over DSMEM; a
+    // second barrier keeps all shared memory alive until every peer is done.
+    float* cl_o = reinterpret_cast<float*>(smem + kClusterOff);   // [G][D]
+    float* cl_lse = cl_o + 16 * D;                                 // [G]
+    for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+      const int row = idx / D, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 16 + row]);
+      float acc = 0.f, tot = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float mw = wm[w * 16 + row];
+          if (mw == -INFINITY) continue;
+          const float f = exp2f(mw - M);
+          acc += wo[(w * G + row) * WS + d] * f;
+          tot += wl[w * 16 + row] * f;
+        }
+      }
+      cl_o[row * D + d] = tot > 0.f ? acc / tot : 0.f;
+      if (d == 0) cl_lse[row] = tot > 0.f ? (M + log2f(tot)) * kLn2 : -INFINITY;
+    }
+    cluster_sync();
+    const int ns = a.nsplit;
+    const int n_el = G * D, chunk = (n_el + ns - 1) / ns;
+    const int e0 = int(cluster_rank()) * chunk, e1 = min(n_el, e0 + chunk);
+    const uint32_t o_base = smem_u32(cl_o), l_base = smem_u32(cl_lse);
+    for (int idx = e0 + threadIdx.x; idx < e1; idx += kThreads) {
+      const int row = idx / D, d = idx % D;
+      float lv[kMaxCluster], ov[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        lv[r] = r < ns ? dsmem_ld_f32(dsmem_map(l_base + 4u * row, r)) : -INFINITY;
+        ov[r] = r < ns ? dsmem_ld_f32(dsmem_map(o_base + 4u * (row * D + d), r)) : 0.f;
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, lv[r] == INFINITY ? -INFINITY : lv[r]);
+      float acc = 0.f, tot = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          if (!(lv[r] > -INFINITY) || lv[r] == INFINITY) continue;
+          const float w = expf(lv[r] - M);
+          acc += w * ov[r];
+          tot += w;
+        }
+      }
+      reinterpret_cast<uint16_t*>(outp)[row * D + d] = E::from_f(tot > 0.f ? acc / tot : 0.f);
+      if (a.lse && d == 0)
+        a.lse[int64_t(b) * a.H_q + int64_t(h) * G + row] = tot > 0.f ? M + logf(tot) : -INFINITY;
+    }
+    cluster_sync();
+    return;
+  }
 
   // last CTA of the unit merges the partials
   __threadfence();
@@ -521,6 +589,7 @@ int num_sms() {
 int choose_nsplit(int units, int max_tiles, int ps, int sms) {
   const int target = kCtasPerSm * sms;
   int s = target / units;
+  if (s > kMaxCluster) s = kMaxCluster;      // split CTAs of a unit fit one cluster
   const int64_t ent_total = (int64_t(max_tiles) * 16 + ps - 1) / ps;
   const int need = int((ent_total + kMaxEnt - 1) / kMaxEnt);
   if (s < need) s = need;
@@ -584,59 +653,63 @@ bool make_pool_map(CUtensorMap* m, const void* base, const sa_cache* c) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_dec_smem[8][64];
+int g_dec_smem[16][64];
 
-template <typename T, int D, bool kTma>
+template <typename T, int D, bool kTma, bool kCluster>
 sa_status launch_decode(const DecodeArgs& a, dim3 grid, cudaStream_t s, const CUtensorMap& mk,
                         const CUtensorMap& mv, int* cache) {
-  auto k = decode_kernel<T, D, kTma>;
+  auto k = decode_kernel<T, D, kTma, kCluster>;
   const int smem = Tile<D>::kSmem + a.ent_max * int(sizeof(int2));
   if (!ensure_smem(k, smem, cache)) return SA_ERR_CUDA;
-  k<<<grid, kThreads, smem, s>>>(a, mk, mv);
-  return launch_status();
+  if (!kCluster) {
+    k<<<grid, kThreads, smem, s>>>(a, mk, mv);
+    return launch_status();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = grid.x;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k, a, mk, mv) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return SA_ERR_UNSUPPORTED;                   // caller falls back to the ticket merge
+  }
+  return SA_OK;
+}
+
+template <typename T, int D, bool kTma>
+sa_status launch_merge_mode(const DecodeArgs& a, dim3 grid, cudaStream_t s, const CUtensorMap& mk,
+                            const CUtensorMap& mv, int slot, bool allow_cluster) {
+  if (allow_cluster && a.nsplit > 1 && a.nsplit <= kMaxCluster) {
+    const sa_status st = launch_decode<T, D, kTma, true>(a, grid, s, mk, mv, g_dec_smem[4 * slot + 2 + kTma]);
+    if (st != SA_ERR_UNSUPPORTED) return st;
+  }
+  if (a.nsplit > 1 && !a.tickets) return SA_ERR_WORKSPACE;
+  return launch_decode<T, D, kTma, false>(a, grid, s, mk, mv, g_dec_smem[4 * slot + kTma]);
 }
 
 template <typename T, int D>
-sa_status dispatch_tma(const DecodeArgs& a, dim3 grid, cudaStream_t s, const sa_cache* c, int slot) {
+sa_status dispatch_tma(const DecodeArgs& a, dim3 grid, cudaStream_t s, const sa_cache* c, int slot,
+                       bool allow_cluster) {
   CUtensorMap mk, mv;
   if (c->page_size >= 16 && make_pool_map(&mk, c->k, c) && make_pool_map(&mv, c->v, c))
-    return launch_decode<T, D, true>(a, grid, s, mk, mv, g_dec_smem[2 * slot]);
+    return launch_merge_mode<T, D, true>(a, grid, s, mk, mv, slot, allow_cluster);
   memset(&mk, 0, sizeof(mk));
   memset(&mv, 0, sizeof(mv));
-  return launch_decode<T, D, false>(a, grid, s, mk, mv, g_dec_smem[2 * slot + 1]);
+  return launch_merge_mode<T, D, false>(a, grid, s, mk, mv, slot, allow_cluster);
 }
 
-}  // namespace
-}  // namespace sa
-
-extern "C" size_t sa_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads,
-                                           int32_t head_dim, int32_t page_size, int32_t sel_stride) {
-  using namespace sa;
-  if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
-      sel_stride <= 0 || num_q_heads % num_kv_heads)
-    return 0;
-  const int units = batch * num_kv_heads;
-  const int64_t max_tiles = (int64_t(sel_stride) * page_size + 15) / 16;
-  const int ns = choose_nsplit(units, int(max_tiles > (1 << 30) ? (1 << 30) : max_tiles), page_size,
-                               num_sms());
-  return ws_layout(units, num_q_heads / num_kv_heads, head_dim, ns).total;
-}
-
-extern "C" sa_status sa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
-  if (!workspace || workspace_bytes == 0) return SA_ERR_INVALID_ARG;
-  return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? SA_OK
-             : SA_ERR_CUDA;
-}
-
-extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* batch, const void* q,
-                                      int32_t num_q_heads, const int32_t* sel_idx,
-                                      const int32_t* sel_cnt, int32_t sel_stride, float scale,
-                                      void* out, float* lse, float* logits, int32_t logits_stride,
-                                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                                      void* stream) {
-  using namespace sa;
+sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* q, int32_t num_q_heads,
+                      const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_stride, float scale,
+                      void* out, float* lse, float* logits, int32_t logits_stride, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_status, void* stream, bool allow_cluster) {
   sa_status st = check_cache(cache, true, false);
   if (st != SA_OK) return st;
   if ((st = check_batch(batch)) != SA_OK) return st;
@@ -671,10 +744,44 @@ extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* bat
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = cache->dtype == SA_BF16;
   if (cache->head_dim == 128)
-    return bf ? dispatch_tma<__nv_bfloat16, 128>(a, grid, s, cache, 0)
-              : dispatch_tma<__half, 128>(a, grid, s, cache, 1);
-  return bf ? dispatch_tma<__nv_bfloat16, 64>(a, grid, s, cache, 2)
-            : dispatch_tma<__half, 64>(a, grid, s, cache, 3);
+    return bf ? dispatch_tma<__nv_bfloat16, 128>(a, grid, s, cache, 0, allow_cluster)
+              : dispatch_tma<__half, 128>(a, grid, s, cache, 1, allow_cluster);
+  return bf ? dispatch_tma<__nv_bfloat16, 64>(a, grid, s, cache, 2, allow_cluster)
+            : dispatch_tma<__half, 64>(a, grid, s, cache, 3, allow_cluster);
+}
+
+}  // namespace
+}  // namespace sa
+
+extern "C" size_t sa_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads,
+                                           int32_t head_dim, int32_t page_size, int32_t sel_stride) {
+  using namespace sa;
+  if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
+      sel_stride <= 0 || num_q_heads % num_kv_heads)
+    return 0;
+  const int units = batch * num_kv_heads;
+  const int64_t max_tiles = (int64_t(sel_stride) * page_size + 15) / 16;
+  const int ns = choose_nsplit(units, int(max_tiles > (1 << 30) ? (1 << 30) : max_tiles), page_size,
+                               num_sms());
+  return ws_layout(units, num_q_heads / num_kv_heads, head_dim, ns).total;
+}
+
+extern "C" sa_status sa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes == 0) return SA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
+}
+
+extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* batch, const void* q,
+                                      int32_t num_q_heads, const int32_t* sel_idx,
+                                      const int32_t* sel_cnt, int32_t sel_stride, float scale,
+                                      void* out, float* lse, float* logits, int32_t logits_stride,
+                                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream) {
+  return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
+                         logits, logits_stride, workspace, workspace_bytes, dev_status, stream, true);
 }
 
 // ---------------------------------------------------------------------------
@@ -725,6 +832,7 @@ extern "C" sa_status sa_sparse_decode_noalloc(const sa_cache* cache, const sa_ba
   const size_t ticket_bytes = size_t(batch->batch) * cache->num_kv_heads * sizeof(int32_t);
   if (cudaMemsetAsync(ws, 0, ticket_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SA_ERR_CUDA;
-  return sa_sparse_decode(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
-                          logits, logits_stride, ws, SA_NOALLOC_SCRATCH_BYTES, dev_status, stream);
+  return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
+                         logits, logits_stride, ws, SA_NOALLOC_SCRATCH_BYTES, dev_status, stream,
+                         /*allow_cluster=*/false);
 }
