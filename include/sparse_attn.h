@@ -11,6 +11,8 @@
  *                     split across pages, partials merged by log-sum-exp
  *   sa_h2o_update     token-level (page_size 1) decayed heavy-hitter fold and
  *                     sink/grace-protected eviction
+ *   sa_decode_step    the page-level chain (append, score, select, decode) in
+ *                     one call, kernels overlapped by programmatic launch
  *
  * Sources (cited by page title and section):
  *   [vortex]  "flow: add H2O sparse attention (page-level and token-level,
@@ -282,6 +284,38 @@ sa_status sa_h2o_update(const sa_batch* batch, int32_t num_kv_heads, int32_t num
                         int32_t budget, int32_t n_sink, int32_t grace, float decay,
                         int32_t* evicted, int32_t* evicted_cnt, int32_t* dev_status,
                         void* stream);
+
+/*
+ * sa_decode_step -- one whole page-level decode step in one call:
+ * sa_append_kv, sa_score_pages, sa_select_topk, sa_sparse_decode.
+ *
+ * [vortex] "Page-level variants" and [entmax] "How it works": the new token's
+ * key refreshes its page's statistics, every page is scored from the
+ * statistics, the top-k pages (tail forced) are chosen and attention runs
+ * exactly over them. Arguments mean what they mean in the four calls (the
+ * selection row length is topk; no H2O slots, no retained lists, no logits).
+ *   k_new      nullable: NULL (or max_new_per_req 0) skips the append, and
+ *              v_new / new_cu are then ignored
+ *   workspace  at least sa_decode_workspace_size(batch, num_kv_heads,
+ *              num_q_heads, head_dim, page_size, topk) bytes, zero-filled once
+ *              (else SA_ERR_WORKSPACE)
+ * Needs cache->meta. Limits: those of the four calls.
+ * The kernels are chained by programmatic dependent launch on `stream`: each
+ * one starts its prologue (reading q, setting up barriers) while its
+ * predecessor finishes and waits on the device for the data it consumes.
+ * With max_new_per_req == 1 the append runs beside the scorer, which then
+ * scores the lengths from before the append: every page the append leaves
+ * untouched gets its exact score, while the score entry of the page the new
+ * token went to (the tail, always selected) is unspecified. With
+ * max_new_per_req > 1 the append runs first and every score is exact.
+ * Selection, output and lse are those of the four calls in order.
+ */
+sa_status sa_decode_step(const sa_cache* cache, const sa_batch* batch, const void* k_new,
+                         const void* v_new, const int32_t* new_cu, int32_t max_new_per_req,
+                         const void* q, int32_t num_q_heads, float w_avg, float w_peak,
+                         float* scores, int32_t max_pages, int32_t topk, int32_t* sel_idx,
+                         int32_t* sel_cnt, float scale, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* sa_status_string(sa_status status);

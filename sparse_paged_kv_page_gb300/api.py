@@ -18,7 +18,8 @@ from ._lib import SaBatch, SaCache
 __all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKVCache",
            "sa_append_kv", "sa_score_pages", "sa_select_topk", "sa_decode_workspace_size",
            "sa_decode_workspace_init", "sa_sparse_decode", "sa_sparse_decode_noalloc",
-           "sa_sparse_decode_noalloc_capacity", "sa_h2o_update", "sa_status_string",
+           "sa_sparse_decode_noalloc_capacity", "sa_h2o_update", "sa_decode_step",
+           "sa_status_string",
            "sa_version", "alloc_decode_workspace"]
 
 _DT = {torch.bfloat16: _lib.SA_BF16, torch.float16: _lib.SA_FP16}
@@ -195,3 +196,20 @@ def sa_h2o_update(batch: SaBatch, num_kv_heads: int, num_q_heads: int, logits,
         float(decay), _p(evicted, torch.int32, "evicted"),
         _p(evicted_cnt, torch.int32, "evicted_cnt"), _p(dev_status, torch.int32, "dev_status"),
         _s(stream)))
+
+
+def sa_decode_step(cache: SaCache, batch: SaBatch, k_new, v_new, new_cu, max_new_per_req: int,
+                   q, num_q_heads: int, w_avg: float, w_peak: float, scores, max_pages: int,
+                   topk: int, sel_idx, sel_cnt, scale: float, out, lse=None, workspace=None,
+                   dev_status=None, stream=None):
+    """Append (k_new may be None), score, select and decode in one chained call."""
+    lib = _lib.load()
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("sa_decode_step", lib.sa_decode_step(
+        ctypes.byref(cache), ctypes.byref(batch), _p(k_new, name="k_new"), _p(v_new, name="v_new"),
+        _p(new_cu, torch.int32, "new_cu"), int(max_new_per_req), _p(q, name="q"),
+        int(num_q_heads), float(w_avg), float(w_peak), _p(scores, torch.float32, "scores"),
+        int(max_pages), int(topk), _p(sel_idx, torch.int32, "sel_idx"),
+        _p(sel_cnt, torch.int32, "sel_cnt"), float(scale), _p(out, name="out"),
+        _p(lse, torch.float32, "lse"), _p(workspace, name="workspace"), wbytes,
+        _p(dev_status, torch.int32, "dev_status"), _s(stream)))

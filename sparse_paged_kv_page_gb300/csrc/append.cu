@@ -225,8 +225,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
 }
 
 // Grid (B): a request's (at most two) pages, then its length, in one CTA.
+// At most 128 registers a thread: with the page scorer's two CTAs resident,
+// the sub-partitions holding three of its warps have exactly one 128-register
+// warp's worth of registers left, so this kernel can run beside the scorer.
 template <typename T>
-__global__ void __launch_bounds__(kFusedThreads) append_fused_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kFusedThreads, 4) append_fused_kernel(AppendArgs a) {
   const int b = blockIdx.x;
   int L_old, n, row0;
   const bool any = plan(a, b, threadIdx.x == 0, L_old, n, row0);
@@ -241,6 +244,10 @@ __global__ void __launch_bounds__(kFusedThreads) append_fused_kernel(AppendArgs 
     }
     if (threadIdx.x == 0) a.seq_lens[b] = L_old + n;
   }
+  // Launched programmatically beside the page scorer (which has read the old
+  // lengths before letting this kernel start), it finishes only after the
+  // scorer, so whatever follows in the stream sees both.
+  pdl_wait();
 }
 
 // Advances lengths (and retained counts) after the append kernel has read them.
@@ -266,10 +273,10 @@ __global__ void advance_kernel(int32_t* seq_lens, const int32_t* new_cu, int32_t
 }  // namespace
 }  // namespace sa
 
-extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, const void* k_new,
-                                  const void* v_new, const int32_t* new_cu, int32_t max_new_per_req,
-                                  void* hh, int32_t* ret_pos, int32_t* ret_cnt, int32_t ret_cap,
-                                  int32_t* dev_status, void* stream) {
+sa_status sa::append_impl(const sa_cache* cache, const sa_batch* batch, const void* k_new,
+                         const void* v_new, const int32_t* new_cu, int32_t max_new_per_req, void* hh,
+                         int32_t* ret_pos, int32_t* ret_cnt, int32_t ret_cap, int32_t* dev_status,
+                         void* stream, bool pdl) {
   using namespace sa;
   sa_status st = check_cache(cache, true, false);
   if (st != SA_OK) return st;
@@ -290,9 +297,14 @@ extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, 
   a.max_new = max_new_per_req; a.ret_cap = ret_pos ? ret_cap : 0;
   const bool bf = cache->dtype == SA_BF16;
   if (max_new_per_req <= a.ps) {                            // touches at most two pages per request
-    if (bf) append_fused_kernel<__nv_bfloat16><<<batch->batch, kFusedThreads, 0, s>>>(a);
-    else append_fused_kernel<__half><<<batch->batch, kFusedThreads, 0, s>>>(a);
-    return launch_status();
+    static int g_fused_attr[2][64];
+    if (bf ? !ensure_smem(append_fused_kernel<__nv_bfloat16>, 0, g_fused_attr[0])
+           : !ensure_smem(append_fused_kernel<__half>, 0, g_fused_attr[1]))
+      return SA_ERR_CUDA;
+    const cudaError_t e =
+        bf ? launch_ex(append_fused_kernel<__nv_bfloat16>, dim3(batch->batch), dim3(kFusedThreads), 0, s, pdl, 1, a)
+           : launch_ex(append_fused_kernel<__half>, dim3(batch->batch), dim3(kFusedThreads), 0, s, pdl, 1, a);
+    return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
   }
   const int64_t pages = (int64_t(max_new_per_req) + a.ps - 1) / a.ps + 1;
   if (pages > 0x7fffffff) return SA_ERR_INVALID_ARG;
@@ -303,4 +315,12 @@ extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, 
   advance_kernel<<<1, 256, 0, s>>>(batch->seq_lens, new_cu, ret_cnt, batch->batch, a.H,
                                    max_new_per_req, int64_t(batch->bt_stride) * a.ps, a.ret_cap);
   return launch_status();
+}
+
+extern "C" sa_status sa_append_kv(const sa_cache* cache, const sa_batch* batch, const void* k_new,
+                                  const void* v_new, const int32_t* new_cu, int32_t max_new_per_req,
+                                  void* hh, int32_t* ret_pos, int32_t* ret_cnt, int32_t ret_cap,
+                                  int32_t* dev_status, void* stream) {
+  return sa::append_impl(cache, batch, k_new, v_new, new_cu, max_new_per_req, hh, ret_pos, ret_cnt,
+                         ret_cap, dev_status, stream, false);
 }

@@ -118,21 +118,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = b * a.H_kv + h;
   const int G = a.G, ps = a.ps, pss = a.ps_shift;
-  const int L = a.seq_lens[b];
-  int cnt = a.cnt[unit];
-  if (cnt < 0 || cnt > a.sel_stride) {
-    if (threadIdx.x == 0 && split == 0) flag(a.status, SA_DEV_BAD_COUNT);
-    cnt = cnt < 0 ? 0 : a.sel_stride;
-  }
-  const int n_rows = cnt << pss;
-  const int n_tiles = (n_rows + 15) >> 4;
-  const int per = (n_tiles + a.nsplit - 1) / a.nsplit;
-  const int t_begin = min(n_tiles, split * per), t_end = min(n_tiles, t_begin + per);
-  const int n_pages_req = L > 0 ? (L + ps - 1) >> pss : 0;
-  const int32_t* sel = a.sel + int64_t(unit) * a.sel_stride;
-  const int32_t* btb = a.bt + int64_t(b) * a.bt_stride;
 
-  // Q as the A operand (rows = query heads of this KV head, zero beyond G)
+  // Q as the A operand (rows = query heads of this KV head, zero beyond G).
+  // Q is an input of the step, so it is read before waiting on the selection.
   const int g = lane >> 2, tq = lane & 3;
   uint32_t qa[D / 16][4];
   {
@@ -147,6 +135,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       qa[kk][3] = g + 8 < G ? qp[(g + 8) * (D / 2) + c1] : 0u;
     }
   }
+  if (kTma && threadIdx.x == 0) {
+    for (int w = 0; w < kWarps; ++w)
+      for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&s_bar[w][s]), 1);
+    mbar_init_fence();
+  }
+  // lengths and selection come from the kernels before this one in the step
+  pdl_wait();
+
+  const int L = a.seq_lens[b];
+  int cnt = a.cnt[unit];
+  if (cnt < 0 || cnt > a.sel_stride) {
+    if (threadIdx.x == 0 && split == 0) flag(a.status, SA_DEV_BAD_COUNT);
+    cnt = cnt < 0 ? 0 : a.sel_stride;
+  }
+  const int n_rows = cnt << pss;
+  const int n_tiles = (n_rows + 15) >> 4;
+  const int per = (n_tiles + a.nsplit - 1) / a.nsplit;
+  const int t_begin = min(n_tiles, split * per), t_end = min(n_tiles, t_begin + per);
+  const int n_pages_req = L > 0 ? (L + ps - 1) >> pss : 0;
+  const int32_t* sel = a.sel + int64_t(unit) * a.sel_stride;
+  const int32_t* btb = a.bt + int64_t(b) * a.bt_stride;
 
   // Prologue: resolve the selection entries this CTA touches to (block, fill)
   // once, in parallel, so the copy loop never waits on sel -> block table.
@@ -167,11 +176,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       else blk = x;
     }
     s_ent[i] = make_int2(blk, fill);
-  }
-  if (kTma && threadIdx.x == 0) {
-    for (int w = 0; w < kWarps; ++w)
-      for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&s_bar[w][s]), 1);
-    mbar_init_fence();
   }
   __syncthreads();
 
@@ -657,59 +661,48 @@ int g_dec_smem[16][64];
 
 template <typename T, int D, bool kTma, bool kCluster>
 sa_status launch_decode(const DecodeArgs& a, dim3 grid, cudaStream_t s, const CUtensorMap& mk,
-                        const CUtensorMap& mv, int* cache) {
+                        const CUtensorMap& mv, int* cache, bool pdl) {
   auto k = decode_kernel<T, D, kTma, kCluster>;
   const int smem = Tile<D>::kSmem + a.ent_max * int(sizeof(int2));
   if (!ensure_smem(k, smem, cache)) return SA_ERR_CUDA;
-  if (!kCluster) {
-    k<<<grid, kThreads, smem, s>>>(a, mk, mv);
-    return launch_status();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = size_t(smem);
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = grid.x;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, k, a, mk, mv) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return SA_ERR_UNSUPPORTED;                   // caller falls back to the ticket merge
-  }
-  return SA_OK;
+  const cudaError_t e = launch_ex(k, grid, dim3(kThreads), size_t(smem), s, pdl, kCluster ? grid.x : 1u,
+                                  a, mk, mv);
+  if (e == cudaSuccess) return SA_OK;
+  if (!kCluster) return SA_ERR_CUDA;
+  (void)cudaGetLastError();
+  return SA_ERR_UNSUPPORTED;                     // caller falls back to the ticket merge
 }
 
 template <typename T, int D, bool kTma>
 sa_status launch_merge_mode(const DecodeArgs& a, dim3 grid, cudaStream_t s, const CUtensorMap& mk,
-                            const CUtensorMap& mv, int slot, bool allow_cluster) {
+                            const CUtensorMap& mv, int slot, bool allow_cluster, bool pdl) {
   if (allow_cluster && a.nsplit > 1 && a.nsplit <= kMaxCluster) {
-    const sa_status st = launch_decode<T, D, kTma, true>(a, grid, s, mk, mv, g_dec_smem[4 * slot + 2 + kTma]);
+    const sa_status st =
+        launch_decode<T, D, kTma, true>(a, grid, s, mk, mv, g_dec_smem[4 * slot + 2 + kTma], pdl);
     if (st != SA_ERR_UNSUPPORTED) return st;
   }
   if (a.nsplit > 1 && !a.tickets) return SA_ERR_WORKSPACE;
-  return launch_decode<T, D, kTma, false>(a, grid, s, mk, mv, g_dec_smem[4 * slot + kTma]);
+  return launch_decode<T, D, kTma, false>(a, grid, s, mk, mv, g_dec_smem[4 * slot + kTma], pdl);
 }
 
 template <typename T, int D>
 sa_status dispatch_tma(const DecodeArgs& a, dim3 grid, cudaStream_t s, const sa_cache* c, int slot,
-                       bool allow_cluster) {
+                       bool allow_cluster, bool pdl) {
   CUtensorMap mk, mv;
   if (c->page_size >= 16 && make_pool_map(&mk, c->k, c) && make_pool_map(&mv, c->v, c))
-    return launch_merge_mode<T, D, true>(a, grid, s, mk, mv, slot, allow_cluster);
+    return launch_merge_mode<T, D, true>(a, grid, s, mk, mv, slot, allow_cluster, pdl);
   memset(&mk, 0, sizeof(mk));
   memset(&mv, 0, sizeof(mv));
-  return launch_merge_mode<T, D, false>(a, grid, s, mk, mv, slot, allow_cluster);
+  return launch_merge_mode<T, D, false>(a, grid, s, mk, mv, slot, allow_cluster, pdl);
 }
+
+}  // namespace
 
 sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* q, int32_t num_q_heads,
                       const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_stride, float scale,
                       void* out, float* lse, float* logits, int32_t logits_stride, void* workspace,
-                      size_t workspace_bytes, int32_t* dev_status, void* stream, bool allow_cluster) {
+                      size_t workspace_bytes, int32_t* dev_status, void* stream, bool allow_cluster,
+                      bool pdl) {
   sa_status st = check_cache(cache, true, false);
   if (st != SA_OK) return st;
   if ((st = check_batch(batch)) != SA_OK) return st;
@@ -744,13 +737,12 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = cache->dtype == SA_BF16;
   if (cache->head_dim == 128)
-    return bf ? dispatch_tma<__nv_bfloat16, 128>(a, grid, s, cache, 0, allow_cluster)
-              : dispatch_tma<__half, 128>(a, grid, s, cache, 1, allow_cluster);
-  return bf ? dispatch_tma<__nv_bfloat16, 64>(a, grid, s, cache, 2, allow_cluster)
-            : dispatch_tma<__half, 64>(a, grid, s, cache, 3, allow_cluster);
+    return bf ? dispatch_tma<__nv_bfloat16, 128>(a, grid, s, cache, 0, allow_cluster, pdl)
+              : dispatch_tma<__half, 128>(a, grid, s, cache, 1, allow_cluster, pdl);
+  return bf ? dispatch_tma<__nv_bfloat16, 64>(a, grid, s, cache, 2, allow_cluster, pdl)
+            : dispatch_tma<__half, 64>(a, grid, s, cache, 3, allow_cluster, pdl);
 }
 
-}  // namespace
 }  // namespace sa
 
 extern "C" size_t sa_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads,
@@ -781,7 +773,7 @@ extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* bat
                                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                       void* stream) {
   return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
-                         logits, logits_stride, workspace, workspace_bytes, dev_status, stream, true);
+                         logits, logits_stride, workspace, workspace_bytes, dev_status, stream, true, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -834,5 +826,5 @@ extern "C" sa_status sa_sparse_decode_noalloc(const sa_cache* cache, const sa_ba
     return SA_ERR_CUDA;
   return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
                          logits, logits_stride, ws, SA_NOALLOC_SCRATCH_BYTES, dev_status, stream,
-                         /*allow_cluster=*/false);
+                         /*allow_cluster=*/false, /*pdl=*/false);
 }

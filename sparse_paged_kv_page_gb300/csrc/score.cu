@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
   __shared__ int scan_tmp[32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
 
   // chunk prefix over requests: request b owns H_kv * ceil(n_b / kChunk) chunks
   {
@@ -121,6 +122,9 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
     mbar_init_fence();
   }
   __syncthreads();
+  // every length this CTA needs is in shared memory: a programmatically
+  // launched successor (the step's append) may start now
+  pdl_trigger();
   const int total = s_prefix[a.B];
   const int c_begin = int((int64_t(total) * blockIdx.x) / gridDim.x);
   const int c_end = int((int64_t(total) * (blockIdx.x + 1)) / gridDim.x);
@@ -282,9 +286,9 @@ int sm_count() {
 }  // namespace
 }  // namespace sa
 
-extern "C" sa_status sa_score_pages(const sa_cache* cache, const sa_batch* batch, const void* q,
-                                    int32_t num_q_heads, float w_avg, float w_peak, float* scores,
-                                    int32_t max_pages, int32_t* dev_status, void* stream) {
+sa_status sa::score_impl(const sa_cache* cache, const sa_batch* batch, const void* q,
+                        int32_t num_q_heads, float w_avg, float w_peak, float* scores,
+                        int32_t max_pages, int32_t* dev_status, void* stream) {
   using namespace sa;
   sa_status st = check_cache(cache, false, true);
   if (st != SA_OK) return st;
@@ -312,4 +316,11 @@ extern "C" sa_status sa_score_pages(const sa_cache* cache, const sa_batch* batch
               : launch_score<__half, 128>(a, grid, s, g_sc_smem[1]);
   return bf ? launch_score<__nv_bfloat16, 64>(a, grid, s, g_sc_smem[2])
             : launch_score<__half, 64>(a, grid, s, g_sc_smem[3]);
+}
+
+extern "C" sa_status sa_score_pages(const sa_cache* cache, const sa_batch* batch, const void* q,
+                                    int32_t num_q_heads, float w_avg, float w_peak, float* scores,
+                                    int32_t max_pages, int32_t* dev_status, void* stream) {
+  return sa::score_impl(cache, batch, q, num_q_heads, w_avg, w_peak, scores, max_pages, dev_status,
+                        stream);
 }

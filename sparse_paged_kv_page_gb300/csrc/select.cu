@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   __shared__ int s_digit, s_above;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int unit = b * a.H + h;
+  pdl_wait();                                  // scores and lengths of this step are final
+  pdl_trigger();                               // the decode may start its prologue
   const int L = a.seq_lens[b];
   int n = L > 0 ? (L + a.ps - 1) / a.ps : 0;
   if (n > a.max_pages) {
@@ -155,10 +157,9 @@ int g_sel_smem[64];
 }  // namespace
 }  // namespace sa
 
-extern "C" sa_status sa_select_topk(const float* scores, int32_t max_pages, const sa_batch* batch,
-                                    int32_t page_size, int32_t num_kv_heads, int32_t topk,
-                                    int32_t* sel_idx, int32_t* sel_cnt, int32_t* dev_status,
-                                    void* stream) {
+sa_status sa::select_impl(const float* scores, int32_t max_pages, const sa_batch* batch,
+                         int32_t page_size, int32_t num_kv_heads, int32_t topk, int32_t* sel_idx,
+                         int32_t* sel_cnt, int32_t* dev_status, void* stream, bool pdl) {
   using namespace sa;
   sa_status st = check_batch(batch);
   if (st != SA_OK) return st;
@@ -174,6 +175,16 @@ extern "C" sa_status sa_select_topk(const float* scores, int32_t max_pages, cons
   // static shared memory (the 16 KB histogram) plus the keys may pass the 48 KB default
   if (!ensure_smem(select_kernel, smem, g_sel_smem)) return SA_ERR_CUDA;
   dim3 grid(unsigned(num_kv_heads), unsigned(batch->batch));
-  select_kernel<<<grid, kSelThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
-  return launch_status();
+  return launch_ex(select_kernel, grid, dim3(kSelThreads), size_t(smem), static_cast<cudaStream_t>(stream),
+                   pdl, 1, a) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
+}
+
+extern "C" sa_status sa_select_topk(const float* scores, int32_t max_pages, const sa_batch* batch,
+                                    int32_t page_size, int32_t num_kv_heads, int32_t topk,
+                                    int32_t* sel_idx, int32_t* sel_cnt, int32_t* dev_status,
+                                    void* stream) {
+  return sa::select_impl(scores, max_pages, batch, page_size, num_kv_heads, topk, sel_idx, sel_cnt,
+                         dev_status, stream, false);
 }

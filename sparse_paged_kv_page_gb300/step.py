@@ -1,6 +1,9 @@
 """Decode-step driver: device buffers plus the per-step chain of C-ABI calls.
 
-Page level (page_size > 1):  append -> score -> select -> sparse decode.
+Page level (page_size > 1):  append -> score -> select -> sparse decode, one
+                             ``sa_decode_step`` call (the append of a single
+                             token runs beside the scorer; the tail page's
+                             score entry is then unspecified).
 Token level (page_size 1):   append (+ retained list) -> sparse decode over
                              the retained tokens (logits + lse) -> H2O update.
 
@@ -16,7 +19,8 @@ from typing import Optional, Sequence
 import torch
 
 from .api import (PagedKVCache, alloc_decode_workspace, make_batch, sa_append_kv,
-                  sa_h2o_update, sa_score_pages, sa_select_topk, sa_sparse_decode)
+                  sa_decode_step, sa_h2o_update, sa_score_pages, sa_select_topk,
+                  sa_sparse_decode)
 
 
 class SparseDecoder:
@@ -115,9 +119,17 @@ class SparseDecoder:
 
     def step(self, q: torch.Tensor, k_new: Optional[torch.Tensor] = None,
              v_new: Optional[torch.Tensor] = None):
-        if k_new is not None:
-            self.append(k_new, v_new)
-        return self.attend(q)
+        if self.token_level:
+            if k_new is not None:
+                self.append(k_new, v_new)
+            return self.attend(q)
+        sa_decode_step(self.cache.struct, self.batch, k_new, v_new,
+                       self.decode_cu if k_new is not None else None,
+                       1 if k_new is not None else 0, q, self.H_q, self.w_avg, self.w_peak,
+                       self.scores, self.max_pages, self.topk, self.sel_idx, self.sel_cnt,
+                       self.scale, self.out, lse=self.lse, workspace=self.workspace,
+                       dev_status=self.dev_status)
+        return self.out
 
     # ------------------------------------------------------------------
     def capture(self, append: bool = True):
