@@ -35,6 +35,29 @@ FALLBACK_HBM = 6800.0
 
 
 # ---------------------------------------------------------------------------
+# multi-rank host logic (one process per GPU; no data-path collective)
+# ---------------------------------------------------------------------------
+def rank_config(cfg, rank, world):
+    """Each rank decodes its own independent batch of the same shapes (weak scaling)."""
+    return cfg.replace(seed=cfg.rng_seed + 7919 * rank) if world > 1 else cfg
+
+
+def dist_max(x: float, world: int, device) -> float:
+    """Maximum of a rank-local float over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_steps_per_s(max_ms: float, world: int) -> float:
+    """Whole-job throughput: every rank runs one step of its own batch per step time."""
+    return world * 1000.0 / max_ms
+
+
+# ---------------------------------------------------------------------------
 # byte model
 # ---------------------------------------------------------------------------
 def step_bytes(cfg, lens):
@@ -254,9 +277,7 @@ def run_gpu(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    cfg = config(args.config)
-    if world > 1:
-        cfg = cfg.replace(seed=cfg.rng_seed + 7919 * rank)      # each rank its own batch
+    cfg = rank_config(config(args.config), rank, world)
     append = cfg.decode_steps > 0
     # input schedule: 1 eager step, W warm-up replays, K timed, kernel reps, e2e steps
     n_in = 1 + args.warmup + args.steps + args.kernel_reps + args.e2e_steps
@@ -426,17 +447,13 @@ def run_gpu(args, rank, world):
             b.record(stream)
             marks.append((a, b))
         torch.cuda.synchronize()
-        em = statistics.mean(x.elapsed_time(y) for x, y in marks)
-        e2e = {"value": world * 1000.0 / em, "unit": "steps/s",
+        em = dist_max(statistics.mean(x.elapsed_time(y) for x, y in marks), world, dev)
+        e2e = {"value": aggregate_steps_per_s(em, world), "unit": "steps/s",
                "h2d_bytes_per_step": int((nq + 2 * nk if append else nq) * 2),
                "d2h_bytes_per_step": int(c.B * c.H_q * c.D * 2), "ms_per_step": em}
     status |= int(dec.dev_status.item())
 
-    max_ms = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        max_ms = float(t.item())
+    max_ms = dist_max(ms, world, dev)
     launches = (1 if append else 0) + (2 if token else 3)
     return dict(ms=ms, max_ms=max_ms, wall=wall, clocks=clk.summary(), bytes=bytes_per_step,
                 kern=kern, status=status, score_ab=score_ab, e2e=e2e, cfg=c, wl=wl,
@@ -512,7 +529,7 @@ def main():
         return
     c = res["cfg"]
     hbm_peak, peak_kind = peaks()
-    value = world * 1000.0 / res["max_ms"]
+    value = aggregate_steps_per_s(res["max_ms"], world)
     step_gbs = res["bytes"] / (res["ms"] * 1e-3) / 1e9
     roof = None
     if res["kern"]:
