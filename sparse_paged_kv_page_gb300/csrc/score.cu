@@ -15,16 +15,21 @@
 // G is. The kernel is then a gather of 3 * head_dim * 2 bytes of statistics
 // per (page, KV head) through the block table, bounded by HBM bandwidth.
 //
-// Design: persistent CTAs (two per SM), the batch's pages cut into chunks of
-// 32 pages of one (request, KV head) and the chunk list split evenly across
-// CTAs (a device-side prefix over request lengths, so ragged batches
-// balance). In each CTA one producer warp resolves a chunk's block ids and has
-// the TMA engine gather every page's contiguous statistics rows with one
-// cp.async.bulk per page into a 4-stage shared-memory ring, completion counted
-// in bytes on the stage's mbarrier; four consumer warps score from shared
-// memory (16 lanes per page, one 16-byte slice of each row per lane, shuffle
-// reduction) and release the stage. Block ids of the next chunk are loaded
-// before waiting for a free stage, so the table lookup overlaps the copies.
+// Design: persistent CTAs (two per SM). A block's statistics for all KV heads
+// are one contiguous run (head after head), so the KV heads are taken Hc at a
+// time (Hc = gcd(H_kv, consumer lane groups)) and the batch's pages are cut
+// into chunks of 32 / Hc pages x Hc heads of one request: 32 (page, head)
+// pairs per chunk, one TMA copy of Hc heads' rows per page. The chunk list is
+// split evenly across CTAs (a device-side prefix over request lengths, so
+// ragged batches balance). In each CTA one producer warp resolves a chunk's
+// block ids and has the TMA engine gather the pages with one cp.async.bulk
+// each into a 4-stage shared-memory ring, completion counted in bytes on the
+// stage's mbarrier; four consumer warps score from shared memory (D/8 lanes
+// per (page, head), one 16-byte slice of each row per lane, shuffle reduction;
+// a lane group always serves the same head of the group, so its query
+// coefficients stay in registers) and release the stage. Block ids of the
+// next chunks are loaded before waiting for a free stage, so the table lookup
+// overlaps the copies.
 #include "common.cuh"
 #include "host.h"
 
@@ -55,6 +60,7 @@ struct ScoreArgs {
   float* scores;
   int32_t* status;
   int B, H_kv, H_q, G, ps, num_blocks, bt_stride, max_pages;
+  int hc_shift;                                            // log2(heads per chunk)
   float w_avg, w_peak;
 };
 
@@ -66,7 +72,7 @@ struct ScoreTile {
 };
 
 struct ChunkHdr {
-  int b, h, p0, count;
+  int b, hg, p0, count;                                    // request, head group, pages p0 .. +count
   uint32_t valid;                                          // bit j: page p0+j has a good block
 };
 
@@ -85,9 +91,12 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
   __shared__ int scan_tmp[32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hcs = a.hc_shift, Hc = 1 << hcs;
+  const int P = kChunk >> hcs;                             // pages per chunk
+  const int n_hg = a.H_kv >> hcs;                          // head groups
   pdl_wait();
 
-  // chunk prefix over requests: request b owns H_kv * ceil(n_b / kChunk) chunks
+  // chunk prefix over requests: request b owns n_hg * ceil(n_b / P) chunks
   {
     const int per = (a.B + kScThreads - 1) / kScThreads;
     const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
@@ -95,7 +104,7 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
     for (int b = b0; b < b1; ++b) {
       int n = (a.seq_lens[b] + a.ps - 1) / a.ps;
       n = max(0, min(n, min(a.max_pages, a.bt_stride)));
-      local += a.H_kv * ((n + kChunk - 1) / kChunk);
+      local += n_hg * ((n + P - 1) / P);
     }
     int total;
     int run = block_exclusive_scan<kScThreads>(local, scan_tmp, &total);
@@ -104,7 +113,7 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
       int n = (a.seq_lens[b] + a.ps - 1) / a.ps;
       n = max(0, min(n, min(a.max_pages, a.bt_stride)));
       s_pages[b] = n;
-      run += a.H_kv * ((n + kChunk - 1) / kChunk);
+      run += n_hg * ((n + P - 1) / P);
     }
     if (tid == 0) s_prefix[a.B] = total;
     if (tid == 0 && blockIdx.x == 0)
@@ -132,7 +141,7 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    auto locate = [&](int ci, int& b, int& h, int& p0, int& count) {
+    auto locate = [&](int ci, int& b, int& hg, int& p0, int& count) {
       int lo = 0, hi = a.B;                                // largest b with prefix[b] <= ci
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -140,26 +149,26 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
       }
       b = lo;
       const int n = s_pages[b];
-      const int kb = (n + kChunk - 1) / kChunk;
+      const int kb = (n + P - 1) / P;
       const int r = ci - s_prefix[b];
-      h = r / kb;
-      p0 = (r % kb) * kChunk;
-      count = min(kChunk, n - p0);
+      hg = r / kb;
+      p0 = (r % kb) * P;
+      count = min(P, n - p0);
     };
     // block ids of the next two chunks are in flight while a stage is waited for
-    int b1, h1, p01, c1, k1 = -1, b2 = 0, h2 = 0, p02 = 0, c2 = 0, k2 = -1;
-    locate(c_begin, b1, h1, p01, c1);
+    int b1, g1, p01, c1, k1 = -1, b2 = 0, g2 = 0, p02 = 0, c2 = 0, k2 = -1;
+    locate(c_begin, b1, g1, p01, c1);
     k1 = lane < c1 ? a.bt[int64_t(b1) * a.bt_stride + p01 + lane] : -1;
     if (c_begin + 1 < c_end) {
-      locate(c_begin + 1, b2, h2, p02, c2);
+      locate(c_begin + 1, b2, g2, p02, c2);
       k2 = lane < c2 ? a.bt[int64_t(b2) * a.bt_stride + p02 + lane] : -1;
     }
     bool ok = true;
     for (int ci = c_begin, it = 0; ci < c_end; ++ci, ++it) {
-      const int b = b1, h = h1, p0 = p01, count = c1, blk = k1;
-      b1 = b2; h1 = h2; p01 = p02; c1 = c2; k1 = k2;
+      const int b = b1, hg = g1, p0 = p01, count = c1, blk = k1;
+      b1 = b2; g1 = g2; p01 = p02; c1 = c2; k1 = k2;
       if (ci + 2 < c_end) {
-        locate(ci + 2, b2, h2, p02, c2);
+        locate(ci + 2, b2, g2, p02, c2);
         k2 = lane < c2 ? a.bt[int64_t(b2) * a.bt_stride + p02 + lane] : -1;
       }
       const int s = it % kStages;
@@ -170,16 +179,17 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
       const bool good = lane < count && blk >= 0 && blk < a.num_blocks;
       if (lane < count && !good) flag(a.status, SA_DEV_BAD_BLOCK);
       const uint32_t valid = __ballot_sync(kFull, good);
+      const uint32_t bytes = uint32_t(TL::kPageBytes) << hcs;   // Hc heads of one block
       if (lane == 0) {
-        hdr[s] = ChunkHdr{b, h, p0, count, valid};
-        mbar_arrive_expect_tx(smem_u32(&full_bar[s]), uint32_t(__popc(valid)) * TL::kPageBytes);
+        hdr[s] = ChunkHdr{b, hg, p0, count, valid};
+        mbar_arrive_expect_tx(smem_u32(&full_bar[s]), uint32_t(__popc(valid)) * bytes);
       }
       __syncwarp();
       if (good) {
         const uint8_t* src = static_cast<const uint8_t*>(a.meta) +
-                             (int64_t(blk) * a.H_kv + h) * int64_t(TL::kPageBytes);
-        bulk_g2s(smem_u32(smem + s * TL::kStageBytes + lane * TL::kPageBytes), src,
-                 TL::kPageBytes, smem_u32(&full_bar[s]));
+                             (int64_t(blk) * a.H_kv + (hg << hcs)) * int64_t(TL::kPageBytes);
+        bulk_g2s(smem_u32(smem + s * TL::kStageBytes + lane * bytes), src, bytes,
+                 smem_u32(&full_bar[s]));
       }
     }
     // never leave with copies in flight: wait (bounded) for the last stages
@@ -192,16 +202,20 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
   }
 
   // -------------------------------------------------------------- consumers
+  // lane group grp serves (page, head) pairs grp, grp + PPP, ... of a chunk;
+  // PPP is a multiple of Hc, so its head within the group is always grp % Hc
   const int grp = tid / LPP, l = tid % LPP;
+  const int hl = grp & (Hc - 1);
   float ca[8], cp[8], cn[8];
   int cur_b = -1, cur_h = -1;
   for (int ci = c_begin, it = 0; ci < c_end; ++ci, ++it) {
     const int s = it % kStages;
     if (!mbar_wait(smem_u32(&full_bar[s]), (it / kStages) & 1, a.status)) break;
     const ChunkHdr hd = hdr[s];
-    if (hd.b != cur_b || hd.h != cur_h) {
+    const int head = (hd.hg << hcs) + hl;
+    if (hd.b != cur_b || head != cur_h) {
       cur_b = hd.b;
-      cur_h = hd.h;
+      cur_h = head;
 #pragma unroll
       for (int e = 0; e < 8; ++e) ca[e] = cp[e] = cn[e] = 0.f;
       const T* qh = static_cast<const T*>(a.q) + (int64_t(cur_b) * a.H_q + int64_t(cur_h) * a.G) * D + l * 8;
@@ -226,15 +240,16 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
 #pragma unroll
       for (int e = 0; e < 8; ++e) { ca[e] *= ia; cp[e] *= ip; cn[e] *= ip; }
     }
-    float* out = a.scores + (int64_t(hd.b) * a.H_kv + hd.h) * a.max_pages + hd.p0;
+    float* out = a.scores + (int64_t(hd.b) * a.H_kv + head) * a.max_pages + hd.p0;
     const uint8_t* st = smem + s * TL::kStageBytes;
 #pragma unroll
     for (int pass = 0; pass < kChunk / PPP; ++pass) {
-      const int j = pass * PPP + grp;
+      const int ph = pass * PPP + grp;                     // (page, head) pair of the chunk
+      const int j = ph >> hcs;                             // its page
       const bool here = j < hd.count && ((hd.valid >> j) & 1u);
       float acc = 0.f;
       if (here) {
-        const uint8_t* pg = st + j * TL::kPageBytes + l * 16;
+        const uint8_t* pg = st + ph * TL::kPageBytes + l * 16;
         const uint4 vmn = *reinterpret_cast<const uint4*>(pg);
         const uint4 vmx = *reinterpret_cast<const uint4*>(pg + D * 2);
         const uint4 vme = *reinterpret_cast<const uint4*>(pg + 2 * D * 2);
@@ -304,9 +319,16 @@ sa_status sa::score_impl(const sa_cache* cache, const sa_batch* batch, const voi
   a.B = batch->batch; a.H_kv = cache->num_kv_heads; a.H_q = num_q_heads; a.G = G;
   a.ps = cache->page_size; a.num_blocks = cache->num_blocks; a.bt_stride = batch->bt_stride;
   a.max_pages = max_pages; a.w_avg = w_avg; a.w_peak = w_peak;
+  // heads per chunk: the largest power of two dividing both H_kv and the
+  // consumers' lane groups (128 / (head_dim / 8))
+  const int groups = 32 * kConsumerWarps / (cache->head_dim / 8);
+  int hc = 1;
+  while (hc < groups && a.H_kv % (2 * hc) == 0) hc *= 2;
+  a.hc_shift = log2i(hc);
   // enough persistent CTAs for two per SM, never more than chunks could exist
   const int cap = max_pages < batch->bt_stride ? max_pages : batch->bt_stride;
-  const int64_t max_chunks = int64_t(batch->batch) * a.H_kv * ((cap + kChunk - 1) / kChunk);
+  const int per_chunk = kChunk / hc;
+  const int64_t max_chunks = int64_t(batch->batch) * (a.H_kv / hc) * ((cap + per_chunk - 1) / per_chunk);
   const int full = kCtasPerSm * sm_count();
   const int grid = int(max_chunks < full ? max_chunks : full);
   cudaStream_t s = static_cast<cudaStream_t>(stream);

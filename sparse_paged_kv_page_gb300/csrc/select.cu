@@ -9,9 +9,10 @@
 // 32-bit keys in shared memory; a most-significant-digit radix select
 // (12-, 12- and 8-bit digits, early exit once a digit bin is taken whole) finds the
 // key K of the (topk-1)-th best candidate and how many candidates equal to K
-// to keep; those are the lowest-indexed ones. Two block-wide prefix sums in
-// page order then give each kept page its slot, so the output is ascending
-// without sorting and the result is deterministic.
+// to keep; those are the lowest-indexed ones. Warp ballots over contiguous
+// segments, with one exchange of per-warp counts, then give each kept page its
+// slot in page order, so the output is ascending without sorting and the
+// result is deterministic.
 #include "common.cuh"
 #include "host.h"
 
@@ -23,8 +24,9 @@ namespace {
 #endif
 constexpr int kSelThreads = SA_SELECT_THREADS;
 constexpr int kBpt = 4096 / kSelThreads;   // histogram bins owned per thread in the digit search
-static_assert(4096 % kSelThreads == 0, "threads must divide the 4096 bins");
-constexpr int kSelMaxPages = 45056;      // keys in shared memory next to a 16 KB histogram
+constexpr int kWarps = kSelThreads / 32;
+static_assert(kSelThreads == 1024, "the digit search maps 4096 bins and 32 warps onto the block");
+constexpr int kSelMaxPages = 45056;      // keys in shared memory next to two 16 KB histograms
 
 struct SelArgs {
   const float* scores;
@@ -37,13 +39,23 @@ struct SelArgs {
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   extern __shared__ uint32_t keys[];
-  __shared__ int hist[4096];
-  __shared__ int scan_tmp[32];
-  __shared__ int s_digit, s_above;
+  __shared__ int hist[2][4096];                  // digit histograms, alternating per pass
+  __shared__ int s_wt[kWarps], s_gt[kWarps], s_eq[kWarps];
+  __shared__ int s_digit, s_above, s_whole;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   const int unit = b * a.H + h;
   pdl_wait();                                  // scores and lengths of this step are final
   pdl_trigger();                               // the decode may start its prologue
+  // The first 8 * kSelThreads scores are loaded together with the length (the
+  // row holds max_pages entries; entries past the length are ignored).
+  const float* sc = a.scores + int64_t(unit) * a.max_pages;
+  float v0[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int i = u * kSelThreads + tid;
+    v0[u] = i < a.max_pages ? sc[i] : 0.f;
+  }
   const int L = a.seq_lens[b];
   int n = L > 0 ? (L + a.ps - 1) / a.ps : 0;
   if (n > a.max_pages) {
@@ -62,8 +74,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     if (tid == 0) { out[0] = n - 1; a.sel_cnt[unit] = 1; }
     return;
   }
-  const float* sc = a.scores + int64_t(unit) * a.max_pages;
-  for (int i0 = 0; i0 < nc; i0 += 8 * kSelThreads) {      // 8 independent loads per thread
+  for (int i = tid; i < 2 * 4096; i += kSelThreads) (&hist[0][0])[i] = 0;
+  __syncthreads();
+  // keys to shared memory; the first digit's histogram straight from registers
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int i = u * kSelThreads + tid;
+    if (i < nc) {
+      const uint32_t k = f32_key(v0[u]);
+      keys[i] = k;
+      atomicAdd(&hist[0][k >> 20], 1);
+    }
+  }
+  for (int i0 = 8 * kSelThreads; i0 < nc; i0 += 8 * kSelThreads) {   // long rows
     float v[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -73,78 +96,118 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = i0 + u * kSelThreads + tid;
-      if (i < nc) keys[i] = f32_key(v[u]);
+      if (i < nc) {
+        const uint32_t k = f32_key(v[u]);
+        keys[i] = k;
+        atomicAdd(&hist[0][k >> 20], 1);
+      }
     }
   }
 
   // Radix select from the most significant digit: 12, 12 and 8 bits. (The top
   // byte of a float key is the sign and high exponent bits -- a 12-bit first
   // digit also takes three mantissa bits, so the first pass already splits
-  // typical score distributions into many bins.)
+  // typical score distributions into many bins.) Warp w owns a contiguous run
+  // of bins from the top, lane l kBpt of them, so the bin holding the
+  // remaining-th largest key is found with two barriers per digit.
   uint32_t prefix = 0, mask = 0;
   int remaining = kprime;                        // still to take among keys matching prefix
   for (int pass = 0; pass < 3; ++pass) {
     const int width = pass < 2 ? 12 : 8;
     const int shift = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
     const int nbins = 1 << width;
-    for (int i = tid; i < nbins; i += kSelThreads) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < nc; i += kSelThreads) {
-      const uint32_t k = keys[i];
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & uint32_t(nbins - 1)], 1);
+    int* hp = hist[pass & 1];
+    if (pass > 0) {
+      for (int i = tid; i < nc; i += kSelThreads) {
+        const uint32_t k = keys[i];
+        if ((k & mask) == prefix) atomicAdd(&hp[(k >> shift) & uint32_t(nbins - 1)], 1);
+      }
     }
-    __syncthreads();
-    // thread t owns bins nbins-1-kBpt*t-j (j < kBpt), i.e. scanned from the top
-    int c[kBpt], sum = 0;
+    __syncthreads();                             // histogram complete
+    const int bpl = nbins / kSelThreads;         // bins per lane: 4 (12-bit) or 0 (8-bit)
+    int c[kBpt], sum = 0, top;
+    if (bpl) {
+      top = nbins - 1 - kBpt * tid;              // lane's bins top, top-1, ..., top-kBpt+1
+#pragma unroll
+      for (int j = 0; j < kBpt; ++j) { c[j] = hp[top - j]; sum += c[j]; }
+    } else {                                     // 256 bins: one per thread of warps 0..7
+      top = nbins - 1 - tid;
+#pragma unroll
+      for (int j = 0; j < kBpt; ++j) c[j] = 0;
+      if (tid < nbins) { c[0] = hp[top]; sum = c[0]; }
+    }
+    int incl = sum;                              // inclusive scan over the warp's lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wt[warp] = incl;
+    __syncthreads();                             // warp totals published, histogram read
+    if (pass == 0)                               // the third digit reuses this buffer
+      for (int i = tid; i < 256; i += kSelThreads) hist[0][i] = 0;
+    int wt = lane < kWarps ? s_wt[lane] : 0;
+    int wincl = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, wincl, o);
+      if (lane >= o) wincl += y;
+    }
+    const int wbefore = __shfl_sync(kFull, wincl - wt, warp);
+    int run = wbefore + incl - sum;              // keys in bins above this lane's first bin
 #pragma unroll
     for (int j = 0; j < kBpt; ++j) {
-      const int bin = nbins - 1 - kBpt * tid - j;
-      c[j] = bin >= 0 ? hist[bin] : 0;
-      sum += c[j];
-    }
-    int total;
-    int run = block_exclusive_scan<kSelThreads>(sum, scan_tmp, &total);
-#pragma unroll
-    for (int j = 0; j < kBpt; ++j) {
-      if (run < remaining && remaining <= run + c[j]) { s_digit = nbins - 1 - kBpt * tid - j; s_above = run; }
+      if (run < remaining && remaining <= run + c[j]) {
+        s_digit = top - j;
+        s_above = run;
+        s_whole = (run + c[j] == remaining);
+      }
       run += c[j];
     }
-    __syncthreads();
+    __syncthreads();                             // digit published
     const int d = s_digit;
     remaining -= s_above;
     prefix |= uint32_t(d) << shift;
     mask |= uint32_t(nbins - 1) << shift;
-    const bool whole = hist[d] == remaining;
-    __syncthreads();                             // everyone has read hist before it is reset
-    if (whole) break;
+    if (s_whole) break;
   }
 
-  // keep: (key & mask) > prefix, or == prefix among the first `remaining` in page order
-  const int per = (nc + kSelThreads - 1) / kSelThreads;
-  const int c0 = min(nc, tid * per), c1 = min(nc, c0 + per);
-  int eq_local = 0;
-  for (int i = c0; i < c1; ++i) eq_local += (keys[i] & mask) == prefix;
-  int total;
-  const int eq_before = block_exclusive_scan<kSelThreads>(eq_local, scan_tmp, &total);
-  int take_local = 0;
-  {
-    int e = eq_before;
-    for (int i = c0; i < c1; ++i) {
-      const uint32_t k = keys[i] & mask;
-      if (k > prefix) ++take_local;
-      else if (k == prefix) { take_local += e < remaining; ++e; }
-    }
+  // keep: (key & mask) > prefix, or == prefix among the first `remaining` in
+  // page order. Warp w walks a contiguous segment in rounds of 32; ballots
+  // count and rank within a round, one barrier shares the per-warp counts.
+  const int seg = (((nc + kWarps - 1) / kWarps) + 31) & ~31;
+  const int s0 = warp * seg, s1 = min(nc, s0 + seg);
+  const uint32_t lt = (1u << lane) - 1u;
+  int gt = 0, eq = 0;
+  for (int base = s0; base < s1; base += 32) {
+    const int i = base + lane;
+    const uint32_t k = i < s1 ? keys[i] & mask : 0u;
+    gt += __popc(__ballot_sync(kFull, i < s1 && k > prefix));
+    eq += __popc(__ballot_sync(kFull, i < s1 && k == prefix));
   }
-  const int take_before = block_exclusive_scan<kSelThreads>(take_local, scan_tmp, &total);
-  {
-    int e = eq_before, o = take_before;
-    for (int i = c0; i < c1; ++i) {
-      const uint32_t k = keys[i] & mask;
-      bool take = false;
-      if (k > prefix) take = true;
-      else if (k == prefix) { take = e < remaining; ++e; }
-      if (take && o < kprime) out[o++] = i;
-    }
+  if (lane == 0) { s_gt[warp] = gt; s_eq[warp] = eq; }
+  __syncthreads();
+  int g = lane < kWarps ? s_gt[lane] : 0, e = lane < kWarps ? s_eq[lane] : 0;
+  const int g_own = g, e_own = e;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int yg = __shfl_up_sync(kFull, g, o), ye = __shfl_up_sync(kFull, e, o);
+    if (lane >= o) { g += yg; e += ye; }
+  }
+  const int gt_before = __shfl_sync(kFull, g - g_own, warp);
+  int eq_run = __shfl_sync(kFull, e - e_own, warp);
+  int take_run = gt_before + min(eq_run, remaining);
+  for (int base = s0; base < s1; base += 32) {
+    const int i = base + lane;
+    const uint32_t k = i < s1 ? keys[i] & mask : 0u;
+    const bool is_gt = i < s1 && k > prefix, is_eq = i < s1 && k == prefix;
+    const uint32_t meq = __ballot_sync(kFull, is_eq);
+    const bool take = is_gt || (is_eq && eq_run + __popc(meq & lt) < remaining);
+    const uint32_t mt = __ballot_sync(kFull, take);
+    const int pos = take_run + __popc(mt & lt);
+    if (take && pos < kprime) out[pos] = i;
+    eq_run += __popc(meq);
+    take_run += __popc(mt);
   }
   if (tid == 0) {
     out[kprime] = n - 1;                         // the tail is the largest index

@@ -73,6 +73,24 @@ def test_scores_group_sizes(G, D, dtype):
             assert_scores(scores[b, h, :O.num_pages(L, cfg.ps)], S, A)
 
 
+@pytest.mark.parametrize("H_kv", [3, 6, 8, 12, 16])
+@pytest.mark.parametrize("D", [128, 64])
+def test_scores_kv_head_counts(H_kv, D):
+    """Chunks gather several KV heads of a block per copy (as many as divide
+    both H_kv and the lane groups): counts that split into 1, 2, 4, 8 or 16."""
+    cfg = config(3, small=True).replace(H_q=2 * H_kv, H_kv=H_kv, D=D, len_range=(5, 700),
+                                        w_avg=0.6, w_peak=0.4)
+    wl = make_workload(cfg)
+    dec = make_decoder(wl)
+    qb = _run_scores(dec, wl, 0)
+    scores = dec.scores.cpu().numpy()
+    for b in range(cfg.B):
+        for h in range(cfg.H_kv):
+            S, A, L = _oracle_scores(wl, b, h, 0, qb[b])
+            assert_scores(scores[b, h, :O.num_pages(L, cfg.ps)], S, A)
+    assert dev_status(dec) == 0
+
+
 def _run_select(scores_np, lens, ps, topk, H):
     from sparse_paged_kv_page_gb300 import make_batch, sa_select_topk
     B, _, maxp = scores_np.shape
