@@ -235,6 +235,24 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // programmatic dependent launch (no-ops unless the launch asked for it)
 // ---------------------------------------------------------------------------
 // Let the next kernel in the stream, if launched programmatically, start now.
+// The SFU's approximate base-2 exponential, base-2 logarithm and reciprocal
+// (single PTX instructions; subnormal results and inputs flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }

@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   __shared__ uint32_t s_mask[kWarps][kStages];
   __shared__ __align__(8) uint64_t s_bar[kWarps][kStages];
   __shared__ int s_last;
+  __shared__ float s_sf[kWarps][16];           // per-warp weights of each output row
+  __shared__ float s_rl[16];                   // this CTA's lse of each row
   // 1024-byte aligned base for the swizzled tiles
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
@@ -143,30 +145,44 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // lengths and selection come from the kernels before this one in the step
   pdl_wait();
 
+  // This CTA's range of selection entries is a function of the count. The
+  // entry it would start at with a full selection (the usual case) is loaded
+  // together with the count, so the block lookups start one round trip early;
+  // the value is used only if the real range starts there too.
+  const int32_t* sel = a.sel + int64_t(unit) * a.sel_stride;
+  auto entry_range = [&](int count, int& e_begin, int& e_cnt, int& t_begin, int& t_end, int& n_rows) {
+    n_rows = count << pss;
+    const int n_tiles = (n_rows + 15) >> 4;
+    const int per = (n_tiles + a.nsplit - 1) / a.nsplit;
+    t_begin = min(n_tiles, split * per);
+    t_end = min(n_tiles, t_begin + per);
+    const int row_begin = t_begin << 4, row_end = min(t_end << 4, n_rows);
+    e_begin = row_begin >> pss;
+    e_cnt = row_end > row_begin ? min(((row_end - 1) >> pss) - e_begin + 1, a.ent_max) : 0;
+  };
+  int eb_s, ec_s, tb_s, te_s, nr_s;
+  entry_range(a.sel_stride, eb_s, ec_s, tb_s, te_s, nr_s);
+  const int spec_page = threadIdx.x < ec_s ? sel[eb_s + threadIdx.x] : -1;
+
   const int L = a.seq_lens[b];
   int cnt = a.cnt[unit];
   if (cnt < 0 || cnt > a.sel_stride) {
     if (threadIdx.x == 0 && split == 0) flag(a.status, SA_DEV_BAD_COUNT);
     cnt = cnt < 0 ? 0 : a.sel_stride;
   }
-  const int n_rows = cnt << pss;
-  const int n_tiles = (n_rows + 15) >> 4;
-  const int per = (n_tiles + a.nsplit - 1) / a.nsplit;
-  const int t_begin = min(n_tiles, split * per), t_end = min(n_tiles, t_begin + per);
+  int e_begin, e_cnt, t_begin, t_end, n_rows;
+  entry_range(cnt, e_begin, e_cnt, t_begin, t_end, n_rows);
+  const int row_end = min(t_end << 4, n_rows);
   const int n_pages_req = L > 0 ? (L + ps - 1) >> pss : 0;
-  const int32_t* sel = a.sel + int64_t(unit) * a.sel_stride;
   const int32_t* btb = a.bt + int64_t(b) * a.bt_stride;
 
   // Prologue: resolve the selection entries this CTA touches to (block, fill)
   // once, in parallel, so the copy loop never waits on sel -> block table.
   int2* s_ent = reinterpret_cast<int2*>(smem_raw + TL::kSmem);
-  const int row_begin = t_begin << 4, row_end = min(t_end << 4, n_rows);
-  const int e_begin = row_begin >> pss;
-  const int e_cnt = row_end > row_begin ? min(((row_end - 1) >> pss) - e_begin + 1, a.ent_max) : 0;
   for (int i = threadIdx.x; i < e_cnt; i += kThreads) {
     const int e = e_begin + i;
     int blk = -1, fill = 0;
-    const int page = sel[e];
+    const int page = (e == eb_s + int(threadIdx.x) && int(threadIdx.x) < ec_s) ? spec_page : sel[e];
     if (page < 0 || page >= n_pages_req || page >= a.bt_stride) {
       flag(a.status, SA_DEV_BAD_BLOCK);
     } else {
@@ -332,13 +348,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       pmax[r] = fmaxf(pmax[r], __shfl_xor_sync(kFull, pmax[r], 2));
       const float m_new = fmaxf(m_r[r], pmax[r]);
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = exp2f(m_r[r] - m_use);
+      const float alpha = ex2_approx(m_r[r] - m_use);
       float rs = 0.f;
 #pragma unroll
       for (int nt2 = 0; nt2 < 2; ++nt2) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float p = exp2f(c[nt2][2 * r + e] - m_use);
+          const float p = ex2_approx(c[nt2][2 * r + e] - m_use);
           c[nt2][2 * r + e] = p;
           rs += p;
         }
@@ -379,10 +395,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
 
-  // merge the 4 warps in shared memory (reusing the tile buffers)
+  // merge the 4 warps in shared memory (reusing the tile buffers): each row's
+  // weights once, then one weighted sum per output element
   constexpr int WS = D + 4;                                    // padded row: no bank conflicts
-  float* wm = reinterpret_cast<float*>(smem);                 // [kWarps][16]
-  float* wl = wm + kWarps * 16;                                // [kWarps][16]
+  float* wm = reinterpret_cast<float*>(smem);                 // [kWarps][16] row maxima (log2)
+  float* wl = wm + kWarps * 16;                                // [kWarps][16] row sums
   float* wo = wl + kWarps * 16;                                // [kWarps][G][WS]
   if (tq == 0) {
     if (g < G) { wm[warp * 16 + g] = m_r[0]; wl[warp * 16 + g] = l_r[0]; }
@@ -401,36 +418,41 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   }
   __syncthreads();
-  const bool single = a.nsplit == 1;
-  T* outp = static_cast<T*>(a.out) + (int64_t(b) * a.H_q + int64_t(h) * G) * D;
-  for (int idx = threadIdx.x; idx < G * D && !(kCluster && !single); idx += kThreads) {
-    const int row = idx / D, d = idx % D;
+  if (threadIdx.x < G) {
+    const int row = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 16 + row]);
-    float acc = 0.f, tot = 0.f;
-    if (M != -INFINITY) {
+    float f[kWarps], tot = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = wm[w * 16 + row];
-        if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - M);
-        acc += wo[(w * G + row) * WS + d] * f;
-        tot += wl[w * 16 + row] * f;
-      }
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = wm[w * 16 + row];
+      f[w] = mw == -INFINITY ? 0.f : ex2_approx(mw - M);      // a warp without tokens weighs 0
+      tot = fmaf(wl[w * 16 + row], f[w], tot);
     }
-    const float os = tot > 0.f ? acc / tot : 0.f;
-    const float ls = tot > 0.f ? (M + log2f(tot)) * kLn2 : -INFINITY;
-    if (single) {
-      reinterpret_cast<uint16_t*>(outp)[row * D + d] = E::from_f(os);
-      if (a.lse && d == 0) a.lse[int64_t(b) * a.H_q + int64_t(h) * G + row] = ls;
-    } else {
-      const int64_t pi = (int64_t(unit) * a.nsplit + split) * G + row;
-      a.part_o[pi * D + d] = os;
-      if (d == 0) a.part_lse[pi] = ls;
-    }
+    const float inv = tot > 0.f ? rcp_approx(tot) : 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s_sf[w][row] = f[w] * inv;
+    s_rl[row] = tot > 0.f ? (M + lg2_approx(tot)) * kLn2 : -INFINITY;
   }
-  if (single) return;
+  __syncthreads();
+  // this CTA's normalised output of element (row, d)
+  auto merged = [&](int row, int d) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float sf = s_sf[w][row];
+      if (sf != 0.f) acc = fmaf(wo[(w * G + row) * WS + d], sf, acc);
+    }
+    return acc;
+  };
+  T* outp = static_cast<T*>(a.out) + (int64_t(b) * a.H_q + int64_t(h) * G) * D;
+  if (a.nsplit == 1) {
+    for (int idx = threadIdx.x; idx < G * D; idx += kThreads)
+      reinterpret_cast<uint16_t*>(outp)[idx] = E::from_f(merged(idx / D, idx % D));
+    if (a.lse && threadIdx.x < G) a.lse[int64_t(b) * a.H_q + int64_t(h) * G + threadIdx.x] = s_rl[threadIdx.x];
+    return;
+  }
 
   if constexpr (kCluster) {
     // The unit's nsplit CTAs form one cluster. Each leaves its partial in its
@@ -438,61 +460,50 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // slice of the unit's G*D outputs from every peer's partial over DSMEM; a
     // second barrier keeps all shared memory alive until every peer is done.
     float* cl_o = reinterpret_cast<float*>(smem + kClusterOff);   // [G][D]
-    float* cl_lse = cl_o + 16 * D;                                 // [G]
-    for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
-      const int row = idx / D, d = idx % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * 16 + row]);
-      float acc = 0.f, tot = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float mw = wm[w * 16 + row];
-          if (mw == -INFINITY) continue;
-          const float f = exp2f(mw - M);
-          acc += wo[(w * G + row) * WS + d] * f;
-          tot += wl[w * 16 + row] * f;
-        }
-      }
-      cl_o[row * D + d] = tot > 0.f ? acc / tot : 0.f;
-      if (d == 0) cl_lse[row] = tot > 0.f ? (M + log2f(tot)) * kLn2 : -INFINITY;
-    }
+    float* cl_lse = cl_o + 16 * D;                                 // [G] natural log
+    for (int idx = threadIdx.x; idx < G * D; idx += kThreads) cl_o[idx] = merged(idx / D, idx % D);
+    if (threadIdx.x < G) cl_lse[threadIdx.x] = s_rl[threadIdx.x];
     cluster_sync();
     const int ns = a.nsplit;
     const int n_el = G * D, chunk = (n_el + ns - 1) / ns;
     const int e0 = int(cluster_rank()) * chunk, e1 = min(n_el, e0 + chunk);
     const uint32_t o_base = smem_u32(cl_o), l_base = smem_u32(cl_lse);
     for (int idx = e0 + threadIdx.x; idx < e1; idx += kThreads) {
-      const int row = idx / D, d = idx % D;
+      const int row = idx / D;
+      // the row's lse and the element from every peer, all loads in flight at once
       float lv[kMaxCluster], ov[kMaxCluster];
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r) {
         lv[r] = r < ns ? dsmem_ld_f32(dsmem_map(l_base + 4u * row, r)) : -INFINITY;
-        ov[r] = r < ns ? dsmem_ld_f32(dsmem_map(o_base + 4u * (row * D + d), r)) : 0.f;
+        ov[r] = r < ns ? dsmem_ld_f32(dsmem_map(o_base + 4u * idx, r)) : 0.f;
       }
       float M = -INFINITY;
 #pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, lv[r] == INFINITY ? -INFINITY : lv[r]);
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (lv[r] < INFINITY) M = fmaxf(M, lv[r]);
       float acc = 0.f, tot = 0.f;
-      if (M != -INFINITY) {
 #pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r) {
-          if (!(lv[r] > -INFINITY) || lv[r] == INFINITY) continue;
-          const float w = expf(lv[r] - M);
-          acc += w * ov[r];
-          tot += w;
-        }
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (!(lv[r] > -INFINITY && lv[r] < INFINITY)) continue;   // an empty (or broken) partial
+        const float w = ex2_approx((lv[r] - M) * kLog2e);
+        acc = fmaf(w, ov[r], acc);
+        tot += w;
       }
-      reinterpret_cast<uint16_t*>(outp)[row * D + d] = E::from_f(tot > 0.f ? acc / tot : 0.f);
-      if (a.lse && d == 0)
-        a.lse[int64_t(b) * a.H_q + int64_t(h) * G + row] = tot > 0.f ? M + logf(tot) : -INFINITY;
+      reinterpret_cast<uint16_t*>(outp)[idx] = E::from_f(tot > 0.f ? acc * rcp_approx(tot) : 0.f);
+      if (a.lse && idx % D == 0)
+        a.lse[int64_t(b) * a.H_q + int64_t(h) * G + row] = tot > 0.f ? M + lg2_approx(tot) * kLn2 : -INFINITY;
     }
     cluster_sync();
     return;
   }
 
-  // last CTA of the unit merges the partials
+  // ticket merge: partials to the workspace, the last CTA of the unit merges
+  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+    const int row = idx / D;
+    const int64_t pi = (int64_t(unit) * a.nsplit + split) * G + row;
+    a.part_o[pi * D + idx % D] = merged(row, idx % D);
+  }
+  if (threadIdx.x < G) a.part_lse[(int64_t(unit) * a.nsplit + split) * G + threadIdx.x] = s_rl[threadIdx.x];
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_last = atomicAdd(&a.tickets[unit], 1) == a.nsplit - 1;
@@ -519,17 +530,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   for (int i = threadIdx.x; i < a.nsplit * G; i += kThreads) {
     const float M = rmax[i % G];
     const float v = wgt[i];
-    wgt[i] = (M == -INFINITY || v == -INFINITY) ? 0.f : expf(v - M);
+    wgt[i] = (M == -INFINITY || v == -INFINITY) ? 0.f : ex2_approx((v - M) * kLog2e);
   }
   __syncthreads();
   if (threadIdx.x < G) {
     const int row = threadIdx.x;
     float t = 0.f;
     for (int s = 0; s < a.nsplit; ++s) t += wgt[s * G + row];
-    rtot[row] = t;
+    rtot[row] = t > 0.f ? rcp_approx(t) : 0.f;
     if (a.lse)
       a.lse[int64_t(b) * a.H_q + int64_t(h) * G + row] =
-          t > 0.f ? rmax[row] + logf(t) : -INFINITY;
+          t > 0.f ? rmax[row] + lg2_approx(t) * kLn2 : -INFINITY;
   }
   __syncthreads();
   // every output element of the unit: sum over splits, loads issued 4 splits
@@ -566,11 +577,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
   for (int k = 0; k < kOut; ++k) {
     const int idx = threadIdx.x + k * kThreads;
-    if (idx < n_el) {
-      const int row = idx / D, d = idx % D;
-      const float t = rtot[row];
-      reinterpret_cast<uint16_t*>(outp)[row * D + d] = E::from_f(t > 0.f ? acc[k] / t : 0.f);
-    }
+    if (idx < n_el) reinterpret_cast<uint16_t*>(outp)[idx] = E::from_f(acc[k] * rtot[idx / D]);
   }
   if (threadIdx.x == 0) a.tickets[unit] = 0;
 }
