@@ -494,9 +494,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         a.lse[int64_t(b) * a.H_q + int64_t(h) * G + row] = tot > 0.f ? M + lg2_approx(tot) * kLn2 : -INFINITY;
     }
     cluster_sync();
-    return;
-  }
-
+  } else {
   // ticket merge: partials to the workspace, the last CTA of the unit merges
   for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
     const int row = idx / D;
@@ -580,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (idx < n_el) reinterpret_cast<uint16_t*>(outp)[idx] = E::from_f(acc[k] * rtot[idx / D]);
   }
   if (threadIdx.x == 0) a.tickets[unit] = 0;
+  }  // ticket merge
 }
 
 int num_sms() {
