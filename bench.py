@@ -104,7 +104,10 @@ def traffic_from_profile(kernel_file, name):
         for line in open(path):
             if ":" in line:
                 k, v = line.split(":", 1)
-                vals[k.strip().strip("-* `")] = v.strip().strip("` ")
+                v = v.strip()
+                if v.startswith("`"):                      # `value` (comment)
+                    v = v[1:].split("`", 1)[0]
+                vals[k.strip().strip("-* `")] = v.split()[0] if v else v
         if vals.get("source_sha256") != sha:
             return None
         return float(vals["dram_bytes_per_launch_full_size"])
