@@ -131,6 +131,23 @@ def test_select_bit_exact_on_generated_scores(kind, topk):
             assert np.all(sel[b, h, cnt[b, h]:] == -7)
 
 
+@pytest.mark.parametrize("maxp", [2048, 2049, 8192, 9000, 16384, 16385])
+def test_select_row_lengths(maxp):
+    """Rows of up to 16 K pages keep their keys in registers (2, 4, 8 or 16 per
+    thread); longer rows in shared memory: both sides of every boundary."""
+    rng = np.random.default_rng([91, maxp])
+    B, H, ps = 2, 2, 16
+    s = rng.standard_normal((B, H, maxp)).astype(np.float32)
+    s[1, 1] = np.round(s[1, 1] * 2) / 2                      # heavy ties
+    lens = [maxp * ps, (maxp - 700) * ps + 5]
+    sel, cnt, st = _run_select(s, lens, ps, 256, H)
+    assert st == 0
+    for b in range(B):
+        n = O.num_pages(lens[b], ps)
+        for h in range(H):
+            assert np.array_equal(sel[b, h, :cnt[b, h]], O.select_pages(s[b, h], n, 256)), (b, h)
+
+
 def test_select_large_candidate_count():
     rng = np.random.default_rng(5)
     B, H, maxp, ps = 1, 2, 45056, 16
