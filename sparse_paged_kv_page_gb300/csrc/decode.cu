@@ -74,6 +74,10 @@ struct DecodeArgs {
   float scale, scale_log2;
 };
 
+// Byte offset (from the 1024-aligned base) of a CTA's cluster partial, past the
+// warp-merge scratch (<= 4 warps x 16 rows x (D + 4) floats + 512 bytes).
+constexpr int kClusterOff = 36 * 1024;
+
 // Shared-memory tile of 16 rows x D columns (2-byte elements): 64-column
 // halves of 16 x 128 bytes, each 16-byte chunk c of row r stored at chunk
 // position c ^ (r & 7) -- the TMA 128-byte swizzle, so 8 rows read at one
@@ -86,12 +90,12 @@ struct Tile {
   static constexpr int kRowsPerOp = 32 / kChunks;    // rows one warp-wide cp.async covers
   static constexpr int kOps = 16 / kRowsPerOp;       // cp.async per lane per tile
   static constexpr int kStageBytes = 2 * kBytes;     // K + V
-  static constexpr int kSmem = kWarps * kStages * kStageBytes + 1024;   // + alignment slack
+  static constexpr int kStageArea = kWarps * kStages * kStageBytes;
+  // the stage area is reused for the merge scratch and the cluster partial
+  static constexpr int kMergeArea = kClusterOff + 4 * (16 * D + 16);
+  static constexpr int kSmem = (kStageArea > kMergeArea ? kStageArea : kMergeArea) + 1024;   // + alignment slack
 };
 
-// Byte offset (from the 1024-aligned base) of a CTA's cluster partial, past the
-// warp-merge scratch (<= 4 warps x 16 rows x (D + 4) floats + 512 bytes).
-constexpr int kClusterOff = 36 * 1024;
 
 template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -105,8 +109,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   using E = Elem<T>;
   using TL = Tile<D>;
   static_assert(kClusterOff >= 4 * (kWarps * 32 + kWarps * 16 * (D + 4)), "warp-merge scratch overlaps");
-  static_assert(kClusterOff + 4 * (16 * D + 16) <= kWarps * kStages * TL::kStageBytes,
-                "cluster partial must fit in the stage area");
+  static_assert(kClusterOff + 4 * (16 * D + 16) <= TL::kSmem - 1024, "cluster partial must fit");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ uint32_t s_mask[kWarps][kStages];
   __shared__ __align__(8) uint64_t s_bar[kWarps][kStages];
