@@ -2,5 +2,6 @@
 from .oracle import *  # noqa: F401,F403
 from .oracle import (decode_kdt, round_to_kdt, encode_kdt, ulp_kdt, num_pages, page_positions,
                      gather_rows, page_stats, cache_meta, head_meta, score_pages, select_pages,
-                     default_scale, attention, selected_positions, merge_partials,
-                     page_decode_unit, h2o_fold, h2o_store, h2o_evict, h2o_unit_step)
+                     select_pages_reserved, default_scale, attention, selected_positions,
+                     merge_partials, page_decode_unit, h2o_fold, h2o_fold_window, h2o_store,
+                     h2o_evict, h2o_unit_step)

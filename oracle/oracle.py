@@ -225,6 +225,33 @@ def select_pages(scores, n_pages: int, topk: int) -> np.ndarray:
     return np.sort(chosen).astype(np.int64)
 
 
+def select_pages_reserved(scores, n_pages: int, topk: int, n_bos: int, n_eos: int) -> np.ndarray:
+    """Indices of the pages attended with reserved leading and trailing pages.
+
+    [vortex] follow-up comment, "Two things I had to fix": the first
+    page_reserved_bos and the last page_reserved_eos pages are kept
+    unconditionally and top-k only ranks the window between them. Reading: the
+    reserved pages count against the budget topk, as [entmax] "Top-k" counts
+    the always-attended tail page (n_bos = 0, n_eos = 1 is select_pages). If
+    n_pages <= topk every page is kept; otherwise the reserved pages plus the
+    topk - n_bos - n_eos best of the window by (score descending, index
+    ascending), -0 == +0, NaN last.
+    """
+    n = int(n_pages)
+    if n <= 0:
+        return np.zeros(0, dtype=np.int64)
+    if n <= topk:
+        return np.arange(n, dtype=np.int64)
+    lo, hi, kk = int(n_bos), n - int(n_eos), topk - int(n_bos) - int(n_eos)
+    s = np.asarray(scores[lo:hi], dtype=np.float64)
+    nan = np.isnan(s)
+    key = np.where(nan, 0.0, -s) + 0.0
+    idx = np.arange(lo, hi)
+    order = np.lexsort((idx, key, nan))
+    chosen = np.concatenate([np.arange(lo), idx[order[:kk]], np.arange(hi, n)])
+    return np.sort(chosen).astype(np.int64)
+
+
 # ---------------------------------------------------------------------------
 # A4: attention over the selected tokens, and the LSE merge
 # ---------------------------------------------------------------------------
@@ -326,6 +353,28 @@ def h2o_fold(hh, logits, lse, decay: float) -> np.ndarray:
     return decay * np.asarray(hh, np.float64) + p.mean(0)
 
 
+def h2o_fold_window(hh, logits, n_bos: int, n_eos: int, decay: float) -> np.ndarray:
+    """The decayed fold with a reserved window, before storage rounding.
+
+    [vortex] follow-up comment, "Two things I had to fix" and its reference
+    step: hh_score is nonzero only between the reserved tokens; the softmax is
+    normalised over that window alone and the reserved entries receive
+    nothing. Here the reserved entries are the first n_bos and the last n_eos
+    of the retained list. hh: [n]; logits: [G, n].
+    p_bar_j = (1/G) sum_g exp(z_gj - lse'_g), lse'_g = log sum_{j in window} exp(z_gj).
+    """
+    z = np.asarray(logits, np.float64)
+    n = z.shape[1]
+    lo, hi = int(n_bos), n - int(n_eos)
+    p = np.zeros_like(z)
+    if hi > lo:
+        zw = z[:, lo:hi]
+        m = zw.max(axis=1, keepdims=True)
+        lse_w = m + np.log(np.exp(zw - m).sum(axis=1, keepdims=True))
+        p[:, lo:hi] = np.exp(zw - lse_w)
+    return decay * np.asarray(hh, np.float64) + p.mean(0)
+
+
 def h2o_store(hh_exact) -> np.ndarray:
     """[vortex] point 3: hh_score is held in bfloat16 -- one rounding to bf16."""
     return round_to_kdt(hh_exact, "bf16")
@@ -359,7 +408,7 @@ def h2o_evict(hh, positions, budget: int, n_sink: int, grace: int):
 
 def h2o_unit_step(hh_ret, positions, k_head_bits, v_head_bits, q_group_bits, *,
                   dtype: str, decay: float, budget: int, n_sink: int, grace: int,
-                  scale: float = 0.0):
+                  scale: float = 0.0, window_softmax: bool = False):
     """One token-level decode step for one (request, KV head), after the new
     token has been appended to the retained list with hh = 0.
 
@@ -368,6 +417,8 @@ def h2o_unit_step(hh_ret, positions, k_head_bits, v_head_bits, q_group_bits, *,
     eviction. hh_ret: bf16 values (float64) of the retained entries in list
     order; positions: their positions (ascending); k/v_head_bits: uint16 [L, D]
     logical keys / values of the request.
+    With window_softmax the fold is h2o_fold_window with the protected entries
+    (the first n_sink and the last grace) as the reserved ones.
     Returns dict(out, lse, logits, hh_exact, hh_bf16, kept, kept_hh, evicted).
     """
     D = k_head_bits.shape[1]
@@ -377,7 +428,8 @@ def h2o_unit_step(hh_ret, positions, k_head_bits, v_head_bits, q_group_bits, *,
     k = decode_kdt(k_head_bits[pos], dtype)
     v = decode_kdt(v_head_bits[pos], dtype)
     o, lse, z = attention(q, k, v, sc)
-    hh_exact = h2o_fold(hh_ret, z, lse, decay)
+    hh_exact = (h2o_fold_window(hh_ret, z, n_sink, grace, decay) if window_softmax
+                else h2o_fold(hh_ret, z, lse, decay))
     hh_b = h2o_store(hh_exact)
     kept, kept_hh, ev = h2o_evict(hh_b, pos, budget, n_sink, grace)
     return {"out": o, "lse": lse, "logits": z, "hh_exact": hh_exact, "hh_bf16": hh_b,

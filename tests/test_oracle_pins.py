@@ -240,6 +240,54 @@ def test_select_edges():
     assert O.select_pages(np.array([1.0, 2.0, 3.0, -99.0]), 4, 2).tolist() == [2, 3]
 
 
+def _brute_select_reserved(s, n, topk, bos, eos):
+    """Reserved pages plus the unique window subset every member of which
+    ranks before every non-member (score desc, index asc, NaN last)."""
+    if n <= topk:
+        return list(range(n))
+    window = list(range(bos, n - eos))
+
+    def better(x, y):
+        sx, sy = s[x], s[y]
+        nx, ny = math.isnan(sx), math.isnan(sy)
+        if nx != ny:
+            return ny
+        if not nx and sx != sy:
+            return sx > sy
+        return x < y
+
+    sols = []
+    for X in itertools.combinations(window, topk - bos - eos):
+        Xs = set(X)
+        if all(better(x, y) for x in Xs for y in window if y not in Xs):
+            sols.append(sorted(list(range(bos)) + list(X) + list(range(n - eos, n))))
+    assert len(sols) == 1
+    return sols[0]
+
+
+def test_select_reserved_brute_force():
+    rng = np.random.default_rng(11)
+    pool = np.array([0.0, -0.0, 1.0, 1.0, -1.0, np.nan, -np.inf, np.inf, 0.5, 0.5, 2.0])
+    for _ in range(400):
+        n = int(rng.integers(1, 11))
+        bos = int(rng.integers(0, 3))
+        eos = int(rng.integers(1, 3))
+        topk = int(rng.integers(bos + eos, bos + eos + 5))
+        s = rng.choice(pool, size=n)
+        got = O.select_pages_reserved(s, n, topk, bos, eos).tolist()
+        assert got == _brute_select_reserved(list(s), n, topk, bos, eos)
+
+
+def test_select_reserved_reduces_to_tail_forcing():
+    rng = np.random.default_rng(12)
+    for _ in range(100):
+        n = int(rng.integers(1, 300))
+        topk = int(rng.integers(1, 40))
+        s = rng.standard_normal(n)
+        s[rng.random(n) < 0.1] = 0.5
+        assert np.array_equal(O.select_pages_reserved(s, n, topk, 0, 1), O.select_pages(s, n, topk))
+
+
 # ---------------------------------------------------------------------------
 # A4 attention and the LSE merge
 # ---------------------------------------------------------------------------
@@ -382,6 +430,30 @@ def test_probabilities_sum_to_one_and_decay_one_is_plain_sum():
     assert abs(p.sum() - 1.0) < 1e-12
     hh = rng.random(50)
     assert np.array_equal(O.h2o_fold(hh, z, lse, 1.0), hh + p)
+
+
+def test_window_fold_normalises_over_the_window_only():
+    rng = np.random.default_rng(19)
+    z = rng.standard_normal((4, 40)) * 2
+    hh = rng.random(40)
+    out = O.h2o_fold_window(hh, z, 3, 5, 0.75)
+    p = out - 0.75 * hh
+    assert np.all(p[:3] == 0) and np.all(p[-5:] == 0)         # reserved entries receive nothing
+    assert abs(p[3:-5].sum() - 1.0) < 1e-12                   # the window's mass is one step's
+    # equal logits in the window: each window entry gets 1 / |window| whatever the rest holds
+    z2 = z.copy()
+    z2[:, 3:-5] = 1.25
+    p2 = O.h2o_fold_window(np.zeros(40), z2, 3, 5, 0.5)
+    assert np.allclose(p2[3:-5], 1.0 / 32, rtol=0, atol=1e-15)
+
+
+def test_window_fold_without_reserved_entries_is_the_plain_fold():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(20)
+    z = rng.standard_normal((3, 25))
+    hh = rng.random(25)
+    assert np.allclose(O.h2o_fold_window(hh, z, 0, 0, 0.9), O.h2o_fold(hh, z, logsumexp(z, axis=1), 0.9),
+                       rtol=1e-14, atol=1e-15)
 
 
 def test_decayed_mass_closed_form():
