@@ -13,6 +13,9 @@
  *                     sink/grace-protected eviction
  *   sa_decode_step    the page-level chain (append, score, select, decode) in
  *                     one call, kernels overlapped by programmatic launch
+ *   sa_select_topk_reserved, sa_h2o_update_window
+ *                     the selection and the H2O fold with reserved leading and
+ *                     trailing pages / tokens
  *
  * Sources (cited by page title and section):
  *   [vortex]  "flow: add H2O sparse attention (page-level and token-level,
@@ -178,6 +181,27 @@ sa_status sa_select_topk(const float* scores, int32_t max_pages, const sa_batch*
                          void* stream);
 
 /*
+ * sa_select_topk_reserved -- sa_select_topk with reserved leading and
+ * trailing pages.
+ *
+ * [vortex] follow-up comment ("Two things I had to fix"): the first
+ * page_reserved_bos and the last page_reserved_eos pages are kept
+ * unconditionally and top-k ranks only the window between them. The reserved
+ * pages count against the budget (as [entmax] "Top-k" counts the tail page):
+ * with n = ceil(seq_lens[b] / page_size), n <= topk selects every page;
+ * otherwise pages 0 .. n_bos-1, pages n-n_eos .. n-1 and the
+ * topk - n_bos - n_eos best of pages n_bos .. n-n_eos-1 by (score descending,
+ * page index ascending), -0 equal to +0, NaN after every number; indices
+ * ascending, sel_cnt = min(topk, n). n_bos = 0, n_eos = 1 is sa_select_topk.
+ * Constraints: n_bos >= 0, n_eos >= 1 (the tail page, which the attention
+ * needs), n_bos + n_eos <= topk (else SA_ERR_INVALID_ARG).
+ */
+sa_status sa_select_topk_reserved(const float* scores, int32_t max_pages, const sa_batch* batch,
+                                  int32_t page_size, int32_t num_kv_heads, int32_t topk,
+                                  int32_t n_bos, int32_t n_eos, int32_t* sel_idx, int32_t* sel_cnt,
+                                  int32_t* dev_status, void* stream);
+
+/*
  * sa_decode_workspace_size -- bytes of workspace sa_sparse_decode needs for
  * these sizes (host function, no GPU access). The workspace holds the split
  * partial states and one ticket counter per (request, KV head); it must be
@@ -293,7 +317,9 @@ sa_status sa_h2o_update(const sa_batch* batch, int32_t num_kv_heads, int32_t num
  * key refreshes its page's statistics, every page is scored from the
  * statistics, the top-k pages (tail forced) are chosen and attention runs
  * exactly over them. Arguments mean what they mean in the four calls (the
- * selection row length is topk; no H2O slots, no retained lists, no logits).
+ * selection row length is topk; no H2O slots, no retained lists, no logits);
+ * the selection is sa_select_topk_reserved's with n_bos, n_eos (0, 1 gives
+ * sa_select_topk's).
  *   k_new      nullable: NULL (or max_new_per_req 0) skips the append, and
  *              v_new / new_cu are then ignored
  *   workspace  at least sa_decode_workspace_size(batch, num_kv_heads,
@@ -313,9 +339,29 @@ sa_status sa_h2o_update(const sa_batch* batch, int32_t num_kv_heads, int32_t num
 sa_status sa_decode_step(const sa_cache* cache, const sa_batch* batch, const void* k_new,
                          const void* v_new, const int32_t* new_cu, int32_t max_new_per_req,
                          const void* q, int32_t num_q_heads, float w_avg, float w_peak,
-                         float* scores, int32_t max_pages, int32_t topk, int32_t* sel_idx,
-                         int32_t* sel_cnt, float scale, void* out, float* lse, void* workspace,
-                         size_t workspace_bytes, int32_t* dev_status, void* stream);
+                         float* scores, int32_t max_pages, int32_t topk, int32_t n_bos,
+                         int32_t n_eos, int32_t* sel_idx, int32_t* sel_cnt, float scale,
+                         void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * sa_h2o_update_window -- sa_h2o_update with the reserved windows of [vortex]
+ * (follow-up comment, "Two things I had to fix"): hh_score stays zero on the
+ * reserved tokens and the softmax is normalised over the window between them.
+ * Here the reserved entries are the protected ones, the first n_sink and the
+ * last grace entries of the retained list: they receive p_bar = 0, and for the
+ * entries j in between
+ *   p_bar_j = (1/G) sum_g exp(logits[g, j] - lse'_g),
+ *   lse'_g  = log sum over those entries of exp(logits[g, .])   (float32);
+ * lse is not read. Eviction and every other argument as sa_h2o_update;
+ * G <= 16.
+ */
+sa_status sa_h2o_update_window(const sa_batch* batch, int32_t num_kv_heads, int32_t num_q_heads,
+                               const float* logits, int32_t logits_stride, const float* lse,
+                               void* hh, int32_t num_slots, int32_t* ret_pos, int32_t* ret_cnt,
+                               int32_t ret_cap, int32_t budget, int32_t n_sink, int32_t grace,
+                               float decay, int32_t* evicted, int32_t* evicted_cnt,
+                               int32_t* dev_status, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* sa_status_string(sa_status status);

@@ -52,8 +52,13 @@ SIGNATURES = {
                               c_ptr, c_i32, c_i32, c_i32, c_i32, c_f32, c_ptr, c_ptr, c_ptr,
                               c_ptr]),
     "sa_decode_step": (c_i32, [P_CACHE, P_BATCH, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_i32, c_f32,
-                               c_f32, c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_f32, c_ptr, c_ptr,
-                               c_ptr, c_size, c_ptr, c_ptr]),
+                               c_f32, c_ptr, c_i32, c_i32, c_i32, c_i32, c_ptr, c_ptr, c_f32,
+                               c_ptr, c_ptr, c_ptr, c_size, c_ptr, c_ptr]),
+    "sa_select_topk_reserved": (c_i32, [c_ptr, c_i32, P_BATCH, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                        c_ptr, c_ptr, c_ptr, c_ptr]),
+    "sa_h2o_update_window": (c_i32, [P_BATCH, c_i32, c_i32, c_ptr, c_i32, c_ptr, c_ptr, c_i32,
+                                     c_ptr, c_ptr, c_i32, c_i32, c_i32, c_i32, c_f32, c_ptr,
+                                     c_ptr, c_ptr, c_ptr]),
     "sa_status_string": (ctypes.c_char_p, [c_i32]),
     "sa_version": (ctypes.c_char_p, []),
 }

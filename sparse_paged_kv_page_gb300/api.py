@@ -19,6 +19,7 @@ __all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKV
            "sa_append_kv", "sa_score_pages", "sa_select_topk", "sa_decode_workspace_size",
            "sa_decode_workspace_init", "sa_sparse_decode", "sa_sparse_decode_noalloc",
            "sa_sparse_decode_noalloc_capacity", "sa_h2o_update", "sa_decode_step",
+           "sa_select_topk_reserved", "sa_h2o_update_window",
            "sa_status_string",
            "sa_version", "alloc_decode_workspace"]
 
@@ -133,6 +134,17 @@ def sa_select_topk(scores, max_pages: int, batch: SaBatch, page_size: int, num_k
         _s(stream)))
 
 
+def sa_select_topk_reserved(scores, max_pages: int, batch: SaBatch, page_size: int,
+                            num_kv_heads: int, topk: int, n_bos: int, n_eos: int, sel_idx,
+                            sel_cnt, dev_status=None, stream=None):
+    lib = _lib.load()
+    _check("sa_select_topk_reserved", lib.sa_select_topk_reserved(
+        _p(scores, torch.float32, "scores"), int(max_pages), ctypes.byref(batch), int(page_size),
+        int(num_kv_heads), int(topk), int(n_bos), int(n_eos), _p(sel_idx, torch.int32, "sel_idx"),
+        _p(sel_cnt, torch.int32, "sel_cnt"), _p(dev_status, torch.int32, "dev_status"),
+        _s(stream)))
+
+
 def sa_decode_workspace_size(batch: int, num_kv_heads: int, num_q_heads: int, head_dim: int,
                              page_size: int, sel_stride: int) -> int:
     return int(_lib.load().sa_decode_workspace_size(batch, num_kv_heads, num_q_heads, head_dim,
@@ -183,12 +195,11 @@ def sa_sparse_decode_noalloc_capacity() -> int:
     return int(_lib.load().sa_sparse_decode_noalloc_capacity())
 
 
-def sa_h2o_update(batch: SaBatch, num_kv_heads: int, num_q_heads: int, logits,
-                  logits_stride: int, lse, hh, num_slots: int, ret_pos, ret_cnt, ret_cap: int,
-                  budget: int, n_sink: int, grace: int, decay: float, evicted=None,
-                  evicted_cnt=None, dev_status=None, stream=None):
+def _h2o(name, batch: SaBatch, num_kv_heads: int, num_q_heads: int, logits, logits_stride: int,
+         lse, hh, num_slots: int, ret_pos, ret_cnt, ret_cap: int, budget: int, n_sink: int,
+         grace: int, decay: float, evicted=None, evicted_cnt=None, dev_status=None, stream=None):
     lib = _lib.load()
-    _check("sa_h2o_update", lib.sa_h2o_update(
+    _check(name, getattr(lib, name)(
         ctypes.byref(batch), int(num_kv_heads), int(num_q_heads),
         _p(logits, torch.float32, "logits"), int(logits_stride), _p(lse, torch.float32, "lse"),
         _p(hh, torch.bfloat16, "hh"), int(num_slots), _p(ret_pos, torch.int32, "ret_pos"),
@@ -198,18 +209,38 @@ def sa_h2o_update(batch: SaBatch, num_kv_heads: int, num_q_heads: int, logits,
         _s(stream)))
 
 
+def sa_h2o_update(batch: SaBatch, num_kv_heads: int, num_q_heads: int, logits,
+                  logits_stride: int, lse, hh, num_slots: int, ret_pos, ret_cnt, ret_cap: int,
+                  budget: int, n_sink: int, grace: int, decay: float, evicted=None,
+                  evicted_cnt=None, dev_status=None, stream=None):
+    _h2o("sa_h2o_update", batch, num_kv_heads, num_q_heads, logits, logits_stride, lse, hh,
+         num_slots, ret_pos, ret_cnt, ret_cap, budget, n_sink, grace, decay, evicted, evicted_cnt,
+         dev_status, stream)
+
+
+def sa_h2o_update_window(batch: SaBatch, num_kv_heads: int, num_q_heads: int, logits,
+                         logits_stride: int, lse, hh, num_slots: int, ret_pos, ret_cnt,
+                         ret_cap: int, budget: int, n_sink: int, grace: int, decay: float,
+                         evicted=None, evicted_cnt=None, dev_status=None, stream=None):
+    """sa_h2o_update with the softmax normalised over the unprotected entries."""
+    _h2o("sa_h2o_update_window", batch, num_kv_heads, num_q_heads, logits, logits_stride, lse,
+         hh, num_slots, ret_pos, ret_cnt, ret_cap, budget, n_sink, grace, decay, evicted,
+         evicted_cnt, dev_status, stream)
+
+
 def sa_decode_step(cache: SaCache, batch: SaBatch, k_new, v_new, new_cu, max_new_per_req: int,
                    q, num_q_heads: int, w_avg: float, w_peak: float, scores, max_pages: int,
                    topk: int, sel_idx, sel_cnt, scale: float, out, lse=None, workspace=None,
-                   dev_status=None, stream=None):
-    """Append (k_new may be None), score, select and decode in one chained call."""
+                   dev_status=None, stream=None, n_bos: int = 0, n_eos: int = 1):
+    """Append (k_new may be None), score, select (reserved pages n_bos / n_eos)
+    and decode in one chained call."""
     lib = _lib.load()
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("sa_decode_step", lib.sa_decode_step(
         ctypes.byref(cache), ctypes.byref(batch), _p(k_new, name="k_new"), _p(v_new, name="v_new"),
         _p(new_cu, torch.int32, "new_cu"), int(max_new_per_req), _p(q, name="q"),
         int(num_q_heads), float(w_avg), float(w_peak), _p(scores, torch.float32, "scores"),
-        int(max_pages), int(topk), _p(sel_idx, torch.int32, "sel_idx"),
+        int(max_pages), int(topk), int(n_bos), int(n_eos), _p(sel_idx, torch.int32, "sel_idx"),
         _p(sel_cnt, torch.int32, "sel_cnt"), float(scale), _p(out, name="out"),
         _p(lse, torch.float32, "lse"), _p(workspace, name="workspace"), wbytes,
         _p(dev_status, torch.int32, "dev_status"), _s(stream)))

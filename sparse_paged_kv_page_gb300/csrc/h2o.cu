@@ -12,6 +12,10 @@
 //
 // One CTA per (KV head, request). Fold: p_bar_j = mean_g exp(z_gj - lse_g) in
 // float32; hh = decay * hh + p_bar as one float64 fma rounded once to bf16.
+// sa_h2o_update_window follows the reserved windows of the vortex follow-up
+// comment ("Two things I had to fix"): the protected entries (the first n_sink
+// and the last grace) receive nothing and the softmax is normalised over the
+// entries between them, lse_g replaced by their own log-sum-exp.
 // Evict: scores are fixed within the step, so evicting the minimum one at a
 // time until |R| = budget removes exactly the m = |R| - budget smallest
 // (score, position) pairs of the eligible window [n_sink, |R| - grace) (the
@@ -40,6 +44,7 @@ struct H2oArgs {
   int32_t* status;
   int H, H_q, G, bt_stride, logits_stride, num_slots, cap, budget, n_sink, grace;
   float decay;
+  int window;      // softmax over the unprotected entries only, the protected ones get 0
 };
 
 __global__ void __launch_bounds__(kH2oThreads) h2o_kernel(H2oArgs a) {
@@ -60,15 +65,39 @@ __global__ void __launch_bounds__(kH2oThreads) h2o_kernel(H2oArgs a) {
   const float inv_g = 1.0f / float(a.G);
   const double decay = double(a.decay);
 
+  // Windowed mode: each query head's log-sum-exp over the unprotected
+  // entries [n_sink, n - grace) only; warp g (< G <= 16) reduces head g.
+  __shared__ float s_lse_w[16];
+  const int wlo = a.n_sink, whi = n - a.grace;
+  if (a.window) {
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < a.G) {
+      const float* zr = a.logits + (int64_t(b) * a.H_q + h * a.G + warp) * a.logits_stride;
+      float m = -INFINITY;
+      for (int j = wlo + lane; j < whi; j += 32) m = fmaxf(m, zr[j]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+      float sum = 0.f;
+      if (m > -INFINITY)
+        for (int j = wlo + lane; j < whi; j += 32) sum += expf(zr[j] - m);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+      if (lane == 0) s_lse_w[warp] = sum > 0.f ? m + logf(sum) : INFINITY;   // +inf: p = 0
+    }
+    __syncthreads();
+  }
+
   // fold
   for (int j = tid; j < n; j += kH2oThreads) {
     const int pos = rp[j];
     s_pos[j] = pos;
     float pb = 0.f;
-    for (int g = 0; g < a.G; ++g) {
-      const int hq = h * a.G + g;
-      const float z = a.logits[(int64_t(b) * a.H_q + hq) * a.logits_stride + j];
-      pb += expf(z - a.lse[int64_t(b) * a.H_q + hq]);
+    if (!a.window || (j >= wlo && j < whi)) {
+      for (int g = 0; g < a.G; ++g) {
+        const int hq = h * a.G + g;
+        const float z = a.logits[(int64_t(b) * a.H_q + hq) * a.logits_stride + j];
+        pb += expf(z - (a.window ? s_lse_w[g] : a.lse[int64_t(b) * a.H_q + hq]));
+      }
     }
     pb *= inv_g;
     uint16_t nw = 0xffffu;
@@ -195,12 +224,12 @@ int g_h2o_smem[64];
 }  // namespace
 }  // namespace sa
 
-extern "C" sa_status sa_h2o_update(const sa_batch* batch, int32_t num_kv_heads, int32_t num_q_heads,
+static sa_status h2o_update(const sa_batch* batch, int32_t num_kv_heads, int32_t num_q_heads,
                                    const float* logits, int32_t logits_stride, const float* lse,
                                    void* hh, int32_t num_slots, int32_t* ret_pos, int32_t* ret_cnt,
                                    int32_t ret_cap, int32_t budget, int32_t n_sink, int32_t grace,
                                    float decay, int32_t* evicted, int32_t* evicted_cnt,
-                                   int32_t* dev_status, void* stream) {
+                                   int32_t* dev_status, void* stream, int window) {
   using namespace sa;
   sa_status st = check_batch(batch);
   if (st != SA_OK) return st;
@@ -210,15 +239,40 @@ extern "C" sa_status sa_h2o_update(const sa_batch* batch, int32_t num_kv_heads, 
   if (n_sink < 0 || grace < 0 || budget <= n_sink + grace) return SA_ERR_INVALID_ARG;
   if (!(decay > 0.f && decay <= 1.f)) return SA_ERR_INVALID_ARG;
   if (ret_cap > kH2oMaxCap) return SA_ERR_UNSUPPORTED;
+  if (window && num_q_heads / num_kv_heads > 16) return SA_ERR_UNSUPPORTED;
   H2oArgs a;
   a.bt = batch->block_table; a.logits = logits; a.lse = lse; a.hh = static_cast<uint16_t*>(hh);
   a.ret_pos = ret_pos; a.ret_cnt = ret_cnt; a.evicted = evicted; a.evicted_cnt = evicted_cnt;
   a.status = dev_status; a.H = num_kv_heads; a.H_q = num_q_heads; a.G = num_q_heads / num_kv_heads;
   a.bt_stride = batch->bt_stride; a.logits_stride = logits_stride; a.num_slots = num_slots;
   a.cap = ret_cap; a.budget = budget; a.n_sink = n_sink; a.grace = grace; a.decay = decay;
+  a.window = window;
   const int smem = ret_cap * 6 + 16;
   if (!ensure_smem(h2o_kernel, smem, g_h2o_smem)) return SA_ERR_CUDA;
   dim3 grid(unsigned(num_kv_heads), unsigned(batch->batch));
   h2o_kernel<<<grid, kH2oThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
   return launch_status();
+}
+
+extern "C" sa_status sa_h2o_update(const sa_batch* batch, int32_t num_kv_heads, int32_t num_q_heads,
+                                   const float* logits, int32_t logits_stride, const float* lse,
+                                   void* hh, int32_t num_slots, int32_t* ret_pos, int32_t* ret_cnt,
+                                   int32_t ret_cap, int32_t budget, int32_t n_sink, int32_t grace,
+                                   float decay, int32_t* evicted, int32_t* evicted_cnt,
+                                   int32_t* dev_status, void* stream) {
+  return h2o_update(batch, num_kv_heads, num_q_heads, logits, logits_stride, lse, hh, num_slots,
+                    ret_pos, ret_cnt, ret_cap, budget, n_sink, grace, decay, evicted, evicted_cnt,
+                    dev_status, stream, 0);
+}
+
+extern "C" sa_status sa_h2o_update_window(const sa_batch* batch, int32_t num_kv_heads,
+                                          int32_t num_q_heads, const float* logits,
+                                          int32_t logits_stride, const float* lse, void* hh,
+                                          int32_t num_slots, int32_t* ret_pos, int32_t* ret_cnt,
+                                          int32_t ret_cap, int32_t budget, int32_t n_sink,
+                                          int32_t grace, float decay, int32_t* evicted,
+                                          int32_t* evicted_cnt, int32_t* dev_status, void* stream) {
+  return h2o_update(batch, num_kv_heads, num_q_heads, logits, logits_stride, lse, hh, num_slots,
+                    ret_pos, ret_cnt, ret_cap, budget, n_sink, grace, decay, evicted, evicted_cnt,
+                    dev_status, stream, 1);
 }

@@ -4,6 +4,11 @@
 // counting pages and including the always-attended tail page. With n pages:
 // n <= topk keeps all; otherwise the tail n-1 plus the topk-1 best of pages
 // 0..n-2 by (score descending, index ascending); -0 == +0; NaN ranks last.
+// "flow: add H2O sparse attention" (vortex_torch PR 6), the follow-up comment:
+// page_reserved_bos leading and page_reserved_eos trailing pages are kept
+// unconditionally and top-k ranks only the window between them
+// (sa_select_topk_reserved; the reserved pages count against the budget, so
+// n_bos = 0, n_eos = 1 is the rule above).
 //
 // One 1024-thread CTA per (KV head, request). Scores become order-preserving
 // 32-bit keys in shared memory; a most-significant-digit radix select
@@ -35,6 +40,7 @@ struct SelArgs {
   int32_t* sel_cnt;
   int32_t* status;
   int H, ps, max_pages, topk;
+  int n_bos, n_eos;      // reserved leading / trailing pages (n_eos >= 1: the tail)
 };
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
@@ -47,14 +53,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   const int unit = b * a.H + h;
   pdl_wait();                                  // scores and lengths of this step are final
   pdl_trigger();                               // the decode may start its prologue
-  // The first 8 * kSelThreads scores are loaded together with the length (the
-  // row holds max_pages entries; entries past the length are ignored).
-  const float* sc = a.scores + int64_t(unit) * a.max_pages;
+  // Candidate i is page n_bos + i. The first 8 * kSelThreads candidates'
+  // scores are loaded together with the length (the row holds max_pages
+  // entries; entries past the length are ignored).
+  const int bos = a.n_bos, eos = a.n_eos;
+  const float* sc = a.scores + int64_t(unit) * a.max_pages + bos;
   float v0[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
     const int i = u * kSelThreads + tid;
-    v0[u] = i < a.max_pages ? sc[i] : 0.f;
+    v0[u] = bos + i < a.max_pages ? sc[i] : 0.f;
   }
   const int L = a.seq_lens[b];
   int n = L > 0 ? (L + a.ps - 1) / a.ps : 0;
@@ -68,12 +76,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     if (tid == 0) a.sel_cnt[unit] = n;
     return;
   }
-  const int kprime = a.topk - 1;                 // best candidates besides the tail
-  const int nc = n - 1;                          // candidates 0 .. n-2
-  if (kprime == 0) {
-    if (tid == 0) { out[0] = n - 1; a.sel_cnt[unit] = 1; }
-    return;
-  }
+  // the reserved pages: 0 .. bos-1 first, n-eos .. n-1 last (the tail among them)
+  const int kprime = a.topk - bos - eos;         // best candidates besides the reserved pages
+  const int nc = n - bos - eos;                  // candidates: pages bos .. n-eos-1
+  for (int j = tid; j < bos; j += kSelThreads) out[j] = j;
+  for (int j = tid; j < eos; j += kSelThreads) out[bos + kprime + j] = n - eos + j;
+  if (tid == 0) a.sel_cnt[unit] = a.topk;
+  if (kprime == 0) return;
   for (int i = tid; i < 2 * 4096; i += kSelThreads) (&hist[0][0])[i] = 0;
   __syncthreads();
   // keys to shared memory; the first digit's histogram straight from registers
@@ -205,13 +214,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     const bool take = is_gt || (is_eq && eq_run + __popc(meq & lt) < remaining);
     const uint32_t mt = __ballot_sync(kFull, take);
     const int pos = take_run + __popc(mt & lt);
-    if (take && pos < kprime) out[pos] = i;
+    if (take && pos < kprime) out[bos + pos] = bos + i;
     eq_run += __popc(meq);
     take_run += __popc(mt);
-  }
-  if (tid == 0) {
-    out[kprime] = n - 1;                         // the tail is the largest index
-    a.sel_cnt[unit] = a.topk;
   }
 }
 
@@ -221,8 +226,9 @@ int g_sel_smem[64];
 }  // namespace sa
 
 sa_status sa::select_impl(const float* scores, int32_t max_pages, const sa_batch* batch,
-                         int32_t page_size, int32_t num_kv_heads, int32_t topk, int32_t* sel_idx,
-                         int32_t* sel_cnt, int32_t* dev_status, void* stream, bool pdl) {
+                         int32_t page_size, int32_t num_kv_heads, int32_t topk, int32_t n_bos,
+                         int32_t n_eos, int32_t* sel_idx, int32_t* sel_cnt, int32_t* dev_status,
+                         void* stream, bool pdl) {
   using namespace sa;
   sa_status st = check_batch(batch);
   if (st != SA_OK) return st;
@@ -230,10 +236,11 @@ sa_status sa::select_impl(const float* scores, int32_t max_pages, const sa_batch
     return SA_ERR_INVALID_ARG;
   if (!is_pow2(page_size) || page_size > 128) return SA_ERR_UNSUPPORTED;
   if (max_pages > kSelMaxPages) return SA_ERR_UNSUPPORTED;
+  if (n_bos < 0 || n_eos < 1 || n_bos + n_eos > topk) return SA_ERR_INVALID_ARG;
   SelArgs a;
   a.scores = scores; a.seq_lens = batch->seq_lens; a.sel_idx = sel_idx; a.sel_cnt = sel_cnt;
   a.status = dev_status; a.H = num_kv_heads; a.ps = page_size; a.max_pages = max_pages;
-  a.topk = topk;
+  a.topk = topk; a.n_bos = n_bos; a.n_eos = n_eos;
   const int smem = max_pages * int(sizeof(uint32_t));
   // static shared memory (the 16 KB histogram) plus the keys may pass the 48 KB default
   if (!ensure_smem(select_kernel, smem, g_sel_smem)) return SA_ERR_CUDA;
@@ -248,6 +255,15 @@ extern "C" sa_status sa_select_topk(const float* scores, int32_t max_pages, cons
                                     int32_t page_size, int32_t num_kv_heads, int32_t topk,
                                     int32_t* sel_idx, int32_t* sel_cnt, int32_t* dev_status,
                                     void* stream) {
-  return sa::select_impl(scores, max_pages, batch, page_size, num_kv_heads, topk, sel_idx, sel_cnt,
-                         dev_status, stream, false);
+  return sa::select_impl(scores, max_pages, batch, page_size, num_kv_heads, topk, 0, 1, sel_idx,
+                         sel_cnt, dev_status, stream, false);
+}
+
+extern "C" sa_status sa_select_topk_reserved(const float* scores, int32_t max_pages,
+                                             const sa_batch* batch, int32_t page_size,
+                                             int32_t num_kv_heads, int32_t topk, int32_t n_bos,
+                                             int32_t n_eos, int32_t* sel_idx, int32_t* sel_cnt,
+                                             int32_t* dev_status, void* stream) {
+  return sa::select_impl(scores, max_pages, batch, page_size, num_kv_heads, topk, n_bos, n_eos,
+                         sel_idx, sel_cnt, dev_status, stream, false);
 }

@@ -19,7 +19,8 @@ extern "C" sa_status sa_decode_step(const sa_cache* cache, const sa_batch* batch
                                     const void* v_new, const int32_t* new_cu,
                                     int32_t max_new_per_req, const void* q, int32_t num_q_heads,
                                     float w_avg, float w_peak, float* scores, int32_t max_pages,
-                                    int32_t topk, int32_t* sel_idx, int32_t* sel_cnt, float scale,
+                                    int32_t topk, int32_t n_bos, int32_t n_eos, int32_t* sel_idx,
+                                    int32_t* sel_cnt, float scale,
                                     void* out, float* lse, void* workspace, size_t workspace_bytes,
                                     int32_t* dev_status, void* stream) {
   using namespace sa;
@@ -30,7 +31,7 @@ extern "C" sa_status sa_decode_step(const sa_cache* cache, const sa_batch* batch
   const bool append = k_new != nullptr && max_new_per_req > 0;
   if (append && (!v_new || !new_cu)) return SA_ERR_INVALID_ARG;
   if (!q || !scores || !sel_idx || !sel_cnt || !out || max_pages <= 0 || topk <= 0 ||
-      max_new_per_req < 0)
+      max_new_per_req < 0 || n_bos < 0 || n_eos < 1 || n_bos + n_eos > topk)
     return SA_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
   if (num_q_heads / cache->num_kv_heads > 16) return SA_ERR_UNSUPPORTED;
@@ -53,8 +54,8 @@ extern "C" sa_status sa_decode_step(const sa_cache* cache, const sa_batch* batch
                      stream, true);
     if (st != SA_OK) return st;
   }
-  st = select_impl(scores, max_pages, batch, cache->page_size, cache->num_kv_heads, topk, sel_idx,
-                   sel_cnt, dev_status, stream, true);
+  st = select_impl(scores, max_pages, batch, cache->page_size, cache->num_kv_heads, topk, n_bos,
+                   n_eos, sel_idx, sel_cnt, dev_status, stream, true);
   if (st != SA_OK) return st;
   return decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, topk, scale, out, lse, nullptr, 0,
                      workspace, workspace_bytes, dev_status, stream, true, true);

@@ -19,8 +19,8 @@ from typing import Optional, Sequence
 import torch
 
 from .api import (PagedKVCache, alloc_decode_workspace, make_batch, sa_append_kv,
-                  sa_decode_step, sa_h2o_update, sa_score_pages, sa_select_topk,
-                  sa_sparse_decode)
+                  sa_decode_step, sa_h2o_update, sa_h2o_update_window, sa_score_pages,
+                  sa_select_topk_reserved, sa_sparse_decode)
 
 
 class SparseDecoder:
@@ -28,12 +28,14 @@ class SparseDecoder:
                  page_size: int, num_blocks: int, bt_stride: int, dtype=torch.bfloat16,
                  topk: int = 0, w_avg: float = 1.0, w_peak: float = 0.25, scale: float = 0.0,
                  budget: int = 0, n_sink: int = 0, grace: int = 0, decay: float = 1.0,
-                 ret_cap: int = 0, device="cuda"):
+                 ret_cap: int = 0, n_bos: int = 0, n_eos: int = 1, window_softmax: bool = False,
+                 device="cuda"):
         self.B, self.H_q, self.H_kv, self.D = batch, num_q_heads, num_kv_heads, head_dim
         self.ps, self.dtype, self.device = page_size, dtype, torch.device(device)
         self.token_level = page_size == 1 and ret_cap > 0
         self.topk, self.w_avg, self.w_peak, self.scale = topk, w_avg, w_peak, scale
         self.budget, self.n_sink, self.grace, self.decay = budget, n_sink, grace, decay
+        self.n_bos, self.n_eos, self.window_softmax = n_bos, n_eos, window_softmax
         self.cache = PagedKVCache(num_blocks, num_kv_heads, page_size, head_dim, dtype, device,
                                   with_meta=not self.token_level, with_hh=self.token_level)
         i32 = dict(dtype=torch.int32, device=device)
@@ -102,7 +104,8 @@ class SparseDecoder:
                              self.ret_cap, self.scale, self.out, lse=self.lse, logits=self.logits,
                              logits_stride=self.ret_cap, workspace=self.workspace,
                              dev_status=self.dev_status)
-            sa_h2o_update(self.batch, self.H_kv, self.H_q, self.logits, self.ret_cap, self.lse,
+            h2o = sa_h2o_update_window if self.window_softmax else sa_h2o_update
+            h2o(self.batch, self.H_kv, self.H_q, self.logits, self.ret_cap, self.lse,
                           self.cache.hh, self.cache.hh.shape[0], self.ret_pos, self.ret_cnt,
                           self.ret_cap, self.budget, self.n_sink, self.grace, self.decay,
                           evicted=self.evicted, evicted_cnt=self.evicted_cnt,
@@ -110,8 +113,9 @@ class SparseDecoder:
         else:
             sa_score_pages(self.cache.struct, self.batch, q, self.H_q, self.w_avg, self.w_peak,
                            self.scores, self.max_pages, dev_status=self.dev_status)
-            sa_select_topk(self.scores, self.max_pages, self.batch, self.ps, self.H_kv, self.topk,
-                           self.sel_idx, self.sel_cnt, dev_status=self.dev_status)
+            sa_select_topk_reserved(self.scores, self.max_pages, self.batch, self.ps, self.H_kv,
+                                    self.topk, self.n_bos, self.n_eos, self.sel_idx, self.sel_cnt,
+                                    dev_status=self.dev_status)
             sa_sparse_decode(self.cache.struct, self.batch, q, self.H_q, self.sel_idx,
                              self.sel_cnt, self.topk, self.scale, self.out, lse=self.lse,
                              workspace=self.workspace, dev_status=self.dev_status)
@@ -128,7 +132,7 @@ class SparseDecoder:
                        1 if k_new is not None else 0, q, self.H_q, self.w_avg, self.w_peak,
                        self.scores, self.max_pages, self.topk, self.sel_idx, self.sel_cnt,
                        self.scale, self.out, lse=self.lse, workspace=self.workspace,
-                       dev_status=self.dev_status)
+                       dev_status=self.dev_status, n_bos=self.n_bos, n_eos=self.n_eos)
         return self.out
 
     # ------------------------------------------------------------------

@@ -45,7 +45,7 @@ def test_host_only_calls(lib):
     assert S.sa_decode_workspace_size(4, 8, 64, 128, 16, 256) > 4 * 8 * 4
     # argument checks run on the host before any launch
     assert lib.sa_decode_step(None, None, None, None, None, 0, None, 8, 1.0, 0.25, None, 16, 4,
-                              None, None, 0.0, None, None, None, 0, None, None) == 1
+                              0, 1, None, None, 0.0, None, None, None, 0, None, None) == 1
 
 
 def test_product_package_does_not_import_the_oracle():

@@ -22,8 +22,8 @@ from gpu_util import make_decoder, step_inputs, dev_status, host_bits
 pytestmark = pytest.mark.gpu
 
 
-def _run_update(hh_bits, logits, lse, ret, cnt, bt, G, budget, n_sink, grace, decay):
-    from sparse_paged_kv_page_gb300 import make_batch, sa_h2o_update
+def _run_update(hh_bits, logits, lse, ret, cnt, bt, G, budget, n_sink, grace, decay, window=False):
+    from sparse_paged_kv_page_gb300 import make_batch, sa_h2o_update, sa_h2o_update_window
     B, H, cap = ret.shape
     nslots = hh_bits.shape[0]
     hh = torch.from_numpy(hh_bits.view(np.int16)).cuda().view(torch.bfloat16)
@@ -36,8 +36,9 @@ def _run_update(hh_bits, logits, lse, ret, cnt, bt, G, budget, n_sink, grace, de
     ev = torch.full((B, H, cap), -1, dtype=torch.int32, device="cuda")
     evc = torch.zeros((B, H), dtype=torch.int32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    sa_h2o_update(make_batch(btt, sl), H, H * G, lg, cap, ls, hh, nslots, rp, rc, cap, budget,
-                  n_sink, grace, decay, evicted=ev, evicted_cnt=evc, dev_status=st)
+    fn = sa_h2o_update_window if window else sa_h2o_update
+    fn(make_batch(btt, sl), H, H * G, lg, cap, ls, hh, nslots, rp, rc, cap, budget,
+       n_sink, grace, decay, evicted=ev, evicted_cnt=evc, dev_status=st)
     torch.cuda.synchronize()
     return (host_bits(hh), rp.cpu().numpy(), rc.cpu().numpy(), ev.cpu().numpy(),
             evc.cpu().numpy(), int(st.item()))
@@ -63,7 +64,7 @@ def _inputs(rng, B, H, G, n, cap, L, zero_probs=False, tie_vals=None):
     return hh_bits, z, lse, ret, cnt, bt
 
 
-def _oracle(hh_bits, z, lse, ret, cnt, bt, G, budget, n_sink, grace, decay):
+def _oracle(hh_bits, z, lse, ret, cnt, bt, G, budget, n_sink, grace, decay, window=False):
     B, H, _ = ret.shape
     res = {}
     for b in range(B):
@@ -72,7 +73,9 @@ def _oracle(hh_bits, z, lse, ret, cnt, bt, G, budget, n_sink, grace, decay):
             pos = ret[b, h, :n]
             slots = bt[b, pos]
             hh = O.decode_kdt(hh_bits[slots, h], "bf16")
-            ex = O.h2o_fold(hh, z[b, h * G:(h + 1) * G, :n], lse[b, h * G:(h + 1) * G], decay)
+            zz = z[b, h * G:(h + 1) * G, :n]
+            ex = (O.h2o_fold_window(hh, zz, n_sink, grace, decay) if window
+                  else O.h2o_fold(hh, zz, lse[b, h * G:(h + 1) * G], decay))
             hb = O.h2o_store(ex)
             kept, _, evd = O.h2o_evict(hb, pos, budget, n_sink, grace)
             res[(b, h)] = (slots, hb, kept, sorted(evd))
@@ -93,16 +96,17 @@ def _check_eviction_valid(kept, pos, vals, budget, n_sink, grace, tol):
         assert (vals - tol)[gone].max() <= (vals + tol)[elig & ~gone].min()
 
 
+@pytest.mark.parametrize("window", [False, True])
 @pytest.mark.parametrize("n,budget", [(700, 512), (513, 512), (100, 512), (4097, 512)])
-def test_fold_and_evict_generated_inputs(n, budget):
+def test_fold_and_evict_generated_inputs(n, budget, window):
     rng = np.random.default_rng([n, budget])
     B, H, G, cap, L = 2, 3, 4, 4200, 5000
     n_sink, grace, decay = 4, 16, 0.984375
     args = _inputs(rng, B, H, G, n, cap, L)
     hh_bits, z, lse, ret, cnt, bt = args
-    got_hh, rp, rc, ev, evc, st = _run_update(*args, G, budget, n_sink, grace, decay)
+    got_hh, rp, rc, ev, evc, st = _run_update(*args, G, budget, n_sink, grace, decay, window)
     assert st == 0
-    want = _oracle(*args, G, budget, n_sink, grace, decay)
+    want = _oracle(*args, G, budget, n_sink, grace, decay, window)
     for (b, h), (slots, hb, kept, evd) in want.items():
         g = O.decode_kdt(got_hh[slots, h], "bf16")
         ulp = O.ulp_kdt(np.maximum(np.abs(g), np.abs(hb)), "bf16")
@@ -142,7 +146,7 @@ def _oracle_traj_init(wl):
     return st
 
 
-def _oracle_traj_step(wl, st, t, qb):
+def _oracle_traj_step(wl, st, t, qb, window=False):
     c = wl.cfg
     for (b, h), s in st.items():
         L = wl.seq_len(b, t + 1)
@@ -153,17 +157,19 @@ def _oracle_traj_step(wl, st, t, qb):
         vs = wl.v_seq(b, t + 1)[:, h, :]
         r = O.h2o_unit_step(s["hh"], s["pos"], ks, vs, qb[b, h * c.G:(h + 1) * c.G],
                             dtype=c.dtype, decay=c.decay, budget=c.budget, n_sink=c.n_sink,
-                            grace=c.grace, scale=c.scale)
-        s["ex"] = O.h2o_fold(s["ex"], r["logits"], r["lse"], c.decay)
+                            grace=c.grace, scale=c.scale, window_softmax=window)
+        s["ex"] = (O.h2o_fold_window(s["ex"], r["logits"], c.n_sink, c.grace, c.decay) if window
+                   else O.h2o_fold(s["ex"], r["logits"], r["lse"], c.decay))
         s["last"] = r
         keep = np.isin(s["pos"], r["kept"])
         s["pos"], s["hh"], s["ex"] = s["pos"][keep], r["hh_bf16"][keep], s["ex"][keep]
 
 
-def test_token_level_trajectory_small():
+@pytest.mark.parametrize("window", [False, True])
+def test_token_level_trajectory_small(window):
     wl = make_workload(config(4, small=True))
     c = wl.cfg
-    dec = make_decoder(wl)
+    dec = make_decoder(wl, extra=dict(window_softmax=window))
     ost = _oracle_traj_init(wl)
     agree = {k: True for k in ost}
     for t in range(c.decode_steps):
@@ -171,7 +177,7 @@ def test_token_level_trajectory_small():
         dec.step(q, kn, vn)
         torch.cuda.synchronize()
         qb = wl.q(t)
-        _oracle_traj_step(wl, ost, t, qb)
+        _oracle_traj_step(wl, ost, t, qb, window)
         rp, rc = dec.ret_pos.cpu().numpy(), dec.ret_cnt.cpu().numpy()
         hh = host_bits(dec.cache.hh)
         out = dec.out.float().cpu().numpy()

@@ -148,6 +148,54 @@ def test_select_row_lengths(maxp):
             assert np.array_equal(sel[b, h, :cnt[b, h]], O.select_pages(s[b, h], n, 256)), (b, h)
 
 
+@pytest.mark.parametrize("bos,eos", [(0, 1), (2, 1), (4, 8), (1, 3)])
+@pytest.mark.parametrize("kind", ["continuous", "ties", "specials"])
+@pytest.mark.parametrize("topk", [12, 64, 256])
+def test_select_reserved_bit_exact(bos, eos, kind, topk):
+    """Reserved leading / trailing pages (the vortex windows): reserved pages
+    kept, top-k over the window between them, against the oracle."""
+    from sparse_paged_kv_page_gb300 import make_batch, sa_select_topk_reserved
+    rng = np.random.default_rng([5, bos, eos, topk, len(kind)])
+    B, H, maxp, ps = 3, 4, 3000, 16
+    if kind == "continuous":
+        s = rng.standard_normal((B, H, maxp)).astype(np.float32)
+    elif kind == "ties":
+        s = rng.integers(-3, 4, size=(B, H, maxp)).astype(np.float32) * 0.5
+    else:
+        pool = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 1e-30, 3.0], dtype=np.float32)
+        s = rng.choice(pool, size=(B, H, maxp))
+    lens = [maxp * ps, (topk + 3) * ps - 7, (topk - 1) * ps]    # long, just above, below the budget
+    sc = torch.from_numpy(s).cuda()
+    bt = torch.zeros((B, maxp), dtype=torch.int32, device="cuda")
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    sel = torch.full((B, H, topk), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, H), -7, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sa_select_topk_reserved(sc, maxp, make_batch(bt, sl), ps, H, topk, bos, eos, sel, cnt, dev_status=st)
+    torch.cuda.synchronize()
+    sel, cnt = sel.cpu().numpy(), cnt.cpu().numpy()
+    assert int(st.item()) == 0
+    for b in range(B):
+        n = O.num_pages(lens[b], ps)
+        for h in range(H):
+            want = O.select_pages_reserved(s[b, h], n, topk, bos, eos)
+            assert cnt[b, h] == len(want)
+            assert np.array_equal(sel[b, h, :cnt[b, h]], want), (b, h)
+
+
+def test_select_reserved_rejects_bad_windows():
+    from sparse_paged_kv_page_gb300 import SaError, make_batch, sa_select_topk_reserved
+    sc = torch.zeros((1, 1, 64), device="cuda")
+    batch = make_batch(torch.zeros((1, 64), dtype=torch.int32, device="cuda"),
+                       torch.full((1,), 64 * 16, dtype=torch.int32, device="cuda"))
+    sel = torch.zeros((1, 1, 8), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    for bos, eos in [(0, 0), (-1, 1), (4, 5)]:
+        with pytest.raises(SaError) as e:
+            sa_select_topk_reserved(sc, 64, batch, 16, 1, 8, bos, eos, sel, cnt)
+        assert e.value.status == 1
+
+
 def test_select_large_candidate_count():
     rng = np.random.default_rng(5)
     B, H, maxp, ps = 1, 2, 45056, 16

@@ -55,6 +55,27 @@ def test_step_matches_separate_calls_with_append(cid, small):
     assert fused.seq_lens.cpu().tolist() == [wl.seq_len(b, steps) for b in range(wl.cfg.B)]
 
 
+def test_step_with_reserved_pages_matches_separate_calls():
+    wl = make_workload(config(2, small=False))
+    extra = dict(n_bos=2, n_eos=3)
+    fused, split = make_decoder(wl, extra=extra), make_decoder(wl, extra=extra)
+    for t in range(6):
+        q, kn, vn = step_inputs(wl, t)
+        fused.step(q, kn, vn)
+        split.append(kn, vn)
+        split.attend(q)
+        torch.cuda.synchronize()
+        _compare(_state(fused), _state(split), wl, tail_unspecified=True)
+        cnt = fused.sel_cnt.cpu().numpy()
+        sel = fused.sel_idx.cpu().numpy()
+        for b in range(wl.cfg.B):
+            n = O.num_pages(wl.seq_len(b, t + 1), wl.cfg.ps)
+            for h in range(wl.cfg.H_kv):
+                s = sel[b, h, :cnt[b, h]]
+                assert s[:2].tolist() == [0, 1] and s[-3:].tolist() == [n - 3, n - 2, n - 1]
+    assert dev_status(fused) == 0
+
+
 @pytest.mark.parametrize("cid", [1, 3])
 def test_step_without_append_is_exact(cid):
     wl, fused, split = _twins(cid)
