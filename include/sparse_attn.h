@@ -16,6 +16,8 @@
  *   sa_select_topk_reserved, sa_h2o_update_window
  *                     the selection and the H2O fold with reserved leading and
  *                     trailing pages / tokens
+ *   sa_score_pages_qh, sa_sparse_decode_qh
+ *                     scores, selection and attention per query head
  *
  * Sources (cited by page title and section):
  *   [vortex]  "flow: add H2O sparse attention (page-level and token-level,
@@ -162,6 +164,23 @@ sa_status sa_score_pages(const sa_cache* cache, const sa_batch* batch, const voi
                          int32_t max_pages, int32_t* dev_status, void* stream);
 
 /*
+ * sa_score_pages_qh -- sa_score_pages with one score row per query head.
+ *
+ * [entmax] "How it works", "Top-k": pages are ranked for each query head and
+ * the top pages are kept per query head. Each query head g of KV head h = g / G
+ * scores the pages of h from their statistics alone (no reduction over the
+ * group): S_g(p) = sum_d [w_avg q_gd mean_pd + w_peak max(q_gd max_pd, q_gd min_pd)].
+ *   scores   [batch, num_q_heads, max_pages] float32 (entries past a
+ *            request's page count untouched)
+ * Everything else as sa_score_pages. The rows select with sa_select_topk /
+ * sa_select_topk_reserved called with num_kv_heads = num_q_heads, and
+ * sa_sparse_decode_qh attends them.
+ */
+sa_status sa_score_pages_qh(const sa_cache* cache, const sa_batch* batch, const void* q,
+                            int32_t num_q_heads, float w_avg, float w_peak, float* scores,
+                            int32_t max_pages, int32_t* dev_status, void* stream);
+
+/*
  * sa_select_topk -- top-k pages per (request, KV head), tail page forced.
  *
  * [entmax] "How it works", "Top-k": keep topk pages, the budget counting the
@@ -249,6 +268,24 @@ sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* batch, const v
                            int32_t sel_stride, float scale, void* out, float* lse,
                            float* logits, int32_t logits_stride, void* workspace,
                            size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * sa_sparse_decode_qh -- sa_sparse_decode with a selection per query head.
+ *
+ * [entmax] "Top-k" (pages kept per query head) and "How it works" (exact
+ * attention over the selection): query head g attends exactly the pages its
+ * own row lists, of its KV head g / G.
+ *   sel_idx  [batch, num_q_heads, sel_stride] int32, sel_cnt [batch, num_q_heads]
+ *   workspace  sa_decode_workspace_size(batch, num_q_heads, num_q_heads,
+ *            head_dim, page_size, sel_stride) bytes (each query head a unit
+ *            of one head)
+ * q, out, lse, scale and the error behaviour as sa_sparse_decode; no logits.
+ */
+sa_status sa_sparse_decode_qh(const sa_cache* cache, const sa_batch* batch, const void* q,
+                              int32_t num_q_heads, const int32_t* sel_idx, const int32_t* sel_cnt,
+                              int32_t sel_stride, float scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream);
 
 /*
  * sa_sparse_decode_noalloc -- sa_sparse_decode without a caller workspace.

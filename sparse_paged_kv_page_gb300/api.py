@@ -19,7 +19,8 @@ __all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKV
            "sa_append_kv", "sa_score_pages", "sa_select_topk", "sa_decode_workspace_size",
            "sa_decode_workspace_init", "sa_sparse_decode", "sa_sparse_decode_noalloc",
            "sa_sparse_decode_noalloc_capacity", "sa_h2o_update", "sa_decode_step",
-           "sa_select_topk_reserved", "sa_h2o_update_window",
+           "sa_select_topk_reserved", "sa_h2o_update_window", "sa_score_pages_qh",
+           "sa_sparse_decode_qh",
            "sa_status_string",
            "sa_version", "alloc_decode_workspace"]
 
@@ -122,6 +123,30 @@ def sa_score_pages(cache: SaCache, batch: SaBatch, q, num_q_heads: int, w_avg: f
         ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads),
         float(w_avg), float(w_peak), _p(scores, torch.float32, "scores"), int(max_pages),
         _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_score_pages_qh(cache: SaCache, batch: SaBatch, q, num_q_heads: int, w_avg: float,
+                      w_peak: float, scores, max_pages: int, dev_status=None, stream=None):
+    """One score row per query head: scores [B, H_q, max_pages]."""
+    lib = _lib.load()
+    _check("sa_score_pages_qh", lib.sa_score_pages_qh(
+        ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads),
+        float(w_avg), float(w_peak), _p(scores, torch.float32, "scores"), int(max_pages),
+        _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_sparse_decode_qh(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_idx, sel_cnt,
+                        sel_stride: int, scale: float, out, lse=None, workspace=None,
+                        dev_status=None, stream=None):
+    """Attention with a selection per query head: sel_idx [B, H_q, sel_stride]."""
+    lib = _lib.load()
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("sa_sparse_decode_qh", lib.sa_sparse_decode_qh(
+        ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads),
+        _p(sel_idx, torch.int32, "sel_idx"), _p(sel_cnt, torch.int32, "sel_cnt"), int(sel_stride),
+        float(scale), _p(out, name="out"), _p(lse, torch.float32, "lse"),
+        _p(workspace, name="workspace"), wbytes, _p(dev_status, torch.int32, "dev_status"),
+        _s(stream)))
 
 
 def sa_select_topk(scores, max_pages: int, batch: SaBatch, page_size: int, num_kv_heads: int,

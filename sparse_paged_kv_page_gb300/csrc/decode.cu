@@ -11,7 +11,8 @@
 // Work unit: a tile of 16 token rows of one (request, KV head) taken in
 // selection order (row i = entry i / page_size, slot i % page_size), so a
 // 16-token page is one tile and page_size 1 gathers 16 retained tokens.
-// Grid (nsplit, H_kv, B): CTA `split` of a unit takes an equal share of the
+// Grid (nsplit, units, B) -- a unit is a KV head with its G query heads, or
+// one query head under per-query-head selection: CTA `split` of a unit takes an equal share of the
 // unit's tiles, counted on the device from sel_cnt, and first resolves the
 // selection entries it touches to (block, fill) in shared memory. Its 4 warps
 // take tiles round robin, each with a private ring of stages:
@@ -70,6 +71,7 @@ struct DecodeArgs {
   int32_t* tickets;
   int32_t* status;
   int H_kv, H_q, G, ps, ps_shift, num_blocks, bt_stride, sel_stride, logits_stride, nsplit;
+  int H_u, kv_div;  // selection units per request (H_kv, or H_q per query head) and per KV head
   int ent_max;      // entries of the selection one CTA can touch
   float scale, scale_log2;
 };
@@ -119,9 +121,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // 1024-byte aligned base for the swizzled tiles
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
+  // h: the selection unit within the request -- a KV head with its G query
+  // heads, or (per-query-head selection, G = 1) one query head of KV head kvh
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = b * a.H_kv + h;
+  const int unit = b * a.H_u + h;
+  const int kvh = h / a.kv_div;
   const int G = a.G, ps = a.ps, pss = a.ps_shift;
 
   // Q as the A operand (rows = query heads of this KV head, zero beyond G).
@@ -220,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int2 en = s_ent[ei];
         if (en.x >= 0 && s0 < en.y) {
           nvalid = min(16, en.y - s0);
-          y = int((int64_t(en.x) * a.H_kv + h) * ps + s0);
+          y = int((int64_t(en.x) * a.H_kv + kvh) * ps + s0);
         }
       }
       const uint32_t vmask = nvalid >= 16 ? 0xffffu : ((1u << nvalid) - 1u);
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           const int2 en = s_ent[ei];
           if (en.x >= 0 && s < en.y) {
             valid = true;
-            off = ((int64_t(en.x) * a.H_kv + h) * ps + s) * D;
+            off = ((int64_t(en.x) * a.H_kv + kvh) * ps + s) * D;
           }
         }
       }
@@ -711,18 +716,21 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
                       const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_stride, float scale,
                       void* out, float* lse, float* logits, int32_t logits_stride, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, void* stream, bool allow_cluster,
-                      bool pdl) {
+                      bool pdl, bool per_query_head) {
   sa_status st = check_cache(cache, true, false);
   if (st != SA_OK) return st;
   if ((st = check_batch(batch)) != SA_OK) return st;
   if (!q || !sel_idx || !sel_cnt || !out || sel_stride <= 0) return SA_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
-  const int G = num_q_heads / cache->num_kv_heads;
-  if (G > 16) return SA_ERR_UNSUPPORTED;
+  const int G_kv = num_q_heads / cache->num_kv_heads;
+  if (G_kv > 16) return SA_ERR_UNSUPPORTED;
+  // per-query-head selection: every query head is its own unit of one row
+  const int G = per_query_head ? 1 : G_kv;
+  const int H_u = per_query_head ? num_q_heads : cache->num_kv_heads;
   const int64_t rows = int64_t(sel_stride) * cache->page_size;
   if (rows > (int64_t(1) << 30)) return SA_ERR_UNSUPPORTED;
   if (logits && logits_stride < rows) return SA_ERR_INVALID_ARG;
-  const int units = batch->batch * cache->num_kv_heads;
+  const int units = batch->batch * H_u;
   const int max_tiles = int((rows + 15) / 16);
   const int ns = choose_nsplit(units, max_tiles, cache->page_size, num_sms());
   const WsLayout w = ws_layout(units, G, cache->head_dim, ns);
@@ -739,10 +747,11 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   a.ps_shift = log2i(cache->page_size); a.num_blocks = cache->num_blocks;
   a.bt_stride = batch->bt_stride; a.sel_stride = sel_stride;
   a.logits_stride = logits ? logits_stride : 0; a.nsplit = ns;
+  a.H_u = H_u; a.kv_div = per_query_head ? G_kv : 1;
   a.ent_max = ent_max_for(max_tiles, ns, cache->page_size);
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf(float(cache->head_dim));
   a.scale_log2 = a.scale * kLog2e;
-  dim3 grid(unsigned(ns), unsigned(cache->num_kv_heads), unsigned(batch->batch));
+  dim3 grid(unsigned(ns), unsigned(H_u), unsigned(batch->batch));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = cache->dtype == SA_BF16;
   if (cache->head_dim == 128)
@@ -782,7 +791,18 @@ extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* bat
                                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                       void* stream) {
   return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
-                         logits, logits_stride, workspace, workspace_bytes, dev_status, stream, true, false);
+                         logits, logits_stride, workspace, workspace_bytes, dev_status, stream, true, false,
+                         false);
+}
+
+extern "C" sa_status sa_sparse_decode_qh(const sa_cache* cache, const sa_batch* batch, const void* q,
+                                         int32_t num_q_heads, const int32_t* sel_idx,
+                                         const int32_t* sel_cnt, int32_t sel_stride, float scale,
+                                         void* out, float* lse, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
+                         nullptr, 0, workspace, workspace_bytes, dev_status, stream, true, false,
+                         true);
 }
 
 // ---------------------------------------------------------------------------
@@ -835,5 +855,5 @@ extern "C" sa_status sa_sparse_decode_noalloc(const sa_cache* cache, const sa_ba
     return SA_ERR_CUDA;
   return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
                          logits, logits_stride, ws, SA_NOALLOC_SCRATCH_BYTES, dev_status, stream,
-                         /*allow_cluster=*/false, /*pdl=*/false);
+                         /*allow_cluster=*/false, /*pdl=*/false, /*per_query_head=*/false);
 }

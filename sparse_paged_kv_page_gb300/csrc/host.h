@@ -97,7 +97,7 @@ sa_status append_impl(const sa_cache* cache, const sa_batch* batch, const void* 
                       void* stream, bool pdl);
 sa_status score_impl(const sa_cache* cache, const sa_batch* batch, const void* q, int32_t num_q_heads,
                      float w_avg, float w_peak, float* scores, int32_t max_pages, int32_t* dev_status,
-                     void* stream);
+                     void* stream, bool per_query_head);
 sa_status select_impl(const float* scores, int32_t max_pages, const sa_batch* batch, int32_t page_size,
                       int32_t num_kv_heads, int32_t topk, int32_t n_bos, int32_t n_eos,
                       int32_t* sel_idx, int32_t* sel_cnt, int32_t* dev_status, void* stream,
@@ -106,6 +106,6 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
                       const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_stride, float scale,
                       void* out, float* lse, float* logits, int32_t logits_stride, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, void* stream, bool allow_cluster,
-                      bool pdl);
+                      bool pdl, bool per_query_head);
 
 }  // namespace sa

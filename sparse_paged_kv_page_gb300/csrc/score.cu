@@ -64,11 +64,15 @@ struct ScoreArgs {
   float w_avg, w_peak;
 };
 
-template <int D>
+// kQH: one score per query head (no group mean); its query coefficients for
+// G <= 16 heads live in a shared-memory table after a 3-stage ring.
+template <int D, bool kQH = false>
 struct ScoreTile {
   static constexpr int kPageBytes = 3 * D * 2;             // min, max, mean rows
   static constexpr int kStageBytes = kChunk * kPageBytes;
-  static constexpr int kSmem = kStages * kStageBytes;
+  static constexpr int kNStages = kQH ? 3 : kStages;
+  static constexpr int kCoefBytes = kQH ? 16 * 3 * D * 4 : 0;
+  static constexpr int kSmem = kNStages * kStageBytes + kCoefBytes;
 };
 
 struct ChunkHdr {
@@ -76,14 +80,16 @@ struct ChunkHdr {
   uint32_t valid;                                          // bit j: page p0+j has a good block
 };
 
-template <typename T, int D>
+template <typename T, int D, bool kQH>
 __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs a) {
   using E = Elem<T>;
-  using TL = ScoreTile<D>;
+  using TL = ScoreTile<D, kQH>;
+  constexpr int NS = TL::kNStages;
   constexpr int LPP = D / 8;                               // lanes per page
   constexpr int PPP = 32 * kConsumerWarps / LPP;           // pages per consumer pass
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t coef_bar;               // per-head mode: consumers meet here
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ ChunkHdr hdr[kStages];
   __shared__ int s_prefix[kMaxBatch + 1];                  // chunks before request b
@@ -124,10 +130,11 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
         }
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), kConsumerWarps);
     }
+    mbar_init(smem_u32(&coef_bar), 32 * kConsumerWarps);
     mbar_init_fence();
   }
   __syncthreads();
@@ -171,8 +178,8 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
         locate(ci + 2, b2, g2, p02, c2);
         k2 = lane < c2 ? a.bt[int64_t(b2) * a.bt_stride + p02 + lane] : -1;
       }
-      const int s = it % kStages;
-      if (it >= kStages && !mbar_wait(smem_u32(&empty_bar[s]), ((it / kStages) - 1) & 1, a.status)) {
+      const int s = it % NS;
+      if (it >= NS && !mbar_wait(smem_u32(&empty_bar[s]), ((it / NS) - 1) & 1, a.status)) {
         ok = false;
         break;
       }
@@ -195,13 +202,94 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
     // never leave with copies in flight: wait (bounded) for the last stages
     if (lane == 0) {
       const int n_it = c_end - c_begin;
-      for (int it = max(0, n_it - kStages); it < n_it && ok; ++it)
-        ok = mbar_wait(smem_u32(&full_bar[it % kStages]), (it / kStages) & 1, a.status);
+      for (int it = max(0, n_it - NS); it < n_it && ok; ++it)
+        ok = mbar_wait(smem_u32(&full_bar[it % NS]), (it / NS) & 1, a.status);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
+  if constexpr (kQH) {
+    // One score per query head: a lane group serves one page of the chunk's
+    // KV head (Hc = 1) and forms the G dot products from a coefficient table
+    // built in shared memory whenever the chunk's (request, head) changes. The
+    // consumers meet on an mbarrier around each rebuild (waits are bounded).
+    const int grp = tid / LPP, l = tid % LPP;
+    float* coef = reinterpret_cast<float*>(smem + NS * TL::kStageBytes);   // [g][avg, pos, neg][D]
+    const uint32_t cb = smem_u32(&coef_bar);
+    uint32_t cphase = 0;
+    bool alive = true;
+    auto meet = [&]() {
+      mbar_arrive(cb);
+      alive = alive && mbar_wait(cb, cphase, a.status);
+      cphase ^= 1u;
+    };
+    int cur_b = -1, cur_h = -1;
+    for (int ci = c_begin, it = 0; ci < c_end && alive; ++ci, ++it) {
+      const int s = it % NS;
+      if (!mbar_wait(smem_u32(&full_bar[s]), (it / NS) & 1, a.status)) break;
+      const ChunkHdr hd = hdr[s];
+      const int head = hd.hg;
+      if (hd.b != cur_b || head != cur_h) {
+        if (cur_b >= 0) meet();                  // every consumer is done with the old table
+        cur_b = hd.b;
+        cur_h = head;
+        const uint16_t* qh = static_cast<const uint16_t*>(a.q) + (int64_t(cur_b) * a.H_q + int64_t(cur_h) * a.G) * D;
+        for (int idx = tid; idx < a.G * D; idx += 32 * kConsumerWarps) {
+          const float x = E::to_f(qh[idx]);
+          const int g = idx / D, d = idx % D;
+          coef[(g * 3 + 0) * D + d] = a.w_avg * x;
+          coef[(g * 3 + 1) * D + d] = a.w_peak * fmaxf(x, 0.f);
+          coef[(g * 3 + 2) * D + d] = a.w_peak * fminf(x, 0.f);
+        }
+        meet();                                  // the new table is complete
+        if (!alive) break;
+      }
+      float* out = a.scores + (int64_t(hd.b) * a.H_q + int64_t(head) * a.G) * a.max_pages + hd.p0;
+      const uint8_t* st = smem + s * TL::kStageBytes;
+#pragma unroll 1
+      for (int pass = 0; pass < kChunk / PPP; ++pass) {
+        const int j = pass * PPP + grp;
+        const bool here = j < hd.count && ((hd.valid >> j) & 1u);
+        uint4 vmn = make_uint4(0, 0, 0, 0), vmx = vmn, vme = vmn;
+        if (here) {
+          const uint8_t* pg = st + j * TL::kPageBytes + l * 16;
+          vmn = *reinterpret_cast<const uint4*>(pg);
+          vmx = *reinterpret_cast<const uint4*>(pg + D * 2);
+          vme = *reinterpret_cast<const uint4*>(pg + 2 * D * 2);
+        }
+        const uint32_t m0[4] = {vmn.x, vmn.y, vmn.z, vmn.w};
+        const uint32_t m1[4] = {vmx.x, vmx.y, vmx.z, vmx.w};
+        const uint32_t m2[4] = {vme.x, vme.y, vme.z, vme.w};
+        for (int g = 0; g < a.G; ++g) {
+          const float4* cf = reinterpret_cast<const float4*>(coef + g * 3 * D + l * 8);
+          const float4 a0 = cf[0], a1 = cf[1];
+          const float4 p0 = cf[D / 4], p1 = cf[D / 4 + 1];
+          const float4 n0 = cf[D / 2], n1 = cf[D / 2 + 1];
+          const float ca[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const float cp[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+          const float cn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc = fmaf(ca[2 * e], E::lo(m2[e]), acc);
+            acc = fmaf(ca[2 * e + 1], E::hi(m2[e]), acc);
+            acc = fmaf(cp[2 * e], E::lo(m1[e]), acc);
+            acc = fmaf(cp[2 * e + 1], E::hi(m1[e]), acc);
+            acc = fmaf(cn[2 * e], E::lo(m0[e]), acc);
+            acc = fmaf(cn[2 * e + 1], E::hi(m0[e]), acc);
+          }
+#pragma unroll
+          for (int o = LPP / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+          if (l == 0 && j < hd.count) out[int64_t(g) * a.max_pages + j] = here ? acc : __int_as_float(0x7fc00000);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+    }
+    return;
+  }
+
   // lane group grp serves (page, head) pairs grp, grp + PPP, ... of a chunk;
   // PPP is a multiple of Hc, so its head within the group is always grp % Hc
   const int grp = tid / LPP, l = tid % LPP;
@@ -209,8 +297,8 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
   float ca[8], cp[8], cn[8];
   int cur_b = -1, cur_h = -1;
   for (int ci = c_begin, it = 0; ci < c_end; ++ci, ++it) {
-    const int s = it % kStages;
-    if (!mbar_wait(smem_u32(&full_bar[s]), (it / kStages) & 1, a.status)) break;
+    const int s = it % NS;
+    if (!mbar_wait(smem_u32(&full_bar[s]), (it / NS) & 1, a.status)) break;
     const ChunkHdr hd = hdr[s];
     const int head = (hd.hg << hcs) + hl;
     if (hd.b != cur_b || head != cur_h) {
@@ -275,13 +363,13 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
   }
 }
 
-int g_sc_smem[4][64];
+int g_sc_smem[8][64];
 
-template <typename T, int D>
+template <typename T, int D, bool kQH>
 sa_status launch_score(const ScoreArgs& a, int grid, cudaStream_t s, int* cache) {
-  auto k = score_kernel<T, D>;
-  if (!ensure_smem(k, ScoreTile<D>::kSmem, cache)) return SA_ERR_CUDA;
-  k<<<grid, kScThreads, ScoreTile<D>::kSmem, s>>>(a);
+  auto k = score_kernel<T, D, kQH>;
+  if (!ensure_smem(k, ScoreTile<D, kQH>::kSmem, cache)) return SA_ERR_CUDA;
+  k<<<grid, kScThreads, ScoreTile<D, kQH>::kSmem, s>>>(a);
   return launch_status();
 }
 
@@ -303,7 +391,7 @@ int sm_count() {
 
 sa_status sa::score_impl(const sa_cache* cache, const sa_batch* batch, const void* q,
                         int32_t num_q_heads, float w_avg, float w_peak, float* scores,
-                        int32_t max_pages, int32_t* dev_status, void* stream) {
+                        int32_t max_pages, int32_t* dev_status, void* stream, bool per_query_head) {
   using namespace sa;
   sa_status st = check_cache(cache, false, true);
   if (st != SA_OK) return st;
@@ -323,7 +411,7 @@ sa_status sa::score_impl(const sa_cache* cache, const sa_batch* batch, const voi
   // consumers' lane groups (128 / (head_dim / 8))
   const int groups = 32 * kConsumerWarps / (cache->head_dim / 8);
   int hc = 1;
-  while (hc < groups && a.H_kv % (2 * hc) == 0) hc *= 2;
+  while (!per_query_head && hc < groups && a.H_kv % (2 * hc) == 0) hc *= 2;
   a.hc_shift = log2i(hc);
   // enough persistent CTAs for two per SM, never more than chunks could exist
   const int cap = max_pages < batch->bt_stride ? max_pages : batch->bt_stride;
@@ -333,16 +421,31 @@ sa_status sa::score_impl(const sa_cache* cache, const sa_batch* batch, const voi
   const int grid = int(max_chunks < full ? max_chunks : full);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = cache->dtype == SA_BF16;
+  if (per_query_head) {
+    if (cache->head_dim == 128)
+      return bf ? launch_score<__nv_bfloat16, 128, true>(a, grid, s, g_sc_smem[4])
+                : launch_score<__half, 128, true>(a, grid, s, g_sc_smem[5]);
+    return bf ? launch_score<__nv_bfloat16, 64, true>(a, grid, s, g_sc_smem[6])
+              : launch_score<__half, 64, true>(a, grid, s, g_sc_smem[7]);
+  }
   if (cache->head_dim == 128)
-    return bf ? launch_score<__nv_bfloat16, 128>(a, grid, s, g_sc_smem[0])
-              : launch_score<__half, 128>(a, grid, s, g_sc_smem[1]);
-  return bf ? launch_score<__nv_bfloat16, 64>(a, grid, s, g_sc_smem[2])
-            : launch_score<__half, 64>(a, grid, s, g_sc_smem[3]);
+    return bf ? launch_score<__nv_bfloat16, 128, false>(a, grid, s, g_sc_smem[0])
+              : launch_score<__half, 128, false>(a, grid, s, g_sc_smem[1]);
+  return bf ? launch_score<__nv_bfloat16, 64, false>(a, grid, s, g_sc_smem[2])
+            : launch_score<__half, 64, false>(a, grid, s, g_sc_smem[3]);
 }
 
 extern "C" sa_status sa_score_pages(const sa_cache* cache, const sa_batch* batch, const void* q,
                                     int32_t num_q_heads, float w_avg, float w_peak, float* scores,
                                     int32_t max_pages, int32_t* dev_status, void* stream) {
   return sa::score_impl(cache, batch, q, num_q_heads, w_avg, w_peak, scores, max_pages, dev_status,
-                        stream);
+                        stream, false);
+}
+
+extern "C" sa_status sa_score_pages_qh(const sa_cache* cache, const sa_batch* batch, const void* q,
+                                       int32_t num_q_heads, float w_avg, float w_peak,
+                                       float* scores, int32_t max_pages, int32_t* dev_status,
+                                       void* stream) {
+  return sa::score_impl(cache, batch, q, num_q_heads, w_avg, w_peak, scores, max_pages, dev_status,
+                        stream, true);
 }

@@ -47,7 +47,8 @@ extern "C" sa_status sa_decode_step(const sa_cache* cache, const sa_batch* batch
                      0, dev_status, stream, false);
     if (st != SA_OK) return st;
   }
-  st = score_impl(cache, batch, q, num_q_heads, w_avg, w_peak, scores, max_pages, dev_status, stream);
+  st = score_impl(cache, batch, q, num_q_heads, w_avg, w_peak, scores, max_pages, dev_status, stream,
+                  false);
   if (st != SA_OK) return st;
   if (overlap) {
     st = append_impl(cache, batch, k_new, v_new, new_cu, 1, nullptr, nullptr, nullptr, 0, dev_status,
@@ -58,5 +59,5 @@ extern "C" sa_status sa_decode_step(const sa_cache* cache, const sa_batch* batch
                    n_eos, sel_idx, sel_cnt, dev_status, stream, true);
   if (st != SA_OK) return st;
   return decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, topk, scale, out, lse, nullptr, 0,
-                     workspace, workspace_bytes, dev_status, stream, true, true);
+                     workspace, workspace_bytes, dev_status, stream, true, true, false);
 }

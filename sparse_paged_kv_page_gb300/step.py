@@ -20,7 +20,8 @@ import torch
 
 from .api import (PagedKVCache, alloc_decode_workspace, make_batch, sa_append_kv,
                   sa_decode_step, sa_h2o_update, sa_h2o_update_window, sa_score_pages,
-                  sa_select_topk_reserved, sa_sparse_decode)
+                  sa_score_pages_qh, sa_select_topk_reserved, sa_sparse_decode,
+                  sa_sparse_decode_qh)
 
 
 class SparseDecoder:
@@ -29,13 +30,16 @@ class SparseDecoder:
                  topk: int = 0, w_avg: float = 1.0, w_peak: float = 0.25, scale: float = 0.0,
                  budget: int = 0, n_sink: int = 0, grace: int = 0, decay: float = 1.0,
                  ret_cap: int = 0, n_bos: int = 0, n_eos: int = 1, window_softmax: bool = False,
-                 device="cuda"):
+                 per_query_head: bool = False, device="cuda"):
         self.B, self.H_q, self.H_kv, self.D = batch, num_q_heads, num_kv_heads, head_dim
         self.ps, self.dtype, self.device = page_size, dtype, torch.device(device)
         self.token_level = page_size == 1 and ret_cap > 0
         self.topk, self.w_avg, self.w_peak, self.scale = topk, w_avg, w_peak, scale
         self.budget, self.n_sink, self.grace, self.decay = budget, n_sink, grace, decay
         self.n_bos, self.n_eos, self.window_softmax = n_bos, n_eos, window_softmax
+        # per-query-head selection: score, select and attend one row per query head
+        self.qh = per_query_head and not self.token_level
+        rows = num_q_heads if self.qh else num_kv_heads
         self.cache = PagedKVCache(num_blocks, num_kv_heads, page_size, head_dim, dtype, device,
                                   with_meta=not self.token_level, with_hh=self.token_level)
         i32 = dict(dtype=torch.int32, device=device)
@@ -56,15 +60,16 @@ class SparseDecoder:
         else:
             if topk <= 0:
                 raise ValueError("page-level decoding needs topk >= 1")
-            self.scores = torch.empty((batch, num_kv_heads, bt_stride), dtype=torch.float32,
+            self.scores = torch.empty((batch, rows, bt_stride), dtype=torch.float32,
                                       device=device)
-            self.sel_idx = torch.zeros((batch, num_kv_heads, topk), **i32)
-            self.sel_cnt = torch.zeros((batch, num_kv_heads), **i32)
+            self.sel_idx = torch.zeros((batch, rows, topk), **i32)
+            self.sel_cnt = torch.zeros((batch, rows), **i32)
             self.sel_stride = topk
         self.out = torch.empty((batch, num_q_heads, head_dim), dtype=dtype, device=device)
         self.lse = torch.empty((batch, num_q_heads), dtype=torch.float32, device=device)
-        self.workspace = alloc_decode_workspace(batch, num_kv_heads, num_q_heads, head_dim,
-                                                page_size, self.sel_stride, device)
+        self.workspace = alloc_decode_workspace(batch, rows if not self.token_level else num_kv_heads,
+                                                num_q_heads, head_dim, page_size, self.sel_stride,
+                                                device)
         self.dev_status = torch.zeros((1,), **i32)
         self.decode_cu = torch.arange(batch + 1, **i32)
         self.q_buf = torch.zeros((batch, num_q_heads, head_dim), dtype=dtype, device=device)
@@ -110,6 +115,15 @@ class SparseDecoder:
                           self.ret_cap, self.budget, self.n_sink, self.grace, self.decay,
                           evicted=self.evicted, evicted_cnt=self.evicted_cnt,
                           dev_status=self.dev_status)
+        elif self.qh:
+            sa_score_pages_qh(self.cache.struct, self.batch, q, self.H_q, self.w_avg, self.w_peak,
+                              self.scores, self.max_pages, dev_status=self.dev_status)
+            sa_select_topk_reserved(self.scores, self.max_pages, self.batch, self.ps, self.H_q,
+                                    self.topk, self.n_bos, self.n_eos, self.sel_idx, self.sel_cnt,
+                                    dev_status=self.dev_status)
+            sa_sparse_decode_qh(self.cache.struct, self.batch, q, self.H_q, self.sel_idx,
+                                self.sel_cnt, self.topk, self.scale, self.out, lse=self.lse,
+                                workspace=self.workspace, dev_status=self.dev_status)
         else:
             sa_score_pages(self.cache.struct, self.batch, q, self.H_q, self.w_avg, self.w_peak,
                            self.scores, self.max_pages, dev_status=self.dev_status)
@@ -123,7 +137,7 @@ class SparseDecoder:
 
     def step(self, q: torch.Tensor, k_new: Optional[torch.Tensor] = None,
              v_new: Optional[torch.Tensor] = None):
-        if self.token_level:
+        if self.token_level or self.qh:
             if k_new is not None:
                 self.append(k_new, v_new)
             return self.attend(q)

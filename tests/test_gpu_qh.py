@@ -1,0 +1,86 @@
+"""Per-query-head selection ([entmax] "Top-k": pages kept per query head) on
+the GPU against the oracle: each query head's scores (the oracle's page score
+with a group of one), a valid top-k per query head, and each head's attention
+over exactly its own selected pages.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from sa_synth import config, make_workload
+from gpu_util import (make_decoder, dev_bits, dev_status, step_inputs, score_norm, assert_scores,
+                      score_error_bound, assert_selection_valid, assert_attention)
+
+pytestmark = pytest.mark.gpu
+
+
+def _head_oracle(wl, b, g, steps_done, q_bits):
+    """Scores, score scale and length for query head g of request b."""
+    c = wl.cfg
+    h = g // c.G
+    L = wl.seq_len(b, steps_done)
+    mn, mx, me = O.head_meta(wl.k_seq(b, steps_done)[:, h, :], L, c.ps, c.dtype)
+    q = O.decode_kdt(q_bits[g:g + 1], c.dtype)
+    return O.score_pages(mn, mx, me, q, c.w_avg, c.w_peak), score_norm(mn, mx, me, q, c.w_avg, c.w_peak), L
+
+
+@pytest.mark.parametrize("cid,G,D", [(1, 4, 64), (2, 4, 128), (3, 4, 128), (3, 1, 128), (3, 16, 64),
+                                      (5, 8, 128)])
+def test_per_head_scores_selection_and_attention(cid, G, D):
+    cfg = config(cid, small=True)
+    cfg = cfg.replace(H_q=cfg.H_kv * G, D=D)
+    wl = make_workload(cfg)
+    c = wl.cfg
+    dec = make_decoder(wl, extra=dict(per_query_head=True))
+    steps = min(wl.total_steps, 3)
+    for t in range(max(steps, 1)):
+        if steps:
+            q, kn, vn = step_inputs(wl, t)
+            dec.step(q, kn, vn)
+            done = t + 1
+        else:
+            q = dev_bits(wl.q(0), c.dtype)
+            dec.step(q)
+            done = 0
+        torch.cuda.synchronize()
+        qb = wl.q(t)
+        scores = dec.scores.cpu().numpy()
+        sel, cnt = dec.sel_idx.cpu().numpy(), dec.sel_cnt.cpu().numpy()
+        out, lse = dec.out.float().cpu().numpy(), dec.lse.cpu().numpy()
+        for b in range(c.B):
+            for g in range(c.H_q):
+                S, A, L = _head_oracle(wl, b, g, done, qb[b])
+                n = O.num_pages(L, c.ps)
+                assert_scores(scores[b, g, :n], S, A)
+                got = sel[b, g, :cnt[b, g]]
+                assert cnt[b, g] == min(c.topk, n)
+                assert_selection_valid(got, S, score_error_bound(A, c.D, 1), n, c.topk)
+                # this head's attention over exactly the pages it selected
+                h = g // c.G
+                pos = O.selected_positions(got, L, c.ps)
+                ks = O.decode_kdt(wl.k_seq(b, done)[pos, h, :], c.dtype)
+                vs = O.decode_kdt(wl.v_seq(b, done)[pos, h, :], c.dtype)
+                qq = O.decode_kdt(qb[b, g:g + 1], c.dtype)
+                o, l, _ = O.attention(qq, ks, vs, c.scale if c.scale > 0 else O.default_scale(c.D))
+                assert_attention(out[b, g:g + 1], o, lse[b, g:g + 1], l)
+    assert dev_status(dec) == 0
+
+
+def test_per_head_equals_group_of_one():
+    """With G = 1 per-query-head and per-KV-head selection are the same thing:
+    bit-identical scores, selection and outputs."""
+    cfg = config(3, small=True).replace(H_q=2, H_kv=2)
+    wl = make_workload(cfg)
+    a = make_decoder(wl, extra=dict(per_query_head=True))
+    b = make_decoder(wl)
+    q = dev_bits(wl.q(0), cfg.dtype)
+    a.attend(q)
+    b.attend(q)
+    torch.cuda.synchronize()
+    for r in range(cfg.B):                      # entries past a request's pages are untouched
+        n = O.num_pages(int(wl.prefill_lens[r]), cfg.ps)
+        assert torch.equal(a.scores[r, :, :n].view(torch.int32), b.scores[r, :, :n].view(torch.int32))
+    assert torch.equal(a.sel_idx, b.sel_idx) and torch.equal(a.sel_cnt, b.sel_cnt)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.lse.view(torch.int32), b.lse.view(torch.int32))
