@@ -62,15 +62,17 @@ def aggregate_steps_per_s(max_ms: float, world: int) -> float:
 # ---------------------------------------------------------------------------
 # byte model
 # ---------------------------------------------------------------------------
-def step_bytes(cfg, lens):
+def step_bytes(cfg, lens, per_query_head=False):
     """Algorithmic bytes of one page-level step: the 3 statistics rows of every
-    page, the K and V of the selected pages, q and out (2-byte elements)."""
+    page, the K and V of the selected pages (per KV head, or per query head
+    with per-query-head selection), q and out (2-byte elements)."""
     e = 2
     tot = 0
+    rows = cfg.H_q if per_query_head else cfg.H_kv
     for L in lens:
         n = -(-L // cfg.ps)
         tot += n * cfg.H_kv * 3 * cfg.D * e
-        tot += min(cfg.topk, n) * cfg.H_kv * 2 * cfg.ps * cfg.D * e
+        tot += min(cfg.topk, n) * rows * 2 * cfg.ps * cfg.D * e
     return tot + 2 * cfg.B * cfg.H_q * cfg.D * e
 
 
@@ -301,7 +303,8 @@ def run_gpu(args, rank, world):
         kw.update(budget=c.budget, n_sink=c.n_sink, grace=c.grace, decay=c.decay,
                   ret_cap=int(wl.prefill_lens.max()) + n_in + 4)
     else:
-        kw.update(topk=c.topk, w_avg=c.w_avg, w_peak=c.w_peak)
+        kw.update(topk=c.topk, w_avg=c.w_avg, w_peak=c.w_peak,
+                  per_query_head=args.per_query_head)
     dec = SparseDecoder(**kw)
     fill_stale(dec.cache.k, "normal3", 11)
     fill_stale(dec.cache.v, "normal3", 12)
@@ -384,7 +387,7 @@ def run_gpu(args, rank, world):
         bytes_per_step = h2o_step_bytes(c, [min(n + 1, c.budget + 1) for n in cnt_start])
     else:
         bytes_per_step = statistics.mean(
-            step_bytes(c, [L + (i + 1 if append else 0) for L in lens_start])
+            step_bytes(c, [L + (i + 1 if append else 0) for L in lens_start], args.per_query_head)
             for i in range(args.steps))
     status = int(dec.dev_status.item())
 
@@ -419,15 +422,18 @@ def run_gpu(args, rank, world):
                             dev_status=dec.dev_status)
             j += 1; e[j].record(stream)
         else:
-            S.sa_score_pages(dec.cache.struct, dec.batch, dec.q_buf, c.H_q, c.w_avg, c.w_peak,
-                             dec.scores, dec.max_pages, dev_status=dec.dev_status)
+            qh = args.per_query_head
+            (S.sa_score_pages_qh if qh else S.sa_score_pages)(
+                dec.cache.struct, dec.batch, dec.q_buf, c.H_q, c.w_avg, c.w_peak,
+                dec.scores, dec.max_pages, dev_status=dec.dev_status)
             j += 1; e[j].record(stream)
-            S.sa_select_topk(dec.scores, dec.max_pages, dec.batch, c.ps, c.H_kv, c.topk,
-                             dec.sel_idx, dec.sel_cnt, dev_status=dec.dev_status)
+            S.sa_select_topk(dec.scores, dec.max_pages, dec.batch, c.ps, c.H_q if qh else c.H_kv,
+                             c.topk, dec.sel_idx, dec.sel_cnt, dev_status=dec.dev_status)
             j += 1; e[j].record(stream)
-            S.sa_sparse_decode(dec.cache.struct, dec.batch, dec.q_buf, c.H_q, dec.sel_idx,
-                               dec.sel_cnt, c.topk, c.scale, dec.out, lse=dec.lse,
-                               workspace=dec.workspace, dev_status=dec.dev_status)
+            (S.sa_sparse_decode_qh if qh else S.sa_sparse_decode)(
+                dec.cache.struct, dec.batch, dec.q_buf, c.H_q, dec.sel_idx,
+                dec.sel_cnt, c.topk, c.scale, dec.out, lse=dec.lse,
+                workspace=dec.workspace, dev_status=dec.dev_status)
             j += 1; e[j].record(stream)
         torch.cuda.synchronize()
         for k, n in enumerate(names):
@@ -491,6 +497,8 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=2)
     ap.add_argument("--workers", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--per-query-head", action="store_true",
+                    help="select pages per query head (score, select, attend one row per query head)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -572,7 +580,8 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["max_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": c.dtype, "data": "synthetic",
-        "config": {"workload": describe(c),
+        "config": {"workload": describe(c) + (", pages selected per query head"
+                                              if args.per_query_head else ""),
                    "l2": "flushed between steps outside the events: 256 MB write, then a 256 MB read so the flush's dirty lines are written back before the step",
                    "timing": "CUDA events around each step (graph replay); the step's q / k_new / v_new are copied from the HBM-resident input set into its input buffers before the events",
                    "parallelism": f"independent batch per GPU x{world}"},

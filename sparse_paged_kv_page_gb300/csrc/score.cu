@@ -69,9 +69,13 @@ struct ScoreArgs {
 template <int D, bool kQH = false>
 struct ScoreTile {
   static constexpr int kPageBytes = 3 * D * 2;             // min, max, mean rows
-  static constexpr int kStageBytes = kChunk * kPageBytes;
+  // per-query-head pages sit 16 bytes apart beyond their rows so that eight
+  // of them read at one column by ldmatrix hit eight different bank groups
+  static constexpr int kPageStride = kQH ? kPageBytes + 16 : kPageBytes;
+  static constexpr int kStageBytes = kChunk * kPageStride;
   static constexpr int kNStages = kQH ? 3 : kStages;
-  static constexpr int kCoefBytes = kQH ? 16 * 3 * D * 4 : 0;
+  static constexpr int kCoefRow = (3 * D + 8) * 2;         // padded coefficient row, bytes
+  static constexpr int kCoefBytes = kQH ? 2 * 16 * kCoefRow : 0;
   static constexpr int kSmem = kNStages * kStageBytes + kCoefBytes;
 };
 
@@ -195,8 +199,8 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
       if (good) {
         const uint8_t* src = static_cast<const uint8_t*>(a.meta) +
                              (int64_t(blk) * a.H_kv + (hg << hcs)) * int64_t(TL::kPageBytes);
-        bulk_g2s(smem_u32(smem + s * TL::kStageBytes + lane * bytes), src, bytes,
-                 smem_u32(&full_bar[s]));
+        bulk_g2s(smem_u32(smem + s * TL::kStageBytes + lane * (kQH ? uint32_t(TL::kPageStride) : bytes)),
+                 src, bytes, smem_u32(&full_bar[s]));
       }
     }
     // never leave with copies in flight: wait (bounded) for the last stages
@@ -210,12 +214,20 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
 
   // -------------------------------------------------------------- consumers
   if constexpr (kQH) {
-    // One score per query head: a lane group serves one page of the chunk's
-    // KV head (Hc = 1) and forms the G dot products from a coefficient table
-    // built in shared memory whenever the chunk's (request, head) changes. The
-    // consumers meet on an mbarrier around each rebuild (waits are bounded).
-    const int grp = tid / LPP, l = tid % LPP;
-    float* coef = reinterpret_cast<float*>(smem + NS * TL::kStageBytes);   // [g][avg, pos, neg][D]
+    // One score per query head, as a small dense product on the tensor cores:
+    // S[g, page] = sum_k A[g, k] B[k, page] with k over the page's 3D
+    // statistics (min | max | mean) and A[g] = (w_peak q_g^-, w_peak q_g^+,
+    // w_avg q_g). A is held in the element type as two terms, hi = round(A)
+    // and lo = round(A - hi) (about 16 significant bits), in rows g and g + 8
+    // of a 16-row tile, so one m16n8k16 product accumulates both in float32
+    // and their sum is the score. The table is rebuilt whenever the chunk's
+    // (request, KV head) changes, the consumers meeting on a bounded mbarrier
+    // around the rebuild. Warp w takes pages 8w .. 8w+7 of the chunk (Hc = 1,
+    // 32 pages).
+    constexpr int KD = 3 * D;
+    uint8_t* coef = smem + NS * TL::kStageBytes;          // [mtile][16 rows][KD + 8] elements
+    const uint32_t coef_s = smem_u32(coef);
+    const int mtiles = a.G > 8 ? 2 : 1;
     const uint32_t cb = smem_u32(&coef_bar);
     uint32_t cphase = 0;
     bool alive = true;
@@ -225,6 +237,7 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
       cphase ^= 1u;
     };
     int cur_b = -1, cur_h = -1;
+    const int g4 = lane >> 2, t4 = lane & 3;
     for (int ci = c_begin, it = 0; ci < c_end && alive; ++ci, ++it) {
       const int s = it % NS;
       if (!mbar_wait(smem_u32(&full_bar[s]), (it / NS) & 1, a.status)) break;
@@ -235,53 +248,56 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
         cur_b = hd.b;
         cur_h = head;
         const uint16_t* qh = static_cast<const uint16_t*>(a.q) + (int64_t(cur_b) * a.H_q + int64_t(cur_h) * a.G) * D;
-        for (int idx = tid; idx < a.G * D; idx += 32 * kConsumerWarps) {
-          const float x = E::to_f(qh[idx]);
-          const int g = idx / D, d = idx % D;
-          coef[(g * 3 + 0) * D + d] = a.w_avg * x;
-          coef[(g * 3 + 1) * D + d] = a.w_peak * fmaxf(x, 0.f);
-          coef[(g * 3 + 2) * D + d] = a.w_peak * fminf(x, 0.f);
+        for (int idx = tid; idx < mtiles * 8 * KD; idx += 32 * kConsumerWarps) {
+          const int mt = idx / (8 * KD), r = (idx / KD) % 8, k = idx % KD;
+          const int g = mt * 8 + r;
+          float c = 0.f;
+          if (g < a.G) {
+            const float x = E::to_f(qh[g * D + (k % D)]);
+            c = k < D ? a.w_peak * fminf(x, 0.f) : (k < 2 * D ? a.w_peak * fmaxf(x, 0.f) : a.w_avg * x);
+          }
+          const uint16_t hi = E::from_f(c);
+          const uint16_t lo = E::from_f(c - E::to_f(hi));
+          uint16_t* row = reinterpret_cast<uint16_t*>(coef + (mt * 16 + r) * TL::kCoefRow);
+          row[k] = hi;
+          row[8 * TL::kCoefRow / 2 + k] = lo;    // row r + 8
         }
         meet();                                  // the new table is complete
         if (!alive) break;
       }
-      float* out = a.scores + (int64_t(hd.b) * a.H_q + int64_t(head) * a.G) * a.max_pages + hd.p0;
-      const uint8_t* st = smem + s * TL::kStageBytes;
-#pragma unroll 1
-      for (int pass = 0; pass < kChunk / PPP; ++pass) {
-        const int j = pass * PPP + grp;
-        const bool here = j < hd.count && ((hd.valid >> j) & 1u);
-        uint4 vmn = make_uint4(0, 0, 0, 0), vmx = vmn, vme = vmn;
-        if (here) {
-          const uint8_t* pg = st + j * TL::kPageBytes + l * 16;
-          vmn = *reinterpret_cast<const uint4*>(pg);
-          vmx = *reinterpret_cast<const uint4*>(pg + D * 2);
-          vme = *reinterpret_cast<const uint4*>(pg + 2 * D * 2);
-        }
-        const uint32_t m0[4] = {vmn.x, vmn.y, vmn.z, vmn.w};
-        const uint32_t m1[4] = {vmx.x, vmx.y, vmx.z, vmx.w};
-        const uint32_t m2[4] = {vme.x, vme.y, vme.z, vme.w};
-        for (int g = 0; g < a.G; ++g) {
-          const float4* cf = reinterpret_cast<const float4*>(coef + g * 3 * D + l * 8);
-          const float4 a0 = cf[0], a1 = cf[1];
-          const float4 p0 = cf[D / 4], p1 = cf[D / 4 + 1];
-          const float4 n0 = cf[D / 2], n1 = cf[D / 2 + 1];
-          const float ca[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-          const float cp[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-          const float cn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-          float acc = 0.f;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc = fmaf(ca[2 * e], E::lo(m2[e]), acc);
-            acc = fmaf(ca[2 * e + 1], E::hi(m2[e]), acc);
-            acc = fmaf(cp[2 * e], E::lo(m1[e]), acc);
-            acc = fmaf(cp[2 * e + 1], E::hi(m1[e]), acc);
-            acc = fmaf(cn[2 * e], E::lo(m0[e]), acc);
-            acc = fmaf(cn[2 * e + 1], E::hi(m0[e]), acc);
+      const int j0 = warp * 8;
+      if (j0 < hd.count) {
+        const uint32_t st = smem_u32(smem + s * TL::kStageBytes);
+        // B rows: pages j0 .. j0+7 (lanes 0-7: k 0-7 of the step, lanes 8-15: k 8-15)
+        const uint32_t baddr = st + (j0 + (lane & 7)) * TL::kPageStride + ((lane >> 3) & 1) * 16;
+        // A rows: lane L addresses row (L>>3 & 1) * 8 + (L & 7), k offset (L >> 4) * 8
+        const uint32_t aaddr = coef_s + (((lane >> 3) & 1) * 8 + (lane & 7)) * TL::kCoefRow + (lane >> 4) * 16;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 4
+        for (int kk = 0; kk < KD / 16; ++kk) {
+          uint32_t bfr[2];
+          asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+                       : "=r"(bfr[0]), "=r"(bfr[1])
+                       : "r"(baddr + kk * 32));
+          uint32_t afr[4];
+          ldmatrix_x4(afr, aaddr + kk * 32);
+          E::mma(acc[0], afr, bfr[0], bfr[1]);
+          if (mtiles > 1) {
+            ldmatrix_x4(afr, aaddr + 16 * TL::kCoefRow + kk * 32);
+            E::mma(acc[1], afr, bfr[0], bfr[1]);
           }
+        }
+        // this lane: query heads mt*8 + g4, pages j0 + 2*t4 and j0 + 2*t4 + 1
+        for (int mt = 0; mt < mtiles; ++mt) {
+          const int g = mt * 8 + g4;
+          if (g >= a.G) continue;
+          float* out = a.scores + (int64_t(hd.b) * a.H_q + int64_t(head) * a.G + g) * a.max_pages + hd.p0;
 #pragma unroll
-          for (int o = LPP / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
-          if (l == 0 && j < hd.count) out[int64_t(g) * a.max_pages + j] = here ? acc : __int_as_float(0x7fc00000);
+          for (int e = 0; e < 2; ++e) {
+            const int j = j0 + 2 * t4 + e;
+            if (j < hd.count)
+              out[j] = ((hd.valid >> j) & 1u) ? acc[mt][e] + acc[mt][2 + e] : __int_as_float(0x7fc00000);
+          }
         }
       }
       __syncwarp();
@@ -337,7 +353,7 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
       const bool here = j < hd.count && ((hd.valid >> j) & 1u);
       float acc = 0.f;
       if (here) {
-        const uint8_t* pg = st + ph * TL::kPageBytes + l * 16;
+        const uint8_t* pg = st + ph * TL::kPageStride + l * 16;
         const uint4 vmn = *reinterpret_cast<const uint4*>(pg);
         const uint4 vmx = *reinterpret_cast<const uint4*>(pg + D * 2);
         const uint4 vme = *reinterpret_cast<const uint4*>(pg + 2 * D * 2);
