@@ -406,6 +406,65 @@ def h2o_evict(hh, positions, budget: int, n_sink: int, grace: int):
     return np.asarray(R, dtype=np.int64), np.asarray(s), evicted
 
 
+def h2o_proxy_token(keys, positions, hh, k_new, pos_new: int, *, decay: float, budget: int,
+                    n_sink: int, grace: int, scale: float, store: bool = True):
+    """One incoming token of the H2O cache, its own key standing in for the query.
+
+    [velox] "How it works", for every incoming token (prefill and decode), per
+    head: 1. the new key attends to every stored key, attn = softmax(K k / sqrt(D))
+    (here the given scale); 2. scores = scores * decay + attn; new tokens start
+    at 0; 3. above budget the minimum-score entry outside the first n_sink and
+    the last grace (the newest) is removed, the first index winning a tie;
+    4. at most budget entries remain. With store, scores are held in bf16, the
+    fold rounded once as in the decode-side update (a reading: [vortex] point 3).
+
+    keys: float64 [n, D] (list order = ascending positions); returns
+    (keys, positions, hh, evicted position or None).
+    """
+    keys = np.asarray(keys, np.float64).reshape(-1, np.asarray(k_new).shape[-1])
+    positions = np.asarray(positions, np.int64)
+    hh = np.asarray(hh, np.float64)
+    if len(positions):
+        z = keys @ np.asarray(k_new, np.float64) * scale
+        p = np.exp(z - z.max())
+        p /= p.sum()
+        hh = decay * hh + p
+        if store:
+            hh = h2o_store(hh)
+    keys = np.vstack([keys, np.asarray(k_new, np.float64)[None, :]])
+    positions = np.append(positions, pos_new)
+    hh = np.append(hh, 0.0)
+    ev = None
+    if len(positions) > budget:
+        lo, hi = n_sink, len(positions) - grace
+        if hi <= lo:
+            raise ValueError("no evictable entry: budget must exceed n_sink + grace")
+        j = lo + int(np.argmin(hh[lo:hi]))
+        ev = int(positions[j])
+        keys = np.delete(keys, j, axis=0)
+        positions = np.delete(positions, j)
+        hh = np.delete(hh, j)
+    return keys, positions, hh, ev
+
+
+def h2o_proxy_prefill(keys_in, pos_in, *, decay: float, budget: int, n_sink: int, grace: int,
+                      scale: float, state=None, store: bool = True):
+    """h2o_proxy_token over incoming tokens in order (a prefill chunk, or the
+    decode tokens), from an optional (keys, positions, hh) state. [velox]
+    "How it works" and the below-budget batched absorb of its changelog, which
+    it states gives the same scores as this token-by-token loop.
+    Returns (keys, positions, hh, evicted positions in order)."""
+    D = np.asarray(keys_in).shape[-1]
+    keys, pos, hh = state if state is not None else (np.zeros((0, D)), np.zeros(0, np.int64), np.zeros(0))
+    evicted = []
+    for k, p in zip(np.asarray(keys_in, np.float64), pos_in):
+        keys, pos, hh, ev = h2o_proxy_token(keys, pos, hh, k, int(p), decay=decay, budget=budget,
+                                            n_sink=n_sink, grace=grace, scale=scale, store=store)
+        if ev is not None:
+            evicted.append(ev)
+    return keys, pos, hh, evicted
+
+
 def h2o_unit_step(hh_ret, positions, k_head_bits, v_head_bits, q_group_bits, *,
                   dtype: str, decay: float, budget: int, n_sink: int, grace: int,
                   scale: float = 0.0, window_softmax: bool = False):

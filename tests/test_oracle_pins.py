@@ -579,3 +579,59 @@ def test_h2o_unit_step_mass_without_eviction():
         hh_exact = O.h2o_fold(hh_exact, r["logits"], r["lse"], decay)
     closed = (1 - decay ** T) / (1 - decay)
     assert abs(hh_exact.sum() - closed) < 1e-9
+
+
+# ---------------------------------------------------------------------------
+# N2 H2O with the key as the query (prefill-side absorb and eviction)
+# ---------------------------------------------------------------------------
+def _batched_absorb(K, decay, scale):
+    """The below-budget absorb as one masked matrix product: token i's key
+    attends to keys 0..i-1, rows weighted by decay^(T-1-i) and summed."""
+    T = K.shape[0]
+    Z = (K @ K.T) * scale
+    Z[np.triu_indices(T)] = -np.inf                # j >= i is not stored yet
+    P = np.zeros_like(Z)
+    for i in range(1, T):
+        z = Z[i, :i]
+        e = np.exp(z - z.max())
+        P[i, :i] = e / e.sum()
+    w = decay ** (T - 1 - np.arange(T))
+    return (w[:, None] * P).sum(axis=0)
+
+
+def test_proxy_absorb_equals_batched_matrix_form():
+    rng = np.random.default_rng(31)
+    for decay in (1.0, 0.98, 0.5):
+        K = rng.standard_normal((40, 16))
+        _, pos, hh, ev = O.h2o_proxy_prefill(K, np.arange(40), decay=decay, budget=100, n_sink=4,
+                                             grace=8, scale=0.25, store=False)
+        assert ev == [] and pos.tolist() == list(range(40))
+        assert np.allclose(hh, _batched_absorb(K, decay, 0.25), rtol=1e-12, atol=1e-14)
+
+
+def test_proxy_mass_closed_form():
+    rng = np.random.default_rng(32)
+    T, decay = 60, 0.9
+    _, _, hh, _ = O.h2o_proxy_prefill(rng.standard_normal((T, 8)), np.arange(T), decay=decay,
+                                      budget=1000, n_sink=0, grace=0, scale=1.0, store=False)
+    assert abs(hh.sum() - (1 - decay ** (T - 1)) / (1 - decay)) < 1e-12
+
+
+def test_proxy_eviction_invariants_and_ties():
+    rng = np.random.default_rng(33)
+    budget, n_sink, grace = 12, 2, 3
+    keys, pos, hh = np.zeros((0, 8)), np.zeros(0, np.int64), np.zeros(0)
+    for t in range(80):
+        k = rng.standard_normal(8) if t % 7 else np.zeros(8)      # some all-equal attention rows
+        before = pos.copy()
+        keys, pos, hh, ev = O.h2o_proxy_token(keys, pos, hh, k, t, decay=0.984375, budget=budget,
+                                              n_sink=n_sink, grace=grace, scale=0.5)
+        assert len(pos) == min(t + 1, budget)
+        assert np.all(np.diff(pos) > 0)
+        assert pos[:n_sink].tolist() == list(range(min(n_sink, t + 1)))
+        assert pos[-grace:].tolist() == list(range(max(0, t + 1 - grace), t + 1))
+        if ev is not None:
+            # the evicted entry had the minimum stored score among the eligible, lowest position first
+            full = np.append(before, t)
+            assert ev in full[n_sink:len(full) - grace]
+        assert np.all(hh >= 0)
