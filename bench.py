@@ -476,6 +476,56 @@ def run_gpu(args, rank, world):
                 step_ms_median=statistics.median(step_ms), max_median_ms=max_median_ms)
 
 
+def run_h2o_prefill(args):
+    """The prefill-side H2O (each key as its own query) of the token-level
+    workload's whole prefill: sa_h2o_prefill timed alone, the pool already
+    holding the prefill's keys, the retained lists emptied before each rep."""
+    import numpy as np
+    import torch
+    from sa_synth import config, make_workload
+    from sparse_paged_kv_page_gb300.step import SparseDecoder
+    import sparse_paged_kv_page_gb300 as S
+    dev = torch.device("cuda", 0)
+    c = config(4).replace(decode_steps=0)
+    wl = make_workload(c)
+    dec = SparseDecoder(batch=c.B, num_q_heads=c.H_q, num_kv_heads=c.H_kv, head_dim=c.D, page_size=1,
+                        num_blocks=wl.num_blocks, bt_stride=wl.max_pages, budget=c.budget,
+                        n_sink=c.n_sink, grace=c.grace, decay=c.decay, scale=c.scale,
+                        ret_cap=int(wl.prefill_lens.max()) + 4, device=dev)
+    dec.set_block_table(torch.from_numpy(wl.block_table))
+    kv = torch.from_numpy(np.ascontiguousarray(wl.k_pre).view(np.int16)).to(dev).view(torch.bfloat16)
+    vv = torch.from_numpy(np.ascontiguousarray(wl.v_pre).view(np.int16)).to(dev).view(torch.bfloat16)
+    cu = torch.from_numpy(wl.pre_cu.astype(np.int32)).to(dev)
+    S.sa_append_kv(dec.cache.struct, dec.batch, kv, vv, cu, int(wl.prefill_lens.max()), hh=dec.cache.hh,
+                   dev_status=dec.dev_status)
+    torch.cuda.synchronize()
+    times = []
+    for i in range(args.warmup + max(1, args.steps)):
+        dec.ret_cnt.zero_()
+        dec.cache.hh.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        S.sa_h2o_prefill(dec.cache.struct, dec.batch, cu, dec.cache.hh, dec.cache.hh.shape[0],
+                         dec.ret_pos, dec.ret_cnt, dec.ret_cap, c.budget, c.n_sink, c.grace, c.decay,
+                         c.scale, dev_status=dec.dev_status)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(a.elapsed_time(b))
+    ms = statistics.mean(times)
+    toks = int(wl.prefill_lens.sum())
+    assert int(dec.dev_status.item()) == 0
+    assert bool((dec.ret_cnt == c.budget).all())
+    print(json.dumps({"metric": "prefill-side H2O absorb + eviction (key as query), tokens/s",
+                      "value": toks / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+                      "steps": len(times), "warmup": args.warmup, "ms_per_step": ms,
+                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                      "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": describe(c) + f", {toks} prefill tokens per call",
+                                 "timing": "CUDA events around each sa_h2o_prefill call"},
+                      "gpu_launches": len(times)}))
+
+
 def describe(c):
     base = f"{c.name}: B={c.B}, H_q={c.H_q}, H_kv={c.H_kv}, D={c.D}, page_size={c.ps}, {c.dtype}"
     if c.ps == 1:
@@ -497,6 +547,8 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=2)
     ap.add_argument("--workers", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--h2o-prefill", action="store_true",
+                    help="time the prefill-side H2O absorb / eviction of the token-level workload")
     ap.add_argument("--per-query-head", action="store_true",
                     help="select pages per query head (score, select, attend one row per query head)")
     args = ap.parse_args()
@@ -539,6 +591,10 @@ def main():
         return
 
     import torch
+    if args.h2o_prefill:
+        if rank == 0:
+            run_h2o_prefill(args)
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl")
     res = run_gpu(args, rank, world)

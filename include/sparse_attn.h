@@ -18,6 +18,8 @@
  *                     trailing pages / tokens
  *   sa_score_pages_qh, sa_sparse_decode_qh
  *                     scores, selection and attention per query head
+ *   sa_h2o_prefill    H2O absorb / eviction of appended tokens with the new key
+ *                     as the query (prefill side)
  *
  * Sources (cited by page title and section):
  *   [vortex]  "flow: add H2O sparse attention (page-level and token-level,
@@ -399,6 +401,36 @@ sa_status sa_h2o_update_window(const sa_batch* batch, int32_t num_kv_heads, int3
                                int32_t ret_cap, int32_t budget, int32_t n_sink, int32_t grace,
                                float decay, int32_t* evicted, int32_t* evicted_cnt,
                                int32_t* dev_status, void* stream);
+
+/*
+ * sa_h2o_prefill -- H2O absorb and eviction for newly appended tokens, each
+ * token's own key standing in for its query (page_size 1, bf16 pool).
+ *
+ * [velox] "How it works": for every incoming token, per head, the new key k
+ * attends to every stored key, attn = softmax(K k * scale); stored scores
+ * become scores * decay + attn; the new token starts at 0; while more than
+ * budget entries remain, the lowest (score, position) entry outside the first
+ * n_sink and the newest grace list entries is removed. The batched absorb of
+ * velox's changelog is the same arithmetic as this token-by-token loop.
+ * Request b's new tokens are positions seq_lens[b] - n_b .. seq_lens[b] - 1
+ * with n_b = new_cu[b+1] - new_cu[b] (already written by sa_append_kv, without
+ * retained lists); they are processed in order against the retained list
+ * (ret_pos / ret_cnt, at most budget entries, every position below them).
+ * Scores: bf16 in hh [num_slots, num_kv_heads] (slot = block of the position),
+ * each fold decay * hh + attn one float64 fma rounded once; attn in float32.
+ *   scale      <= 0 selects head_dim ** -0.5
+ *   evicted    nullable int32 [batch, num_kv_heads, evicted_cap]: positions
+ *              evicted, in eviction order; evicted_cnt [batch, num_kv_heads]
+ * Limits: budget + 1 <= 1024 and the retained keys of a (request, KV head)
+ * fit in shared memory (budget <= 700 at head_dim 128), else
+ * SA_ERR_UNSUPPORTED. One CTA per (request, KV head) holds its keys on chip
+ * for the whole call.
+ */
+sa_status sa_h2o_prefill(const sa_cache* cache, const sa_batch* batch, const int32_t* new_cu,
+                         void* hh, int32_t num_slots, int32_t* ret_pos, int32_t* ret_cnt,
+                         int32_t ret_cap, int32_t budget, int32_t n_sink, int32_t grace,
+                         float decay, float scale, int32_t* evicted, int32_t* evicted_cnt,
+                         int32_t evicted_cap, int32_t* dev_status, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* sa_status_string(sa_status status);

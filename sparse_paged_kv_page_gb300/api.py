@@ -20,7 +20,7 @@ __all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKV
            "sa_decode_workspace_init", "sa_sparse_decode", "sa_sparse_decode_noalloc",
            "sa_sparse_decode_noalloc_capacity", "sa_h2o_update", "sa_decode_step",
            "sa_select_topk_reserved", "sa_h2o_update_window", "sa_score_pages_qh",
-           "sa_sparse_decode_qh",
+           "sa_sparse_decode_qh", "sa_h2o_prefill",
            "sa_status_string",
            "sa_version", "alloc_decode_workspace"]
 
@@ -268,4 +268,20 @@ def sa_decode_step(cache: SaCache, batch: SaBatch, k_new, v_new, new_cu, max_new
         int(max_pages), int(topk), int(n_bos), int(n_eos), _p(sel_idx, torch.int32, "sel_idx"),
         _p(sel_cnt, torch.int32, "sel_cnt"), float(scale), _p(out, name="out"),
         _p(lse, torch.float32, "lse"), _p(workspace, name="workspace"), wbytes,
+        _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_h2o_prefill(cache: SaCache, batch: SaBatch, new_cu, hh, num_slots: int, ret_pos, ret_cnt,
+                   ret_cap: int, budget: int, n_sink: int, grace: int, decay: float,
+                   scale: float = 0.0, evicted=None, evicted_cnt=None, dev_status=None,
+                   stream=None):
+    """H2O absorb / eviction of the tokens just appended, each new key as the query."""
+    lib = _lib.load()
+    ev_cap = 0 if evicted is None else evicted.shape[-1]
+    _check("sa_h2o_prefill", lib.sa_h2o_prefill(
+        ctypes.byref(cache), ctypes.byref(batch), _p(new_cu, torch.int32, "new_cu"),
+        _p(hh, torch.bfloat16, "hh"), int(num_slots), _p(ret_pos, torch.int32, "ret_pos"),
+        _p(ret_cnt, torch.int32, "ret_cnt"), int(ret_cap), int(budget), int(n_sink), int(grace),
+        float(decay), float(scale), _p(evicted, torch.int32, "evicted"),
+        _p(evicted_cnt, torch.int32, "evicted_cnt"), int(ev_cap),
         _p(dev_status, torch.int32, "dev_status"), _s(stream)))

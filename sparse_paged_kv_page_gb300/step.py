@@ -19,7 +19,8 @@ from typing import Optional, Sequence
 import torch
 
 from .api import (PagedKVCache, alloc_decode_workspace, make_batch, sa_append_kv,
-                  sa_decode_step, sa_h2o_update, sa_h2o_update_window, sa_score_pages,
+                  sa_decode_step, sa_h2o_prefill, sa_h2o_update, sa_h2o_update_window,
+                  sa_score_pages,
                   sa_score_pages_qh, sa_select_topk_reserved, sa_sparse_decode,
                   sa_sparse_decode_qh)
 
@@ -30,7 +31,7 @@ class SparseDecoder:
                  topk: int = 0, w_avg: float = 1.0, w_peak: float = 0.25, scale: float = 0.0,
                  budget: int = 0, n_sink: int = 0, grace: int = 0, decay: float = 1.0,
                  ret_cap: int = 0, n_bos: int = 0, n_eos: int = 1, window_softmax: bool = False,
-                 per_query_head: bool = False, device="cuda"):
+                 per_query_head: bool = False, proxy_prefill: bool = False, device="cuda"):
         self.B, self.H_q, self.H_kv, self.D = batch, num_q_heads, num_kv_heads, head_dim
         self.ps, self.dtype, self.device = page_size, dtype, torch.device(device)
         self.token_level = page_size == 1 and ret_cap > 0
@@ -39,6 +40,8 @@ class SparseDecoder:
         self.n_bos, self.n_eos, self.window_softmax = n_bos, n_eos, window_softmax
         # per-query-head selection: score, select and attend one row per query head
         self.qh = per_query_head and not self.token_level
+        # token level: trim a prefill H2O-style as it arrives (each key as its own query)
+        self.proxy_prefill = proxy_prefill and self.token_level
         rows = num_q_heads if self.qh else num_kv_heads
         self.cache = PagedKVCache(num_blocks, num_kv_heads, page_size, head_dim, dtype, device,
                                   with_meta=not self.token_level, with_hh=self.token_level)
@@ -82,12 +85,23 @@ class SparseDecoder:
         self.block_table.copy_(bt.to(device=self.device, dtype=torch.int32))
 
     def prefill(self, k: torch.Tensor, v: torch.Tensor, lens: Sequence[int]):
-        """Append lens[b] tokens per request: k, v [sum(lens), H_kv, D] in request order."""
+        """Append lens[b] tokens per request: k, v [sum(lens), H_kv, D] in request order.
+        With proxy_prefill the retained lists take the tokens through the
+        key-as-query absorb and eviction instead of all at once."""
         cu = [0]
         for n in lens:
             cu.append(cu[-1] + int(n))
         new_cu = torch.tensor(cu, dtype=torch.int32, device=self.device)
-        self._append(k, v, new_cu, max(int(n) for n in lens))
+        mx = max(int(n) for n in lens)
+        if self.proxy_prefill:
+            sa_append_kv(self.cache.struct, self.batch, k, v, new_cu, mx, hh=self.cache.hh,
+                         dev_status=self.dev_status)
+            sa_h2o_prefill(self.cache.struct, self.batch, new_cu, self.cache.hh,
+                           self.cache.hh.shape[0], self.ret_pos, self.ret_cnt, self.ret_cap,
+                           self.budget, self.n_sink, self.grace, self.decay, self.scale,
+                           dev_status=self.dev_status)
+        else:
+            self._append(k, v, new_cu, mx)
 
     def _append(self, k, v, new_cu, max_new):
         if self.token_level:
