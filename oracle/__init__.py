@@ -4,4 +4,5 @@ from .oracle import (decode_kdt, round_to_kdt, encode_kdt, ulp_kdt, num_pages, p
                      gather_rows, page_stats, cache_meta, head_meta, score_pages, select_pages,
                      select_pages_reserved, default_scale, attention, selected_positions,
                      merge_partials, page_decode_unit, h2o_fold, h2o_fold_window, h2o_store,
-                     h2o_evict, h2o_unit_step, h2o_proxy_token, h2o_proxy_prefill)
+                     h2o_evict, h2o_unit_step, h2o_proxy_token, h2o_proxy_prefill, entmax_threshold, entmax,
+                     attention_entmax)

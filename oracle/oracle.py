@@ -253,6 +253,71 @@ def select_pages_reserved(scores, n_pages: int, topk: int, n_bos: int, n_eos: in
 
 
 # ---------------------------------------------------------------------------
+# N3: alpha-entmax in place of the softmax over the selected tokens
+# ---------------------------------------------------------------------------
+def entmax_threshold(z, alpha: float) -> float:
+    """tau of alpha-entmax: p_i = [(alpha-1) z_i - tau]_+ ** (1/(alpha-1)), sum p = 1.
+
+    [entmax] "How it works" and "Quick start" (alpha = 1.5 by default, 1.5 and
+    2 decoded exactly). With a = (alpha - 1) z sorted descending and a support
+    of the k largest, sum_{i<=k} (a_i - tau)^(1/(alpha-1)) = 1 fixes tau:
+      alpha = 2:   tau = (sum_{i<=k} a_i - 1) / k
+      alpha = 1.5: k tau^2 - 2 tau S1 + S2 - 1 = 0, the root below a_k,
+    and the support is the largest k whose tau stays below a_k. Other alpha
+    by bisection on the monotone sum. -inf entries never enter the support.
+    """
+    a = np.sort((alpha - 1.0) * np.asarray(z, np.float64)[np.isfinite(z)])[::-1]
+    if a.size == 0:
+        raise ValueError("no finite logits")
+    if alpha == 2.0 or alpha == 1.5:
+        S1 = np.cumsum(a)
+        S2 = np.cumsum(a * a)
+        k = np.arange(1, a.size + 1)
+        if alpha == 2.0:
+            tau = (S1 - 1.0) / k
+        else:
+            disc = np.maximum(S1 * S1 - k * (S2 - 1.0), 0.0)
+            tau = (S1 - np.sqrt(disc)) / k
+        ok = tau < a                                  # every member of the support stays positive
+        kk = int(np.nonzero(ok)[0].max())             # largest such k (k = 1 always qualifies)
+        return float(tau[kk])
+    r = 1.0 / (alpha - 1.0)
+    lo, hi = a[0] - 1.0, a[0]
+    for _ in range(200):
+        mid = 0.5 * (lo + hi)
+        if (np.maximum(a - mid, 0.0) ** r).sum() >= 1.0:
+            lo = mid
+        else:
+            hi = mid
+    return 0.5 * (lo + hi)
+
+
+def entmax(z, alpha: float) -> np.ndarray:
+    """alpha-entmax probabilities of logits z (see entmax_threshold)."""
+    z = np.asarray(z, np.float64)
+    tau = entmax_threshold(z, alpha)
+    p = np.where(np.isfinite(z), np.maximum((alpha - 1.0) * z - tau, 0.0), 0.0)
+    return p ** (1.0 / (alpha - 1.0))
+
+
+def attention_entmax(q, k, v, scale: float, alpha: float):
+    """Attention with alpha-entmax in place of the softmax: for each query row,
+    o = sum_j entmax(scale q.k_j)_j v_j. Returns (o [G, D], tau [G], z [G, T])."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    z = (q @ k.T) * scale
+    o = np.zeros((q.shape[0], v.shape[1]))
+    tau = np.full(q.shape[0], np.nan)
+    for g in range(q.shape[0]):
+        if z.shape[1] == 0:
+            continue
+        tau[g] = entmax_threshold(z[g], alpha)
+        o[g] = entmax(z[g], alpha) @ v
+    return o, tau, z
+
+
+# ---------------------------------------------------------------------------
 # A4: attention over the selected tokens, and the LSE merge
 # ---------------------------------------------------------------------------
 def default_scale(D: int) -> float:

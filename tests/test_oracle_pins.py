@@ -635,3 +635,55 @@ def test_proxy_eviction_invariants_and_ties():
             full = np.append(before, t)
             assert ev in full[n_sink:len(full) - grace]
         assert np.all(hh >= 0)
+
+
+# ---------------------------------------------------------------------------
+# N3 alpha-entmax
+# ---------------------------------------------------------------------------
+def test_sparsemax_worked_example():
+    # sorted [1, 0.5, -1]: k = 2 (1 + 2 * 0.5 > 1.5, 1 + 3 * (-1) < 0.5), tau = (1.5 - 1) / 2
+    p = O.entmax(np.array([0.5, -1.0, 1.0]), 2.0)
+    assert np.allclose(p, [0.25, 0.0, 0.75], atol=1e-15)
+
+
+def test_entmax15_two_way_closed_form():
+    # a = z/2; for two entries in the support, (a1-t)^2 + (a2-t)^2 = 1
+    for gap in (0.0, 0.3, 1.0):
+        z = np.array([0.0, -gap])
+        p = O.entmax(z, 1.5)
+        a1, a2 = 0.0, -gap / 2
+        t = ((a1 + a2) - np.sqrt((a1 + a2) ** 2 - 2 * (a1 * a1 + a2 * a2 - 1))) / 2
+        assert np.allclose(p, [(a1 - t) ** 2, (a2 - t) ** 2], atol=1e-14)
+    assert np.allclose(O.entmax(np.array([0.0, -3.0]), 1.5), [1.0, 0.0])   # gap past the support
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_entmax_sort_form_equals_bisection_and_sums_to_one(alpha):
+    rng = np.random.default_rng(int(alpha * 10))
+    r = 1.0 / (alpha - 1.0)
+    for _ in range(50):
+        z = rng.standard_normal(int(rng.integers(1, 300))) * rng.choice([0.1, 1.0, 5.0])
+        tau = O.entmax_threshold(z, alpha)
+        # bisection on the monotone sum, written independently of the sort form
+        a = (alpha - 1) * z
+        lo, hi = a.max() - 1, a.max()
+        for _ in range(200):
+            mid = (lo + hi) / 2
+            if (np.maximum(a - mid, 0) ** r).sum() >= 1:
+                lo = mid
+            else:
+                hi = mid
+        assert abs(tau - (lo + hi) / 2) < 1e-12
+        assert abs(O.entmax(z, alpha).sum() - 1.0) < 1e-12
+
+
+def test_entmax_special_cases():
+    for alpha in (1.5, 2.0):
+        assert np.allclose(O.entmax(np.zeros(7), alpha), np.full(7, 1 / 7))      # equal logits: uniform
+        assert np.allclose(O.entmax(np.array([10.0, 0.0, -1.0]), alpha), [1, 0, 0])
+        p = O.entmax(np.array([1.0, -np.inf, 0.9]), alpha)                      # -inf never enters
+        assert p[1] == 0 and abs(p.sum() - 1) < 1e-12
+    # alpha -> 1 approaches the softmax (bisection path)
+    z = np.array([0.3, -0.2, 1.1, 0.0])
+    sm = np.exp(z - z.max()); sm /= sm.sum()
+    assert np.allclose(O.entmax(z, 1.001), sm, atol=5e-3)
