@@ -20,6 +20,8 @@
  *                     scores, selection and attention per query head
  *   sa_h2o_prefill    H2O absorb / eviction of appended tokens with the new key
  *                     as the query (prefill side)
+ *   sa_sparse_decode_entmax, sa_entmax_workspace_size
+ *                     attention over the selection with alpha-entmax
  *
  * Sources (cited by page title and section):
  *   [vortex]  "flow: add H2O sparse attention (page-level and token-level,
@@ -257,7 +259,8 @@ sa_status sa_decode_workspace_init(void* workspace, size_t workspace_bytes, void
  *   logits     nullable float32 [batch, num_q_heads, logits_stride]: the scaled
  *              logit scale * q . k of selection token i = e * page_size + slot
  *              (entry e, slot within the page); -inf for slots past the page's
- *              fill; logits_stride >= sel_stride * page_size
+ *              fill and for entries skipped as invalid; logits_stride >=
+ *              sel_stride * page_size
  *   workspace  see sa_decode_workspace_size
  * Only the valid tokens of each selected page are read (the tail page's stale
  * slots are zero-filled in shared memory, never loaded). Tensor cores
@@ -288,6 +291,49 @@ sa_status sa_sparse_decode_qh(const sa_cache* cache, const sa_batch* batch, cons
                               int32_t sel_stride, float scale, void* out, float* lse,
                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
                               void* stream);
+
+/*
+ * sa_entmax_workspace_size -- bytes of workspace sa_sparse_decode_entmax
+ * needs for these sizes (host function; reads the device's SM count). The
+ * workspace holds the logits (when the caller passes none), the thresholds
+ * and the per-split partial sums; it needs no initialisation. Calls that share
+ * a workspace must be ordered on one stream.
+ */
+size_t sa_entmax_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads,
+                                int32_t head_dim, int32_t page_size, int32_t sel_stride);
+
+/*
+ * sa_sparse_decode_entmax -- attention over the selected pages with
+ * alpha-entmax in place of the softmax.
+ *
+ * [entmax] "How it works" and "Quick start": the selection of sa_select_topk
+ * is attended exactly, normalised by alpha-entmax (the pages' default
+ * alpha = 1.5; alpha = 2 is sparsemax). With z_j = scale * q . k_j over the
+ * valid tokens of the selection and a_j = (alpha - 1) z_j,
+ *   p_j = max(a_j - tau, 0) ^ (1 / (alpha - 1)),  sum_j p_j = 1,
+ *   o   = sum_j p_j v_j.
+ * tau is exact for alpha = 1.5 and 2 (the closed form on the support, the
+ * support being the largest set whose threshold stays below its smallest
+ * member) and found by Newton's method to float64 precision otherwise.
+ *   q, sel_idx, sel_cnt, sel_stride, scale, out   as sa_sparse_decode
+ *   alpha      1 < alpha <= 2, else SA_ERR_INVALID_ARG
+ *   tau        nullable float32 [batch, num_q_heads]: the threshold in units
+ *              of a; NaN for a head with no valid token (its output is 0)
+ *   logits     nullable float32 [batch, num_q_heads, logits_stride], as
+ *              sa_sparse_decode's (logits_stride >= sel_stride * page_size)
+ *   workspace  sa_entmax_workspace_size(...) bytes, else SA_ERR_WORKSPACE
+ * The output is divided by the float32 sum of the p_j it used (1 up to the
+ * rounding of tau). K of every selected token is read once; V only for the
+ * tokens some query head of the group keeps. Limits: num_q_heads / num_kv_heads
+ * <= 16 and sel_stride * page_size <= 40960, else SA_ERR_UNSUPPORTED. Data
+ * errors as sa_sparse_decode.
+ */
+sa_status sa_sparse_decode_entmax(const sa_cache* cache, const sa_batch* batch, const void* q,
+                                  int32_t num_q_heads, const int32_t* sel_idx,
+                                  const int32_t* sel_cnt, int32_t sel_stride, float alpha,
+                                  float scale, void* out, float* tau, float* logits,
+                                  int32_t logits_stride, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, void* stream);
 
 /*
  * sa_sparse_decode_noalloc -- sa_sparse_decode without a caller workspace.

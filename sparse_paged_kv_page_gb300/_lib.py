@@ -65,6 +65,10 @@ SIGNATURES = {
                                     c_ptr, c_ptr, c_ptr, c_size, c_ptr, c_ptr]),
     "sa_h2o_prefill": (c_i32, [P_CACHE, P_BATCH, c_ptr, c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_i32,
                                c_i32, c_i32, c_f32, c_f32, c_ptr, c_ptr, c_i32, c_ptr, c_ptr]),
+    "sa_entmax_workspace_size": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "sa_sparse_decode_entmax": (c_i32, [P_CACHE, P_BATCH, c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_f32,
+                                        c_f32, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_size, c_ptr,
+                                        c_ptr]),
     "sa_status_string": (ctypes.c_char_p, [c_i32]),
     "sa_version": (ctypes.c_char_p, []),
 }

@@ -20,7 +20,8 @@ __all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKV
            "sa_decode_workspace_init", "sa_sparse_decode", "sa_sparse_decode_noalloc",
            "sa_sparse_decode_noalloc_capacity", "sa_h2o_update", "sa_decode_step",
            "sa_select_topk_reserved", "sa_h2o_update_window", "sa_score_pages_qh",
-           "sa_sparse_decode_qh", "sa_h2o_prefill",
+           "sa_sparse_decode_qh", "sa_h2o_prefill", "sa_entmax_workspace_size",
+           "alloc_entmax_workspace", "sa_sparse_decode_entmax",
            "sa_status_string",
            "sa_version", "alloc_decode_workspace"]
 
@@ -198,6 +199,34 @@ def sa_sparse_decode(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_id
         ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads),
         _p(sel_idx, torch.int32, "sel_idx"), _p(sel_cnt, torch.int32, "sel_cnt"), int(sel_stride),
         float(scale), _p(out, name="out"), _p(lse, torch.float32, "lse"),
+        _p(logits, torch.float32, "logits"), int(logits_stride), _p(workspace, name="workspace"),
+        wbytes, _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_entmax_workspace_size(batch: int, num_kv_heads: int, num_q_heads: int, head_dim: int,
+                             page_size: int, sel_stride: int) -> int:
+    return int(_lib.load().sa_entmax_workspace_size(int(batch), int(num_kv_heads), int(num_q_heads),
+                                                    int(head_dim), int(page_size), int(sel_stride)))
+
+
+def alloc_entmax_workspace(batch, num_kv_heads, num_q_heads, head_dim, page_size, sel_stride,
+                           device="cuda"):
+    """A workspace tensor of the size sa_sparse_decode_entmax needs."""
+    n = max(256, sa_entmax_workspace_size(batch, num_kv_heads, num_q_heads, head_dim, page_size,
+                                          sel_stride))
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def sa_sparse_decode_entmax(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_idx, sel_cnt,
+                            sel_stride: int, alpha: float, scale: float, out, tau=None, logits=None,
+                            logits_stride: int = 0, workspace=None, dev_status=None, stream=None):
+    """Attention over the selection with alpha-entmax (1 < alpha <= 2) in place of the softmax."""
+    lib = _lib.load()
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("sa_sparse_decode_entmax", lib.sa_sparse_decode_entmax(
+        ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads),
+        _p(sel_idx, torch.int32, "sel_idx"), _p(sel_cnt, torch.int32, "sel_cnt"), int(sel_stride),
+        float(alpha), float(scale), _p(out, name="out"), _p(tau, torch.float32, "tau"),
         _p(logits, torch.float32, "logits"), int(logits_stride), _p(workspace, name="workspace"),
         wbytes, _p(dev_status, torch.int32, "dev_status"), _s(stream)))
 

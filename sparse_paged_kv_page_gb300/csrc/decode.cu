@@ -72,6 +72,7 @@ struct DecodeArgs {
   int32_t* status;
   int H_kv, H_q, G, ps, ps_shift, num_blocks, bt_stride, sel_stride, logits_stride, nsplit;
   int H_u, kv_div;  // selection units per request (H_kv, or H_q per query head) and per KV head
+  int logits_only;  // write the scaled logits and stop: V is neither read nor used
   int ent_max;      // entries of the selection one CTA can touch
   float scale, scale_log2;
 };
@@ -233,12 +234,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         s_mask[warp][st] = vmask;
         const uint32_t bar = smem_u32(&s_bar[warp][st]);
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, vmask ? uint32_t(2 * TL::kBytes) : 0u);
+        const int nbuf = a.logits_only ? 1 : 2;
+        mbar_arrive_expect_tx(bar, vmask ? uint32_t(nbuf * TL::kBytes) : 0u);
         if (vmask) {
 #pragma unroll
           for (int hf = 0; hf < TL::kHalves; ++hf) {
             tma_load_2d(sk + hf * 2048, &tmk, hf * 64, y, bar);
-            tma_load_2d(sv + hf * 2048, &tmv, hf * 64, y, bar);
+            if (!a.logits_only) tma_load_2d(sv + hf * 2048, &tmv, hf * 64, y, bar);
           }
         }
       }
@@ -270,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const bool rv = (vmask >> row) & 1u;
         const uint32_t d = swz<D>(row, chunk);
         cp_async_16(sk + d, rv ? static_cast<const void*>(kbase + ro + chunk * 8) : a.k, rv ? 16 : 0);
-        cp_async_16(sv + d, rv ? static_cast<const void*>(vbase + ro + chunk * 8) : a.v, rv ? 16 : 0);
+        if (!a.logits_only)
+          cp_async_16(sv + d, rv ? static_cast<const void*>(vbase + ro + chunk * 8) : a.v, rv ? 16 : 0);
       }
     }
   };
@@ -297,8 +300,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const uint32_t sk = smem_u32(wbuf + st * TL::kStageBytes);
     const uint32_t sv = sk + TL::kBytes;
     const uint32_t vmask = s_mask[warp][st];
-    if (vmask == 0) continue;
-    if (kTma && vmask != 0xffffu) {
+    if (vmask == 0) {
+      if (a.logits) {                                          // no valid token in the tile
+        const int j = (t << 4) + (lane & 15);
+        if (j < n_rows)
+          for (int gg = lane >> 4; gg < G; gg += 2)
+            a.logits[(int64_t(b) * a.H_q + int64_t(h) * G + gg) * a.logits_stride + j] = -INFINITY;
+      }
+      continue;
+    }
+    if (kTma && vmask != 0xffffu && !a.logits_only) {
       // a partial page: its stale V rows could hold anything (NaN) -- zero them
       for (int idx = lane; idx < 16 * TL::kChunks; idx += 32) {
         const int row = idx / TL::kChunks, chunk = idx % TL::kChunks;
@@ -350,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         pmax[1] = fmaxf(pmax[1], c[nt2][2 + e]);
       }
     }
+    if (a.logits_only) continue;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       pmax[r] = fmaxf(pmax[r], __shfl_xor_sync(kFull, pmax[r], 1));
@@ -396,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   } else {
     cp_async_wait<0>();
   }
+  if (a.logits_only) return;                                   // (uniform across the CTA)
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     l_r[r] += __shfl_xor_sync(kFull, l_r[r], 1);
@@ -695,7 +708,7 @@ sa_status launch_merge_mode(const DecodeArgs& a, dim3 grid, cudaStream_t s, cons
         launch_decode<T, D, kTma, true>(a, grid, s, mk, mv, g_dec_smem[4 * slot + 2 + kTma], pdl);
     if (st != SA_ERR_UNSUPPORTED) return st;
   }
-  if (a.nsplit > 1 && !a.tickets) return SA_ERR_WORKSPACE;
+  if (a.nsplit > 1 && !a.tickets && !a.logits_only) return SA_ERR_WORKSPACE;
   return launch_decode<T, D, kTma, false>(a, grid, s, mk, mv, g_dec_smem[4 * slot + kTma], pdl);
 }
 
@@ -716,7 +729,7 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
                       const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_stride, float scale,
                       void* out, float* lse, float* logits, int32_t logits_stride, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, void* stream, bool allow_cluster,
-                      bool pdl, bool per_query_head) {
+                      bool pdl, bool per_query_head, bool logits_only) {
   sa_status st = check_cache(cache, true, false);
   if (st != SA_OK) return st;
   if ((st = check_batch(batch)) != SA_OK) return st;
@@ -734,7 +747,8 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   const int max_tiles = int((rows + 15) / 16);
   const int ns = choose_nsplit(units, max_tiles, cache->page_size, num_sms());
   const WsLayout w = ws_layout(units, G, cache->head_dim, ns);
-  if (ns > 1 && (!workspace || workspace_bytes < w.total)) return SA_ERR_WORKSPACE;
+  if (logits_only && !logits) return SA_ERR_INVALID_ARG;
+  if (ns > 1 && !logits_only && (!workspace || workspace_bytes < w.total)) return SA_ERR_WORKSPACE;
   DecodeArgs a;
   a.k = cache->k; a.v = cache->v; a.q = q; a.bt = batch->block_table; a.seq_lens = batch->seq_lens;
   a.sel = sel_idx; a.cnt = sel_cnt; a.out = out; a.lse = lse; a.logits = logits;
@@ -748,6 +762,7 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   a.bt_stride = batch->bt_stride; a.sel_stride = sel_stride;
   a.logits_stride = logits ? logits_stride : 0; a.nsplit = ns;
   a.H_u = H_u; a.kv_div = per_query_head ? G_kv : 1;
+  a.logits_only = logits_only ? 1 : 0;
   a.ent_max = ent_max_for(max_tiles, ns, cache->page_size);
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf(float(cache->head_dim));
   a.scale_log2 = a.scale * kLog2e;
@@ -792,7 +807,7 @@ extern "C" sa_status sa_sparse_decode(const sa_cache* cache, const sa_batch* bat
                                       void* stream) {
   return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
                          logits, logits_stride, workspace, workspace_bytes, dev_status, stream, true, false,
-                         false);
+                         false, false);
 }
 
 extern "C" sa_status sa_sparse_decode_qh(const sa_cache* cache, const sa_batch* batch, const void* q,
@@ -802,7 +817,7 @@ extern "C" sa_status sa_sparse_decode_qh(const sa_cache* cache, const sa_batch* 
                                          size_t workspace_bytes, int32_t* dev_status, void* stream) {
   return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
                          nullptr, 0, workspace, workspace_bytes, dev_status, stream, true, false,
-                         true);
+                         true, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -855,5 +870,6 @@ extern "C" sa_status sa_sparse_decode_noalloc(const sa_cache* cache, const sa_ba
     return SA_ERR_CUDA;
   return sa::decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, lse,
                          logits, logits_stride, ws, SA_NOALLOC_SCRATCH_BYTES, dev_status, stream,
-                         /*allow_cluster=*/false, /*pdl=*/false, /*per_query_head=*/false);
+                         /*allow_cluster=*/false, /*pdl=*/false, /*per_query_head=*/false,
+                         /*logits_only=*/false);
 }

@@ -106,6 +106,6 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
                       const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_stride, float scale,
                       void* out, float* lse, float* logits, int32_t logits_stride, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, void* stream, bool allow_cluster,
-                      bool pdl, bool per_query_head);
+                      bool pdl, bool per_query_head, bool logits_only = false);
 
 }  // namespace sa

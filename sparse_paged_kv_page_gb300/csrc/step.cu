@@ -59,5 +59,5 @@ extern "C" sa_status sa_decode_step(const sa_cache* cache, const sa_batch* batch
                    n_eos, sel_idx, sel_cnt, dev_status, stream, true);
   if (st != SA_OK) return st;
   return decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, topk, scale, out, lse, nullptr, 0,
-                     workspace, workspace_bytes, dev_status, stream, true, true, false);
+                     workspace, workspace_bytes, dev_status, stream, true, true, false, false);
 }
