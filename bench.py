@@ -76,6 +76,38 @@ def step_bytes(cfg, lens, per_query_head=False):
     return tot + 2 * cfg.B * cfg.H_q * cfg.D * e
 
 
+def entmax_step_bytes(cfg, lens, v_rows):
+    """Page level with alpha-entmax: the statistics rows, K of the selected
+    pages, V of the v_rows tokens some query head keeps (entmax is sparse: the
+    rest is never read), q and out. The logits between the passes stay in L2."""
+    e = 2
+    tot = 0
+    for L in lens:
+        n = -(-L // cfg.ps)
+        tot += n * cfg.H_kv * 3 * cfg.D * e
+        tot += min(cfg.topk, n) * cfg.H_kv * cfg.ps * cfg.D * e
+    return tot + v_rows * cfg.D * e + 2 * cfg.B * cfg.H_q * cfg.D * e
+
+
+def entmax_kept(dec, alpha):
+    """V rows the last step read, and the mean support per query head, from
+    the step's own logits and thresholds."""
+    import numpy as np
+    z = dec.logits.cpu().numpy().astype(np.float64)
+    tau = dec.tau.cpu().numpy().astype(np.float64)
+    cnt = dec.sel_cnt.cpu().numpy()
+    B, Hq, R = z.shape
+    G = Hq // cnt.shape[1]
+    with np.errstate(invalid="ignore"):
+        keep = np.isfinite(z) & ((alpha - 1.0) * z - tau[:, :, None] > 0)
+    rows = 0
+    for b in range(B):
+        for h in range(cnt.shape[1]):
+            n = int(cnt[b, h]) * dec.ps
+            rows += int(keep[b, h * G:(h + 1) * G, :n].any(0).sum())
+    return rows, float(keep.sum(-1).mean())
+
+
 def h2o_step_bytes(cfg, cnts):
     """Token level: K and V of every retained token, its bf16 score read and
     written, q and out."""
@@ -205,11 +237,11 @@ def _worker_task(task):
 class OracleRunner:
     """The float64 oracle on the host cores, one unit per spawned worker."""
 
-    def __init__(self, wl, workers):
+    def __init__(self, wl, workers, alpha=1.0):
         import multiprocessing as mp
         import tempfile
         import numpy as np
-        self.wl, self.workers = wl, workers
+        self.wl, self.workers, self.alpha = wl, workers, alpha
         self.dir = tempfile.mkdtemp(prefix="sa_oracle_")
         spec = {}
         for name, arr in (("k", wl.k_pre), ("v", wl.v_pre)):
@@ -240,7 +272,7 @@ class OracleRunner:
                 out.append((b, h, lo, hi, ek, ev, L, qg, "h2o", kw, np.zeros(n), np.arange(L - n, L)))
             else:
                 kw = dict(ps=c.ps, topk=c.topk, w_avg=c.w_avg, w_peak=c.w_peak, dtype=c.dtype,
-                          scale=c.scale)
+                          scale=c.scale, alpha=self.alpha)
                 out.append((b, h, lo, hi, ek, ev, L, qg, "page", kw, None, None))
         return out
 
@@ -260,9 +292,9 @@ def units_of(cfg):
     return [(b, h) for b in range(cfg.B) for h in range(cfg.H_kv)]
 
 
-def cpu_baseline(wl, full_steps, workers):
+def cpu_baseline(wl, full_steps, workers, alpha=1.0):
     """Full steps of the oracle (every unit), on `workers` processes."""
-    r = OracleRunner(wl, workers)
+    r = OracleRunner(wl, workers, alpha)
     try:
         r.run(r.tasks(0, units_of(wl.cfg)[:workers]))          # warm the workers
         walls = [r.run(r.tasks(s, units_of(wl.cfg))) for s in range(full_steps)]
@@ -304,7 +336,7 @@ def run_gpu(args, rank, world):
                   ret_cap=int(wl.prefill_lens.max()) + n_in + 4)
     else:
         kw.update(topk=c.topk, w_avg=c.w_avg, w_peak=c.w_peak,
-                  per_query_head=args.per_query_head)
+                  per_query_head=args.per_query_head, alpha=args.entmax or 1.0)
     dec = SparseDecoder(**kw)
     fill_stale(dec.cache.k, "normal3", 11)
     fill_stale(dec.cache.v, "normal3", 12)
@@ -382,9 +414,16 @@ def run_gpu(args, rank, world):
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(step_ms)
+    ent = None
     if token:
         # retained tokens attended per (request, KV head): budget + 1 after the first step
         bytes_per_step = h2o_step_bytes(c, [min(n + 1, c.budget + 1) for n in cnt_start])
+    elif args.entmax:
+        v_rows, support = entmax_kept(dec, args.entmax)
+        bytes_per_step = entmax_step_bytes(c, [L + args.steps for L in lens_start], v_rows)
+        ent = {"alpha": args.entmax, "v_rows_read_last_step": v_rows,
+               "mean_support_per_query_head": support,
+               "selected_tokens_per_kv_head": c.topk * c.ps}
     else:
         bytes_per_step = statistics.mean(
             step_bytes(c, [L + (i + 1 if append else 0) for L in lens_start], args.per_query_head)
@@ -430,10 +469,16 @@ def run_gpu(args, rank, world):
             S.sa_select_topk(dec.scores, dec.max_pages, dec.batch, c.ps, c.H_q if qh else c.H_kv,
                              c.topk, dec.sel_idx, dec.sel_cnt, dev_status=dec.dev_status)
             j += 1; e[j].record(stream)
-            (S.sa_sparse_decode_qh if qh else S.sa_sparse_decode)(
-                dec.cache.struct, dec.batch, dec.q_buf, c.H_q, dec.sel_idx,
-                dec.sel_cnt, c.topk, c.scale, dec.out, lse=dec.lse,
-                workspace=dec.workspace, dev_status=dec.dev_status)
+            if args.entmax:
+                S.sa_sparse_decode_entmax(
+                    dec.cache.struct, dec.batch, dec.q_buf, c.H_q, dec.sel_idx, dec.sel_cnt,
+                    c.topk, args.entmax, c.scale, dec.out, tau=dec.tau, logits=dec.logits,
+                    logits_stride=c.topk * c.ps, workspace=dec.ent_ws, dev_status=dec.dev_status)
+            else:
+                (S.sa_sparse_decode_qh if qh else S.sa_sparse_decode)(
+                    dec.cache.struct, dec.batch, dec.q_buf, c.H_q, dec.sel_idx,
+                    dec.sel_cnt, c.topk, c.scale, dec.out, lse=dec.lse,
+                    workspace=dec.workspace, dev_status=dec.dev_status)
             j += 1; e[j].record(stream)
         torch.cuda.synchronize()
         for k, n in enumerate(names):
@@ -469,8 +514,8 @@ def run_gpu(args, rank, world):
 
     max_ms = dist_max(ms, world, dev)
     max_median_ms = dist_max(statistics.median(step_ms), world, dev)
-    launches = (1 if append else 0) + (2 if token else 3)
-    return dict(ms=ms, max_ms=max_ms, wall=wall, clocks=clk.summary(), bytes=bytes_per_step,
+    launches = (1 if append else 0) + (2 if token else 3) + (3 if args.entmax else 0)
+    return dict(ent=ent, ms=ms, max_ms=max_ms, wall=wall, clocks=clk.summary(), bytes=bytes_per_step,
                 kern=kern, status=status, score_ab=score_ab, e2e=e2e, cfg=c, wl=wl,
                 launches_per_step=launches, step_ms_min=min(step_ms), step_ms_max=max(step_ms),
                 step_ms_median=statistics.median(step_ms), max_median_ms=max_median_ms)
@@ -549,6 +594,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--h2o-prefill", action="store_true",
                     help="time the prefill-side H2O absorb / eviction of the token-level workload")
+    ap.add_argument("--entmax", type=float, default=0.0,
+                    help="attend the selection with alpha-entmax (1 < alpha <= 2) instead of softmax")
     ap.add_argument("--per-query-head", action="store_true",
                     help="select pages per query head (score, select, attend one row per query head)")
     args = ap.parse_args()
@@ -565,7 +612,7 @@ def main():
         if rank != 0:
             return
         wl = make_workload(cfg, extra_steps=2)
-        r = OracleRunner(wl, workers)
+        r = OracleRunner(wl, workers, args.entmax or 1.0)
         try:
             units = units_of(cfg)
             r.run(r.tasks(0, units[:workers]))
@@ -625,7 +672,7 @@ def main():
                 "kernel_ms": res["kern"]}
     cpu = None
     if world == 1 and not args.no_cpu:
-        walls = cpu_baseline(res["wl"], args.cpu_steps, workers)
+        walls = cpu_baseline(res["wl"], args.cpu_steps, workers, args.entmax or 1.0)
         cpu = {"value": 1.0 / statistics.mean(walls), "unit": "steps/s", "cores": workers,
                "kind": "oracle",
                "sample": (f"{len(walls)} full step(s): all {c.B * c.H_kv} (request, KV head) "
@@ -637,7 +684,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": c.dtype, "data": "synthetic",
         "config": {"workload": describe(c) + (", pages selected per query head"
-                                              if args.per_query_head else ""),
+                                              if args.per_query_head else "")
+                   + (f", {args.entmax}-entmax instead of softmax" if args.entmax else ""),
                    "l2": "flushed between steps outside the events: 256 MB write, then a 256 MB read so the flush's dirty lines are written back before the step",
                    "timing": "CUDA events around each step (graph replay); the step's q / k_new / v_new are copied from the HBM-resident input set into its input buffers before the events",
                    "parallelism": f"independent batch per GPU x{world}"},
@@ -651,6 +699,8 @@ def main():
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"], "dev_status": res["status"],
     }
+    if res["ent"]:
+        line["entmax"] = res["ent"]
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -381,13 +381,15 @@ def merge_partials(o_parts, lse_parts):
 # ---------------------------------------------------------------------------
 def page_decode_unit(k_head_bits, v_head_bits, L: int, q_group_bits, *, ps: int,
                      topk: int, w_avg: float, w_peak: float, dtype: str,
-                     scale: float = 0.0):
+                     scale: float = 0.0, alpha: float = 1.0):
     """Steps A1 -> A4 for one (request, KV head): page statistics of the L
     cached keys, page scores, top-k with the tail forced, and attention of the
-    G query heads over the selected pages' valid tokens.
+    G query heads over the selected pages' valid tokens -- softmax, or with
+    alpha != 1 the alpha-entmax of attention_entmax ([entmax] How it works).
 
     k_head_bits, v_head_bits: uint16 [L, D]; q_group_bits: uint16 [G, D].
-    Returns dict(meta=(mn, mx, me), scores, sel, out [G, D], lse [G]).
+    Returns dict(meta=(mn, mx, me), scores, sel, out [G, D], lse [G]) (with
+    entmax: tau [G] in place of lse).
     """
     D = k_head_bits.shape[1]
     sc = scale if scale > 0 else default_scale(D)
@@ -398,6 +400,9 @@ def page_decode_unit(k_head_bits, v_head_bits, L: int, q_group_bits, *, ps: int,
     pos = selected_positions(sel, L, ps)
     k = decode_kdt(k_head_bits[pos], dtype)
     v = decode_kdt(v_head_bits[pos], dtype)
+    if alpha != 1.0:
+        o, tau, _ = attention_entmax(q, k, v, sc, alpha)
+        return {"meta": (mn, mx, me), "scores": scores, "sel": sel, "out": o, "tau": tau}
     o, lse, _ = attention(q, k, v, sc)
     return {"meta": (mn, mx, me), "scores": scores, "sel": sel, "out": o, "lse": lse}
 

@@ -18,7 +18,9 @@
 //      closed-form root of that support; once that root lies below every
 //      member of the support it is the exact tau (the rule "largest support
 //      whose threshold stays below its smallest member"). Sums are float64,
-//      centred on the current iterate;
+//      centred on the current iterate. Since tau >= a_max - 1, only entries
+//      above a_max - 1 can enter the support: those are gathered first (in
+//      row order) and one warp iterates over them alone;
 //  (3) entmax_pv_kernel, split over tokens, one CTA per (split, request, KV
 //      head): each warp tests 32 tokens at a time against the G heads' tau
 //      and loads V rows only for tokens some head of the group keeps
@@ -36,6 +38,7 @@ constexpr int kTauWarps = kTauThreads / 32;
 constexpr int kPvThreads = 256;
 constexpr int kPvWarps = kPvThreads / 32;
 constexpr int kTauMaxIter = 100;
+constexpr int kTauCand = 2048;          // candidates one warp solves over
 
 struct EntArgs {
   const void* v;
@@ -71,10 +74,150 @@ __device__ __forceinline__ double warp_min_d(double v) {
   return v;
 }
 
+// Newton's method with the closed-form finish over the values x[0, m),
+// entries <= skip never in the support, from tau (back to tau_left = a_max - 1,
+// always left of the root, if tau turns out to lie right of it). kBlock: all threads of the CTA share
+// the work (float64 sums through shared memory); else one warp alone. Every
+// participating thread returns the same tau.
+template <bool kBlock>
+__device__ double solve_tau(const float* x, int m, double tau, double tau_left, float skip,
+                            int kind, double r, double (*red)[kTauWarps][4]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = kBlock ? int(threadIdx.x) : lane;
+  const int stride = kBlock ? kTauThreads : 32;
+  bool restarted = tau == tau_left;
+  for (int it = 0; it < kTauMaxIter; ++it) {
+    // over the support {a > tau}: count, sum d^r, sum d^(r-1), min d  (d = a - tau)
+    double k = 0.0, p0 = 0.0, p1 = 0.0, mn = INFINITY;
+    for (int j = t0; j < m; j += stride) {
+      const float xf = x[j];
+      if (!(xf > skip)) continue;
+      const double d = double(xf) - tau;
+      if (d > 0.0) {
+        k += 1.0;
+        if (kind == 2) { p0 += d; p1 += 1.0; }
+        else if (kind == 1) { p0 += d * d; p1 += d; }
+        else { const double t = pow(d, r - 1.0); p0 += t * d; p1 += t; }
+        mn = fmin(mn, d);
+      }
+    }
+    k = warp_sum_d(k); p0 = warp_sum_d(p0); p1 = warp_sum_d(p1); mn = warp_min_d(mn);
+    if constexpr (kBlock) {
+      double(*rb)[4] = red[it & 1];                       // alternate buffers: one barrier a round
+      if (lane == 0) { rb[warp][0] = k; rb[warp][1] = p0; rb[warp][2] = p1; rb[warp][3] = mn; }
+      __syncthreads();
+      k = rb[0][0]; p0 = rb[0][1]; p1 = rb[0][2]; mn = rb[0][3];
+#pragma unroll
+      for (int w = 1; w < kTauWarps; ++w) {
+        k += rb[w][0]; p0 += rb[w][1]; p1 += rb[w][2]; mn = fmin(mn, rb[w][3]);
+      }
+    }
+    if (k <= 0.0) break;                                  // (cannot happen below the root)
+    if (kind != 0) {
+      // the closed-form root of this support, as an offset from tau
+      double delta;
+      if (kind == 2) {
+        delta = (p0 - 1.0) / k;                           // sum d = 1 + k delta
+      } else {
+        const double disc = fmax(p1 * p1 - k * (p0 - 1.0), 0.0);   // k delta^2 - 2 delta sum d + sum d^2 - 1 = 0
+        delta = (p1 - sqrt(disc)) / k;
+      }
+      if (delta >= 0.0 && delta < mn) { tau += delta; break; }   // every member stays positive: exact
+    }
+    const double f = p0 - 1.0;
+    if (f < -1e-12 && !restarted) {                       // started right of the root: go left
+      tau = tau_left;
+      restarted = true;
+      continue;
+    }
+    if (f <= 0.0) break;                                  // at the root up to rounding
+    const double step = f / (r * p1);
+    if (kind == 0 && step <= 1e-15 * fmax(1.0, fabs(tau))) break;
+    tau += step;
+  }
+  return tau;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_min_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ double warp_max_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// One warp, float32: Newton from a_max - 1 (with the closed-form shortcut for
+// alpha 1.5 / 2) to locate the support. Only a first estimate: the float64
+// check below decides.
+__device__ float tau_estimate(const float* x, int m, float tau, int kind, float r) {
+  const int lane = threadIdx.x & 31;
+  for (int it = 0; it < kTauMaxIter; ++it) {
+    float k = 0.f, p0 = 0.f, p1 = 0.f, mn = INFINITY;
+    for (int j = lane; j < m; j += 32) {
+      const float d = x[j] - tau;
+      if (d > 0.f) {
+        k += 1.f;
+        if (kind == 2) { p0 += d; p1 += 1.f; }
+        else if (kind == 1) { p0 += d * d; p1 += d; }
+        else { const float t = powf(d, r - 1.f); p0 += t * d; p1 += t; }
+        mn = fminf(mn, d);
+      }
+    }
+    k = warp_sum_f(k); p0 = warp_sum_f(p0); p1 = warp_sum_f(p1); mn = warp_min_f(mn);
+    if (k <= 0.f) break;
+    if (kind != 0) {
+      float delta;
+      if (kind == 2) delta = (p0 - 1.f) / k;
+      else delta = (p1 - sqrtf(fmaxf(p1 * p1 - k * (p0 - 1.f), 0.f))) / k;
+      if (delta >= 0.f && delta < mn) return tau + delta;
+    }
+    const float f = p0 - 1.f;
+    if (f <= 0.f) break;
+    const float step = f / (r * p1);
+    if (step <= 1e-7f * fmaxf(1.f, fabsf(tau))) break;
+    tau += step;
+  }
+  return tau;
+}
+
+// One warp, float64, alpha 1.5 / 2: the closed-form root tau_c of the support
+// S = {a > t}. It is the exact threshold when S is consistent with it: every
+// member above tau_c and every other entry at or below it (then S = {a > tau_c}
+// and sum_S (a - tau_c)^r = 1, whose root is unique).
+__device__ bool tau_exact_check(const float* x, int m, double t, int kind, double* tau) {
+  const int lane = threadIdx.x & 31;
+  double k = 0.0, s1 = 0.0, s2 = 0.0, mn = INFINITY, mo = -INFINITY;
+  for (int j = lane; j < m; j += 32) {
+    const double d = double(x[j]) - t;
+    if (d > 0.0) { k += 1.0; s1 += d; s2 += d * d; mn = fmin(mn, d); }
+    else mo = fmax(mo, d);
+  }
+  k = warp_sum_d(k); s1 = warp_sum_d(s1); s2 = warp_sum_d(s2);
+  mn = warp_min_d(mn); mo = warp_max_d(mo);
+  if (k <= 0.0) return false;
+  const double delta = kind == 2 ? (s1 - 1.0) / k
+                                 : (s1 - sqrt(fmax(s1 * s1 - k * (s2 - 1.0), 0.0))) / k;
+  if (!(delta < mn && delta >= mo)) return false;
+  *tau = t + delta;
+  return true;
+}
+
 __global__ void __launch_bounds__(kTauThreads) entmax_tau_kernel(EntArgs a) {
   extern __shared__ float s_a[];                          // (alpha - 1) z of the row
+  __shared__ float s_c[kTauCand];                         // the candidates, in row order
   __shared__ double red[2][kTauWarps][4];
   __shared__ float redf[kTauWarps];
+  __shared__ int redi[kTauWarps];
   const int gq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   int c = a.cnt[b * a.H_kv + gq / a.G];
@@ -106,46 +249,43 @@ __global__ void __launch_bounds__(kTauThreads) entmax_tau_kernel(EntArgs a) {
   }
   const int kind = alpha_kind(a.alpha);
   const double r = 1.0 / double(am1);
-  double tau = double(mx) - 1.0;
-  for (int it = 0; it < kTauMaxIter; ++it) {
-    // over the support {a > tau}: count, sum d^r, sum d^(r-1), min d  (d = a - tau)
-    double k = 0.0, p0 = 0.0, p1 = 0.0, mn = INFINITY;
-    for (int j = tid; j < n; j += kTauThreads) {
-      const double d = double(s_a[j]) - tau;
-      if (d > 0.0) {
-        k += 1.0;
-        if (kind == 2) { p0 += d; p1 += 1.0; }
-        else if (kind == 1) { p0 += d * d; p1 += d; }
-        else { const double t = pow(d, r - 1.0); p0 += t * d; p1 += t; }
-        mn = fmin(mn, d);
-      }
-    }
-    k = warp_sum_d(k); p0 = warp_sum_d(p0); p1 = warp_sum_d(p1); mn = warp_min_d(mn);
-    double(*rb)[4] = red[it & 1];                         // alternate buffers: one barrier a round
-    if (lane == 0) { rb[warp][0] = k; rb[warp][1] = p0; rb[warp][2] = p1; rb[warp][3] = mn; }
-    __syncthreads();
-    k = rb[0][0]; p0 = rb[0][1]; p1 = rb[0][2]; mn = rb[0][3];
+  // tau never drops below a_max - 1, so only a > a_max - 1 can be in the
+  // support: gather those (with a margin for the float rounding) in row order
+  const float lo = (mx - 1.0f) - 1e-6f * (1.0f + fabsf(mx));
+  const int per = (n + kTauThreads - 1) / kTauThreads;
+  const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
+  int mine = 0;
+  for (int j = j0; j < j1; ++j) mine += s_a[j] > lo;
+  int incl = mine;
 #pragma unroll
-    for (int w = 1; w < kTauWarps; ++w) {
-      k += rb[w][0]; p0 += rb[w][1]; p1 += rb[w][2]; mn = fmin(mn, rb[w][3]);
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) redi[warp] = incl;
+  __syncthreads();
+  int off = incl - mine, m = 0;
+#pragma unroll
+  for (int w = 0; w < kTauWarps; ++w) {
+    if (w < warp) off += redi[w];
+    m += redi[w];
+  }
+  double tau;
+  if (m <= kTauCand) {
+    for (int j = j0; j < j1; ++j)
+      if (s_a[j] > lo) s_c[off++] = s_a[j];
+    __syncthreads();
+    if (warp != 0) return;
+    const float est = tau_estimate(s_c, m, mx - 1.0f, kind, float(r));
+    if (kind == 0 || !tau_exact_check(s_c, m, double(est), kind, &tau)) {
+      // generic alpha, or a support the float32 estimate got wrong: float64
+      // Newton from the left (from a_max - 1, or from just below the estimate
+      // when that is still left of the root)
+      const double t0 = fmax(double(mx) - 1.0, double(est) - 1e-3 * (1.0 + fabs(double(est))));
+      tau = solve_tau<false>(s_c, m, t0, double(mx) - 1.0, -INFINITY, kind, r, red);
     }
-    if (k <= 0.0) break;                                  // (cannot happen below the root)
-    if (kind != 0) {
-      // the closed-form root of this support, as an offset from tau
-      double delta;
-      if (kind == 2) {
-        delta = (p0 - 1.0) / k;                           // sum d = 1 + k delta
-      } else {
-        const double disc = fmax(p1 * p1 - k * (p0 - 1.0), 0.0);   // k delta^2 - 2 delta sum d + sum d^2 - 1 = 0
-        delta = (p1 - sqrt(disc)) / k;
-      }
-      if (delta < mn) { tau += delta; break; }            // every member stays positive: exact
-    }
-    const double f = p0 - 1.0;
-    if (f <= 0.0) break;                                  // at the root up to rounding
-    const double step = f / (r * p1);
-    if (kind == 0 && step <= 1e-15 * fmax(1.0, fabs(tau))) break;
-    tau += step;
+  } else {
+    tau = solve_tau<true>(s_a, n, double(mx) - 1.0, double(mx) - 1.0, lo, kind, r, red);
   }
   if (tid == 0) {
     a.tau[row] = float(tau);

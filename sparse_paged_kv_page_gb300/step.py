@@ -6,6 +6,9 @@ Page level (page_size > 1):  append -> score -> select -> sparse decode, one
                              score entry is then unspecified).
 Token level (page_size 1):   append (+ retained list) -> sparse decode over
                              the retained tokens (logits + lse) -> H2O update.
+alpha-entmax (1 < alpha <= 2, page level): append -> score -> select ->
+                             ``sa_sparse_decode_entmax`` (the selection
+                             normalised by alpha-entmax instead of softmax).
 
 PyTorch only allocates the buffers and supplies the stream; every step runs in
 the native kernels. ``capture()`` records one step into a CUDA graph whose
@@ -18,10 +21,10 @@ from typing import Optional, Sequence
 
 import torch
 
-from .api import (PagedKVCache, alloc_decode_workspace, make_batch, sa_append_kv,
-                  sa_decode_step, sa_h2o_prefill, sa_h2o_update, sa_h2o_update_window,
-                  sa_score_pages,
-                  sa_score_pages_qh, sa_select_topk_reserved, sa_sparse_decode,
+from .api import (PagedKVCache, alloc_decode_workspace, alloc_entmax_workspace, make_batch,
+                  sa_append_kv, sa_decode_step, sa_h2o_prefill, sa_h2o_update,
+                  sa_h2o_update_window, sa_score_pages, sa_score_pages_qh,
+                  sa_select_topk_reserved, sa_sparse_decode, sa_sparse_decode_entmax,
                   sa_sparse_decode_qh)
 
 
@@ -31,7 +34,8 @@ class SparseDecoder:
                  topk: int = 0, w_avg: float = 1.0, w_peak: float = 0.25, scale: float = 0.0,
                  budget: int = 0, n_sink: int = 0, grace: int = 0, decay: float = 1.0,
                  ret_cap: int = 0, n_bos: int = 0, n_eos: int = 1, window_softmax: bool = False,
-                 per_query_head: bool = False, proxy_prefill: bool = False, device="cuda"):
+                 per_query_head: bool = False, proxy_prefill: bool = False, alpha: float = 1.0,
+                 device="cuda"):
         self.B, self.H_q, self.H_kv, self.D = batch, num_q_heads, num_kv_heads, head_dim
         self.ps, self.dtype, self.device = page_size, dtype, torch.device(device)
         self.token_level = page_size == 1 and ret_cap > 0
@@ -43,6 +47,11 @@ class SparseDecoder:
         # token level: trim a prefill H2O-style as it arrives (each key as its own query)
         self.proxy_prefill = proxy_prefill and self.token_level
         rows = num_q_heads if self.qh else num_kv_heads
+        # alpha-entmax instead of softmax over the selection (page level, per KV head)
+        self.alpha = float(alpha)
+        self.entmax = self.alpha != 1.0
+        if self.entmax and (self.token_level or self.qh or not 1.0 < self.alpha <= 2.0):
+            raise ValueError("entmax decoding needs 1 < alpha <= 2, page level, per-KV-head selection")
         self.cache = PagedKVCache(num_blocks, num_kv_heads, page_size, head_dim, dtype, device,
                                   with_meta=not self.token_level, with_hh=self.token_level)
         i32 = dict(dtype=torch.int32, device=device)
@@ -73,6 +82,12 @@ class SparseDecoder:
         self.workspace = alloc_decode_workspace(batch, rows if not self.token_level else num_kv_heads,
                                                 num_q_heads, head_dim, page_size, self.sel_stride,
                                                 device)
+        if self.entmax:
+            self.ent_ws = alloc_entmax_workspace(batch, num_kv_heads, num_q_heads, head_dim,
+                                                 page_size, self.sel_stride, device)
+            self.tau = torch.empty((batch, num_q_heads), dtype=torch.float32, device=device)
+            self.logits = torch.empty((batch, num_q_heads, self.sel_stride * page_size),
+                                      dtype=torch.float32, device=device)
         self.dev_status = torch.zeros((1,), **i32)
         self.decode_cu = torch.arange(batch + 1, **i32)
         self.q_buf = torch.zeros((batch, num_q_heads, head_dim), dtype=dtype, device=device)
@@ -144,6 +159,13 @@ class SparseDecoder:
             sa_select_topk_reserved(self.scores, self.max_pages, self.batch, self.ps, self.H_kv,
                                     self.topk, self.n_bos, self.n_eos, self.sel_idx, self.sel_cnt,
                                     dev_status=self.dev_status)
+            if self.entmax:
+                sa_sparse_decode_entmax(self.cache.struct, self.batch, q, self.H_q, self.sel_idx,
+                                        self.sel_cnt, self.topk, self.alpha, self.scale, self.out,
+                                        tau=self.tau, logits=self.logits,
+                                        logits_stride=self.topk * self.ps, workspace=self.ent_ws,
+                                        dev_status=self.dev_status)
+                return self.out
             sa_sparse_decode(self.cache.struct, self.batch, q, self.H_q, self.sel_idx,
                              self.sel_cnt, self.topk, self.scale, self.out, lse=self.lse,
                              workspace=self.workspace, dev_status=self.dev_status)
@@ -151,7 +173,7 @@ class SparseDecoder:
 
     def step(self, q: torch.Tensor, k_new: Optional[torch.Tensor] = None,
              v_new: Optional[torch.Tensor] = None):
-        if self.token_level or self.qh:
+        if self.token_level or self.qh or self.entmax:
             if k_new is not None:
                 self.append(k_new, v_new)
             return self.attend(q)

@@ -33,3 +33,15 @@ def test_byte_models():
     # 3 statistics rows of D bf16 per (page, KV head)
     assert bench.score_bytes(c, [16 * 10]) == 10 * c.H_kv * 3 * c.D * 2
     assert bench.score_bytes(c, [16 * 10 + 1]) == 11 * c.H_kv * 3 * c.D * 2
+
+
+def test_entmax_byte_model_reads_v_only_for_kept_rows():
+    from sa_synth import config
+    c = config(5)
+    L = 16 * 1000
+    full = bench.step_bytes(c, [L])
+    # every selected token kept: the softmax step's bytes
+    all_rows = c.topk * c.ps * c.H_kv
+    assert bench.entmax_step_bytes(c, [L], all_rows) == full
+    # no V row read: K of the selection, the statistics, q and out
+    assert full - bench.entmax_step_bytes(c, [L], 0) == all_rows * c.D * 2

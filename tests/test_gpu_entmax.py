@@ -205,3 +205,30 @@ def test_entmax_rejects_before_launching():
     assert e.value.status == 3
     torch.cuda.synchronize()
     assert torch.all(out.float() == 7.0)                     # nothing ran
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0, 1.25])
+def test_many_candidates_take_the_block_solver(alpha):
+    """Near-equal logits put every token within 1 of the top one: more
+    candidates than one warp gathers, so the CTA-wide float64 solver runs."""
+    cfg = config(3, small=True).replace(len_range=(2600, 3000), topk=170)
+    wl = make_workload(cfg)
+    dec = make_decoder(wl)
+    c = wl.cfg
+    sel, cnt = _selection(wl, np.random.default_rng(8), c.topk)
+    assert (cnt * c.ps).max() > 2048
+    qb = wl.q(0)
+    out, tau, lg = _run(dec, dev_bits(qb, c.dtype), sel, cnt, c.topk, alpha, scale=1e-3)
+    _check(wl, qb, sel, cnt, out, tau, lg, alpha, 1e-3)
+    # q = 0: every logit 0, p uniform; tau = -1/n (alpha 2), -1/sqrt(n) (alpha 1.5)
+    if alpha in (1.5, 2.0):
+        q0 = torch.zeros_like(dev_bits(qb, c.dtype))
+        out, tau, _ = _run(dec, q0, sel, cnt, c.topk, alpha)
+        t_np = tau.cpu().numpy()
+        for b in range(c.B):
+            L = int(wl.prefill_lens[b])
+            for h in range(c.H_kv):
+                n = len(O.selected_positions(sel[b, h, :cnt[b, h]], L, c.ps))
+                want = -1.0 / n if alpha == 2.0 else -1.0 / np.sqrt(n)
+                assert np.allclose(t_np[b, h * c.G:(h + 1) * c.G], want, rtol=1e-6, atol=0)
+    assert dev_status(dec) == 0

@@ -156,3 +156,46 @@ def test_full_token_h2o_first_steps():
                 assert (vals - tol)[gone].max() <= (vals + tol)[elig & ~gone].min()
                 break
     assert dev_status(dec) == 0
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_full_long_context_entmax(alpha):
+    """The long-context workload with alpha-entmax over the selection, as
+    bench.py --entmax runs it (graph replay, one-token appends): sampled units
+    against the oracle's entmax attention over the GPU's own selection."""
+    wl = make_workload(config(5))
+    c = wl.cfg
+    dec = make_decoder(wl, stale="nan", extra=dict(alpha=alpha))
+    units = [(0, 0), (2, 5), (3, 7)]
+    sc = c.scale if c.scale > 0 else O.default_scale(c.D)
+
+    def check(t):
+        out = dec.out.float()
+        assert torch.isfinite(out).all() and torch.isfinite(dec.tau).all()
+        if t not in (0, 3):
+            return
+        sel = dec.sel_idx.cpu().numpy()
+        cnt = dec.sel_cnt.cpu().numpy()
+        o_np = out.cpu().numpy()
+        tau = dec.tau.cpu().numpy()
+        lg = dec.logits.cpu().numpy()
+        for b, h in units:
+            L = wl.seq_len(b, t + 1)
+            m = int(cnt[b, h])
+            assert m == c.topk
+            pos = O.selected_positions(sel[b, h, :m], L, c.ps)
+            ks = O.decode_kdt(wl.k_seq(b, t + 1)[:, h, :][pos], c.dtype)
+            vs = O.decode_kdt(wl.v_seq(b, t + 1)[:, h, :][pos], c.dtype)
+            rows = slice(h * c.G, (h + 1) * c.G)
+            q = O.decode_kdt(wl.q(t)[b, rows], c.dtype)
+            o, _, z = O.attention_entmax(q, ks, vs, sc, alpha)
+            assert_attention(o_np[b, rows], o)
+            zg = lg[b, rows, :m * c.ps]
+            zg = zg[:, np.isfinite(zg[0])].astype(np.float64)
+            assert zg.shape == z.shape and np.all(np.abs(zg - z) <= 1e-4 * (1 + np.abs(z)))
+            for gi in range(c.G):
+                tz = O.entmax_threshold(zg[gi], alpha)
+                assert abs(float(tau[b, h * c.G + gi]) - tz) <= 1e-6 * (1 + abs(tz))
+
+    _graph_steps(dec, wl, 4, True, check)
+    assert dev_status(dec) == 0

@@ -687,3 +687,23 @@ def test_entmax_special_cases():
     z = np.array([0.3, -0.2, 1.1, 0.0])
     sm = np.exp(z - z.max()); sm /= sm.sum()
     assert np.allclose(O.entmax(z, 1.001), sm, atol=5e-3)
+
+
+def test_page_decode_unit_entmax_with_every_page_is_dense_entmax():
+    """All pages selected: the unit's entmax output is entmax attention over
+    every cached token, and alpha = 1 keeps the softmax path."""
+    rng = np.random.default_rng(21)
+    L, D, G, ps = 45, 16, 2, 8
+    kb = O.encode_kdt(rng.standard_normal((L, D)), "bf16")
+    vb = O.encode_kdt(rng.standard_normal((L, D)), "bf16")
+    qb = O.encode_kdt(rng.standard_normal((G, D)), "bf16")
+    for alpha in (1.5, 2.0):
+        r = O.page_decode_unit(kb, vb, L, qb, ps=ps, topk=99, w_avg=1.0, w_peak=0.25,
+                               dtype="bf16", alpha=alpha)
+        k, v, q = (O.decode_kdt(x, "bf16") for x in (kb, vb, qb))
+        o, tau, _ = O.attention_entmax(q, k, v, D ** -0.5, alpha)
+        assert np.array_equal(r["out"], o) and np.array_equal(r["tau"], tau)
+        # rows of p sum to 1: o lies in the convex hull of V, per dimension
+        assert np.all(r["out"] <= v.max(0) + 1e-12) and np.all(r["out"] >= v.min(0) - 1e-12)
+    r1 = O.page_decode_unit(kb, vb, L, qb, ps=ps, topk=99, w_avg=1.0, w_peak=0.25, dtype="bf16")
+    assert "lse" in r1
