@@ -295,9 +295,11 @@ sa_status sa_sparse_decode_qh(const sa_cache* cache, const sa_batch* batch, cons
 /*
  * sa_entmax_workspace_size -- bytes of workspace sa_sparse_decode_entmax
  * needs for these sizes (host function; reads the device's SM count). The
- * workspace holds the logits (when the caller passes none), the thresholds
- * and the per-split partial sums; it needs no initialisation. Calls that share
- * a workspace must be ordered on one stream.
+ * workspace holds the logits (when the caller passes none), the per-split
+ * partial sums and one counter per (request, KV head); it must be zero-filled
+ * once before its first use (sa_decode_workspace_init does this) and every
+ * call leaves the counters at zero again. Calls that share a workspace must be
+ * ordered on one stream.
  */
 size_t sa_entmax_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads,
                                 int32_t head_dim, int32_t page_size, int32_t sel_stride);
@@ -312,9 +314,10 @@ size_t sa_entmax_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num
  * valid tokens of the selection and a_j = (alpha - 1) z_j,
  *   p_j = max(a_j - tau, 0) ^ (1 / (alpha - 1)),  sum_j p_j = 1,
  *   o   = sum_j p_j v_j.
- * tau is exact for alpha = 1.5 and 2 (the closed form on the support, the
- * support being the largest set whose threshold stays below its smallest
- * member) and found by Newton's method to float64 precision otherwise.
+ * tau is computed in float32: for alpha = 1.5 and 2 as the closed form on the
+ * support (the largest set whose threshold stays below its smallest member,
+ * found by Newton's method from max_j a_j - 1), otherwise by Newton's method
+ * until its step falls below float32 resolution.
  *   q, sel_idx, sel_cnt, sel_stride, scale, out   as sa_sparse_decode
  *   alpha      1 < alpha <= 2, else SA_ERR_INVALID_ARG
  *   tau        nullable float32 [batch, num_q_heads]: the threshold in units
@@ -325,8 +328,9 @@ size_t sa_entmax_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num
  * The output is divided by the float32 sum of the p_j it used (1 up to the
  * rounding of tau). K of every selected token is read once; V only for the
  * tokens some query head of the group keeps. Limits: num_q_heads / num_kv_heads
- * <= 16 and sel_stride * page_size <= 40960, else SA_ERR_UNSUPPORTED. Data
- * errors as sa_sparse_decode.
+ * <= 16, and the selection entries one CTA resolves must fit its shared
+ * memory (a few thousand entries), else SA_ERR_UNSUPPORTED before anything is
+ * launched. Data errors as sa_sparse_decode.
  */
 sa_status sa_sparse_decode_entmax(const sa_cache* cache, const sa_batch* batch, const void* q,
                                   int32_t num_q_heads, const int32_t* sel_idx,

@@ -211,10 +211,10 @@ def sa_entmax_workspace_size(batch: int, num_kv_heads: int, num_q_heads: int, he
 
 def alloc_entmax_workspace(batch, num_kv_heads, num_q_heads, head_dim, page_size, sel_stride,
                            device="cuda"):
-    """A workspace tensor of the size sa_sparse_decode_entmax needs."""
+    """A zero-filled workspace tensor of the size sa_sparse_decode_entmax needs."""
     n = max(256, sa_entmax_workspace_size(batch, num_kv_heads, num_q_heads, head_dim, page_size,
                                           sel_stride))
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def sa_sparse_decode_entmax(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_idx, sel_cnt,

@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   // lengths and selection come from the kernels before this one in the step
   pdl_wait();
+  if (a.logits_only) pdl_trigger();                           // the entmax threshold kernel may launch
 
   // This CTA's range of selection entries is a function of the count. The
   // entry it would start at with a full selection (the usual case) is loaded

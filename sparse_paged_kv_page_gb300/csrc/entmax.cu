@@ -7,38 +7,39 @@
 // scaled logits of the selection, p_j = (a_j - tau)_+ ^ (1 / (alpha - 1)) and
 // tau fixed by sum_j p_j = 1.
 //
-// Four launches:
+// Three launches, chained by programmatic dependent launch:
 //  (1) the decode kernel in its logits-only mode writes z for every selected
 //      token (K is read; V is not);
-//  (2) entmax_tau_kernel, one CTA per (request, query head), finds tau.
-//      f(tau) = sum_j (a_j - tau)_+^r - 1 (r = 1 / (alpha - 1) >= 1) is convex
-//      and decreasing, and f(a_max - 1) >= 0 (the top entry alone gives 1), so
-//      Newton's method from a_max - 1 rises monotonically to the root. For
-//      alpha = 2 and 1.5 each iterate's support {a_j > tau} also gives the
-//      closed-form root of that support; once that root lies below every
-//      member of the support it is the exact tau (the rule "largest support
-//      whose threshold stays below its smallest member"). Sums are float64,
-//      centred on the current iterate. Since tau >= a_max - 1, only entries
-//      above a_max - 1 can enter the support: those are gathered first (in
-//      row order) and one warp iterates over them alone;
-//  (3) entmax_pv_kernel, split over tokens, one CTA per (split, request, KV
-//      head): each warp tests 32 tokens at a time against the G heads' tau
+//  (2) entmax_tau_kernel, one CTA per (request, query head), finds tau:
+//      only entries above a_max - 1 can ever be in the support (tau >= a_max
+//      - 1): the CTA gathers those. For alpha = 2 and 1.5 it ranks them and
+//      takes the closed-form root of the largest support whose root stays
+//      below its smallest member (the sort-based rule, exact); for
+//      other alpha one warp runs Newton's method from a_max - 1, which rises
+//      monotonically to the root of the convex, decreasing f(tau) = sum_j
+//      (a_j - tau)_+^r - 1 (r = 1 / (alpha - 1) >= 1), with the closed-form
+//      shortcut of each iterate's support where one exists. float32;
+//  (3) entmax_attend_kernel, split over tokens, one CTA per (split, request,
+//      KV head): each warp tests 32 tokens at a time against the G heads' tau
 //      and loads V rows only for tokens some head of the group keeps
 //      (entmax is sparse), accumulating sum_j p_j v_j and sum_j p_j in fp32;
-//  (4) entmax_finish_kernel adds the splits in a fixed order and divides by
-//      sum_j p_j (1 up to the rounding of tau), writing bf16/fp16.
+//      the last CTA of a (request, KV head) adds the splits in a fixed order
+//      and divides by sum_j p_j (1 up to the rounding of tau).
 #include "common.cuh"
 #include "host.h"
 
 namespace sa {
 namespace {
 
-constexpr int kTauThreads = 256;
-constexpr int kTauWarps = kTauThreads / 32;
-constexpr int kPvThreads = 256;
-constexpr int kPvWarps = kPvThreads / 32;
-constexpr int kTauMaxIter = 100;
-constexpr int kTauCand = 2048;          // candidates one warp solves over
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCand = 256;               // candidates each warp of the tau kernel gathers (beyond: the row is streamed)
+constexpr int kMaxIter = 100;
+constexpr int kRowReg = 16;              // row entries per thread the tau kernel keeps in registers
+constexpr int kSortMax = kWarps * kCand; // every gathered candidate can be ranked
+constexpr int kRankDirect = 64;          // up to this many candidates: rank by direct counting
+static_assert(kCand == 256, "the per-warp sort holds 8 candidates a lane");
 
 struct EntArgs {
   const void* v;
@@ -51,6 +52,7 @@ struct EntArgs {
   float* tau_out;        // optional copy for the caller
   float* part_o;         // [B, H_q, nsplit, D]
   float* part_l;         // [B, H_q, nsplit]
+  int32_t* tickets;      // [B, H_kv]: splits of the (request, KV head) done
   void* out;
   int32_t* status;
   int H_kv, H_q, G, ps, ps_shift, num_blocks, bt_stride, sel_stride, logits_stride, nsplit, ent_cap;
@@ -60,82 +62,6 @@ struct EntArgs {
 // 0: generic alpha (Newton only), 1: alpha = 1.5, 2: alpha = 2
 __host__ __device__ inline int alpha_kind(float alpha) {
   return alpha == 2.0f ? 2 : (alpha == 1.5f ? 1 : 0);
-}
-
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
-
-__device__ __forceinline__ double warp_min_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmin(v, __shfl_xor_sync(kFull, v, o));
-  return v;
-}
-
-// Newton's method with the closed-form finish over the values x[0, m),
-// entries <= skip never in the support, from tau (back to tau_left = a_max - 1,
-// always left of the root, if tau turns out to lie right of it). kBlock: all threads of the CTA share
-// the work (float64 sums through shared memory); else one warp alone. Every
-// participating thread returns the same tau.
-template <bool kBlock>
-__device__ double solve_tau(const float* x, int m, double tau, double tau_left, float skip,
-                            int kind, double r, double (*red)[kTauWarps][4]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t0 = kBlock ? int(threadIdx.x) : lane;
-  const int stride = kBlock ? kTauThreads : 32;
-  bool restarted = tau == tau_left;
-  for (int it = 0; it < kTauMaxIter; ++it) {
-    // over the support {a > tau}: count, sum d^r, sum d^(r-1), min d  (d = a - tau)
-    double k = 0.0, p0 = 0.0, p1 = 0.0, mn = INFINITY;
-    for (int j = t0; j < m; j += stride) {
-      const float xf = x[j];
-      if (!(xf > skip)) continue;
-      const double d = double(xf) - tau;
-      if (d > 0.0) {
-        k += 1.0;
-        if (kind == 2) { p0 += d; p1 += 1.0; }
-        else if (kind == 1) { p0 += d * d; p1 += d; }
-        else { const double t = pow(d, r - 1.0); p0 += t * d; p1 += t; }
-        mn = fmin(mn, d);
-      }
-    }
-    k = warp_sum_d(k); p0 = warp_sum_d(p0); p1 = warp_sum_d(p1); mn = warp_min_d(mn);
-    if constexpr (kBlock) {
-      double(*rb)[4] = red[it & 1];                       // alternate buffers: one barrier a round
-      if (lane == 0) { rb[warp][0] = k; rb[warp][1] = p0; rb[warp][2] = p1; rb[warp][3] = mn; }
-      __syncthreads();
-      k = rb[0][0]; p0 = rb[0][1]; p1 = rb[0][2]; mn = rb[0][3];
-#pragma unroll
-      for (int w = 1; w < kTauWarps; ++w) {
-        k += rb[w][0]; p0 += rb[w][1]; p1 += rb[w][2]; mn = fmin(mn, rb[w][3]);
-      }
-    }
-    if (k <= 0.0) break;                                  // (cannot happen below the root)
-    if (kind != 0) {
-      // the closed-form root of this support, as an offset from tau
-      double delta;
-      if (kind == 2) {
-        delta = (p0 - 1.0) / k;                           // sum d = 1 + k delta
-      } else {
-        const double disc = fmax(p1 * p1 - k * (p0 - 1.0), 0.0);   // k delta^2 - 2 delta sum d + sum d^2 - 1 = 0
-        delta = (p1 - sqrt(disc)) / k;
-      }
-      if (delta >= 0.0 && delta < mn) { tau += delta; break; }   // every member stays positive: exact
-    }
-    const double f = p0 - 1.0;
-    if (f < -1e-12 && !restarted) {                       // started right of the root: go left
-      tau = tau_left;
-      restarted = true;
-      continue;
-    }
-    if (f <= 0.0) break;                                  // at the root up to rounding
-    const double step = f / (r * p1);
-    if (kind == 0 && step <= 1e-15 * fmax(1.0, fabs(tau))) break;
-    tau += step;
-  }
-  return tau;
 }
 
 __device__ __forceinline__ float warp_sum_f(float v) {
@@ -150,162 +76,369 @@ __device__ __forceinline__ float warp_min_f(float v) {
   return v;
 }
 
-__device__ __forceinline__ double warp_max_d(double v) {
+__device__ __forceinline__ float warp_max_f(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(kFull, v, o));
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
   return v;
 }
 
-// One warp, float32: Newton from a_max - 1 (with the closed-form shortcut for
-// alpha 1.5 / 2) to locate the support. Only a first estimate: the float64
-// check below decides.
-__device__ float tau_estimate(const float* x, int m, float tau, int kind, float r) {
+// s += x with the rounding error carried in c (Kahan-Babuska-Neumaier)
+__device__ __forceinline__ void csum(float& s, float& c, float x) {
+  const float t = s + x;
+  c += fabsf(s) >= fabsf(x) ? (s - t) + x : (x - t) + s;
+  s = t;
+}
+
+// The support sums at tau over this lane's share of the entries: count,
+// sum d^r, sum d^(r-1), min d over the members (d = a - tau > 0) and max d
+// over the others.
+struct Sums {
+  float k, p0, p1, mn, mo;
+};
+
+__device__ __forceinline__ void add_entry(float x, float tau, int kind, float r, Sums& s, float& c0,
+                                          float& c1) {
+  const float d = x - tau;
+  if (d > 0.f) {
+    s.k += 1.f;
+    if (kind == 2) {
+      csum(s.p0, c0, d);
+      s.p1 += 1.f;
+    } else if (kind == 1) {
+      csum(s.p0, c0, d * d);
+      csum(s.p1, c1, d);
+    } else {
+      const float t = powf(d, r - 1.f);
+      csum(s.p0, c0, t * d);
+      csum(s.p1, c1, t);
+    }
+    s.mn = fminf(s.mn, d);
+  } else {
+    s.mo = fmaxf(s.mo, d);
+  }
+}
+
+// One Newton round given the warp's reduced sums: returns true when tau is final.
+__device__ __forceinline__ bool newton_round(const Sums& s, int kind, float r, float& tau) {
+  if (s.k <= 0.f) return true;                              // (cannot happen below the root)
+  const float f = s.p0 - 1.f;
+  if (kind != 0) {
+    // closed-form root of this support, as an offset from tau, without
+    // cancellation: alpha 2: sum d = 1 + k delta; alpha 1.5: the smaller root
+    // of k delta^2 - 2 delta sum d + sum d^2 - 1 = 0
+    const float delta = kind == 2 ? f / s.k : f / (s.p1 + sqrtf(fmaxf(s.p1 * s.p1 - s.k * f, 0.f)));
+    if (delta >= s.mo && delta < s.mn) {
+      // every member stays above tau + delta and every other entry at or
+      // below it: the support is consistent with its root. A large step came
+      // from sums taken far from the root (d near 1), so take one more round
+      tau += delta;
+      return fabsf(delta) <= 1e-6f * (1.f + fabsf(tau));
+    }
+  }
+  if (f <= 0.f) return true;                                // at the root up to rounding
+  const float step = f / (r * s.p1);
+  if (step <= 1e-7f * fmaxf(1.f, fabsf(tau))) return true;
+  tau += step;
+  return false;
+}
+
+// a = (alpha - 1) z, non-finite logits never entering
+__device__ __forceinline__ float a_of(float z, float am1) {
+  return (z > -INFINITY && z < INFINITY) ? am1 * z : -INFINITY;
+}
+
+// One warp's Newton rounds over the candidates gathered per warp
+// (cand[w][0, cnt[w])); every lane returns tau.
+__device__ float solve_gathered(const float (*cand)[kCand], const int* cnt, float tau, int kind,
+                                float r) {
   const int lane = threadIdx.x & 31;
-  for (int it = 0; it < kTauMaxIter; ++it) {
-    float k = 0.f, p0 = 0.f, p1 = 0.f, mn = INFINITY;
-    for (int j = lane; j < m; j += 32) {
-      const float d = x[j] - tau;
-      if (d > 0.f) {
-        k += 1.f;
-        if (kind == 2) { p0 += d; p1 += 1.f; }
-        else if (kind == 1) { p0 += d * d; p1 += d; }
-        else { const float t = powf(d, r - 1.f); p0 += t * d; p1 += t; }
-        mn = fminf(mn, d);
-      }
-    }
-    k = warp_sum_f(k); p0 = warp_sum_f(p0); p1 = warp_sum_f(p1); mn = warp_min_f(mn);
-    if (k <= 0.f) break;
-    if (kind != 0) {
-      float delta;
-      if (kind == 2) delta = (p0 - 1.f) / k;
-      else delta = (p1 - sqrtf(fmaxf(p1 * p1 - k * (p0 - 1.f), 0.f))) / k;
-      if (delta >= 0.f && delta < mn) return tau + delta;
-    }
-    const float f = p0 - 1.f;
-    if (f <= 0.f) break;
-    const float step = f / (r * p1);
-    if (step <= 1e-7f * fmaxf(1.f, fabsf(tau))) break;
-    tau += step;
+  for (int it = 0; it < kMaxIter; ++it) {
+    Sums s = {0.f, 0.f, 0.f, INFINITY, -INFINITY};
+    float c0 = 0.f, c1 = 0.f;
+    for (int w = 0; w < kWarps; ++w)
+      for (int j = lane; j < cnt[w]; j += 32) add_entry(cand[w][j], tau, kind, r, s, c0, c1);
+    s.p0 += c0;
+    s.p1 += c1;
+    s.k = warp_sum_f(s.k); s.p0 = warp_sum_f(s.p0); s.p1 = warp_sum_f(s.p1);
+    s.mn = warp_min_f(s.mn); s.mo = warp_max_f(s.mo);
+    if (newton_round(s, kind, r, tau)) break;
   }
   return tau;
 }
 
-// One warp, float64, alpha 1.5 / 2: the closed-form root tau_c of the support
-// S = {a > t}. It is the exact threshold when S is consistent with it: every
-// member above tau_c and every other entry at or below it (then S = {a > tau_c}
-// and sum_S (a - tau_c)^r = 1, whose root is unique).
-__device__ bool tau_exact_check(const float* x, int m, double t, int kind, double* tau) {
-  const int lane = threadIdx.x & 31;
-  double k = 0.0, s1 = 0.0, s2 = 0.0, mn = INFINITY, mo = -INFINITY;
-  for (int j = lane; j < m; j += 32) {
-    const double d = double(x[j]) - t;
-    if (d > 0.0) { k += 1.0; s1 += d; s2 += d * d; mn = fmin(mn, d); }
-    else mo = fmax(mo, d);
+// All threads over the whole row (entries <= skip never in the support), the
+// sums combined through shared memory; every thread returns the same tau.
+__device__ float solve_row(const float* z, int n, float am1, float tau, float skip, int kind, float r,
+                           float (*red)[kWarps][5]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int it = 0; it < kMaxIter; ++it) {
+    Sums s = {0.f, 0.f, 0.f, INFINITY, -INFINITY};
+    float c0 = 0.f, c1 = 0.f;
+    for (int j = threadIdx.x; j < n; j += kThreads) {
+      const float x = a_of(__ldcg(z + j), am1);
+      if (x > skip) add_entry(x, tau, kind, r, s, c0, c1);
+    }
+    s.p0 += c0;
+    s.p1 += c1;
+    s.k = warp_sum_f(s.k); s.p0 = warp_sum_f(s.p0); s.p1 = warp_sum_f(s.p1);
+    s.mn = warp_min_f(s.mn); s.mo = warp_max_f(s.mo);
+    float(*rb)[5] = red[it & 1];                            // alternate buffers: one barrier a round
+    if (lane == 0) {
+      rb[warp][0] = s.k; rb[warp][1] = s.p0; rb[warp][2] = s.p1; rb[warp][3] = s.mn; rb[warp][4] = s.mo;
+    }
+    __syncthreads();
+    s = {rb[0][0], rb[0][1], rb[0][2], rb[0][3], rb[0][4]};
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+      s.k += rb[w][0]; s.p0 += rb[w][1]; s.p1 += rb[w][2]; s.mn = fminf(s.mn, rb[w][3]);
+      s.mo = fmaxf(s.mo, rb[w][4]);
+    }
+    if (newton_round(s, kind, r, tau)) break;
   }
-  k = warp_sum_d(k); s1 = warp_sum_d(s1); s2 = warp_sum_d(s2);
-  mn = warp_min_d(mn); mo = warp_max_d(mo);
-  if (k <= 0.0) return false;
-  const double delta = kind == 2 ? (s1 - 1.0) / k
-                                 : (s1 - sqrt(fmax(s1 * s1 - k * (s2 - 1.0), 0.0))) / k;
-  if (!(delta < mn && delta >= mo)) return false;
-  *tau = t + delta;
-  return true;
+  return tau;
 }
 
-__global__ void __launch_bounds__(kTauThreads) entmax_tau_kernel(EntArgs a) {
-  extern __shared__ float s_a[];                          // (alpha - 1) z of the row
-  __shared__ float s_c[kTauCand];                         // the candidates, in row order
-  __shared__ double red[2][kTauWarps][4];
-  __shared__ float redf[kTauWarps];
-  __shared__ int redi[kTauWarps];
+// One warp sorts 256 values descending, 8 per lane in blocked order (lane l
+// holds entries 8 l .. 8 l + 7): the bitonic network, pairs (e, e ^ j) inside
+// a lane swapped in registers, across lanes exchanged by shuffle.
+__device__ __forceinline__ void warp_sort256_desc(float (&v)[8]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 256; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 8) {
+        const int lj = j >> 3;
+        const bool lower = (lane & lj) == 0;              // the smaller index of the pair
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float o = __shfl_xor_sync(kFull, v[i], lj);
+          const bool desc = ((lane * 8 + i) & k) == 0;
+          v[i] = (lower == desc) ? fmaxf(v[i], o) : fminf(v[i], o);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if ((i & j) == 0) {
+            const int ip = i | j;
+            const bool desc = ((lane * 8 + i) & k) == 0;
+            const float x = v[i], y = v[ip];
+            v[i] = desc ? fmaxf(x, y) : fminf(x, y);
+            v[ip] = desc ? fminf(x, y) : fmaxf(x, y);
+          }
+        }
+      }
+    }
+  }
+}
+
+// entries of the descending run r[0, n) that are >= x (ge) or > x (!ge)
+__device__ __forceinline__ int count_above(const float* r, int n, float x, bool ge) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const float y = r[mid];
+    if (ge ? (y >= x) : (y > x)) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// alpha 1.5 / 2, one warp: the candidates sorted descending in srt[0, m),
+// centred on their maximum (x' = a - a_max <= 0). With S1, S2 the sums of
+// x' and x'^2 over the k largest, the root of that support is
+//   alpha 2:   t_k = (S1 - 1) / k
+//   alpha 1.5: t_k = (S1 - sqrt(S1^2 - k S2 + k)) / k   (k t^2 - 2 t S1 + S2 - 1 = 0,
+//              the smaller root; both terms <= 0, so nothing cancels)
+// and the support is the largest k with t_k below its k-th value. Returns
+// that t_k (in the centred units); every lane returns it.
+__device__ float tau_sorted(const float* srt, int m, int kind) {
+  const int lane = threadIdx.x & 31;
+  const int per = (m + 31) >> 5;
+  const int j0 = min(m, lane * per), j1 = min(m, j0 + per);
+  float s1 = 0.f, s2 = 0.f;
+  for (int j = j0; j < j1; ++j) {
+    const float x = srt[j];
+    s1 += x;
+    s2 = fmaf(x, x, s2);
+  }
+  // exclusive prefix over the lanes
+  float e1 = s1, e2 = s2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y1 = __shfl_up_sync(kFull, e1, o), y2 = __shfl_up_sync(kFull, e2, o);
+    if (lane >= o) { e1 += y1; e2 += y2; }
+  }
+  e1 -= s1;
+  e2 -= s2;
+  int best = 0;
+  float tbest = 0.f;
+  for (int j = j0; j < j1; ++j) {
+    const float x = srt[j];
+    e1 += x;
+    e2 = fmaf(x, x, e2);
+    const float k = float(j + 1);
+    const float t = kind == 2 ? (e1 - 1.f) / k : (e1 - sqrtf(fmaxf(fmaf(e1, e1, k - k * e2), 0.f))) / k;
+    if (t < x) { best = j + 1; tbest = t; }
+  }
+  int kmax = best;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+  const unsigned who = __ballot_sync(kFull, best == kmax);
+  return __shfl_sync(kFull, tbest, __ffs(who) - 1);
+}
+
+// tau of one (request, query head). The CTA reads the row once into registers
+// (rows up to kThreads * kRowReg entries; longer rows are read again from L2)
+// for its maximum, gathers the entries above maximum - 1 per warp, and then,
+// for alpha 1.5 / 2, ranks them (a few: by counting; more: a sort per warp and
+// a merge of the runs by binary search) and takes the closed form of the
+// largest consistent support; generic alpha iterates Newton's method instead.
+__global__ void __launch_bounds__(kThreads) entmax_tau_kernel(EntArgs a) {
+  __shared__ float s_c[kWarps][kCand];
+  __shared__ float s_srt[kSortMax];
+  __shared__ int s_n[kWarps];
+  __shared__ float red[2][kWarps][5];
+  __shared__ float s_mx[kWarps];
   const int gq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();                                          // the weighted-V kernel may start its prologue
+  pdl_wait();                                             // the logits of this call are written
   int c = a.cnt[b * a.H_kv + gq / a.G];
   c = max(0, min(c, a.sel_stride));
   const int n = c << a.ps_shift;
   const float* z = a.logits + (int64_t(b) * a.H_q + gq) * a.logits_stride;
   const float am1 = a.alpha - 1.0f;
+  const bool in_reg = n <= kThreads * kRowReg;
+  float xr[kRowReg];
   float mx = -INFINITY;
-  for (int j = tid; j < n; j += kTauThreads) {
-    const float v = z[j];
-    const float x = (v > -INFINITY && v < INFINITY) ? am1 * v : -INFINITY;  // NaN / inf never enter
-    s_a[j] = x;
-    mx = fmaxf(mx, x);
-  }
+  if (in_reg) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-  if (lane == 0) redf[warp] = mx;
-  __syncthreads();
-  mx = redf[0];
-#pragma unroll
-  for (int w = 1; w < kTauWarps; ++w) mx = fmaxf(mx, redf[w]);
-  const int64_t row = int64_t(b) * a.H_q + gq;
-  if (!(mx > -INFINITY)) {
-    if (tid == 0) {
-      a.tau[row] = __int_as_float(0x7fc00000);
-      if (a.tau_out) a.tau_out[row] = __int_as_float(0x7fc00000);
-    }
-    return;
-  }
-  const int kind = alpha_kind(a.alpha);
-  const double r = 1.0 / double(am1);
-  // tau never drops below a_max - 1, so only a > a_max - 1 can be in the
-  // support: gather those (with a margin for the float rounding) in row order
-  const float lo = (mx - 1.0f) - 1e-6f * (1.0f + fabsf(mx));
-  const int per = (n + kTauThreads - 1) / kTauThreads;
-  const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
-  int mine = 0;
-  for (int j = j0; j < j1; ++j) mine += s_a[j] > lo;
-  int incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) redi[warp] = incl;
-  __syncthreads();
-  int off = incl - mine, m = 0;
-#pragma unroll
-  for (int w = 0; w < kTauWarps; ++w) {
-    if (w < warp) off += redi[w];
-    m += redi[w];
-  }
-  double tau;
-  if (m <= kTauCand) {
-    for (int j = j0; j < j1; ++j)
-      if (s_a[j] > lo) s_c[off++] = s_a[j];
-    __syncthreads();
-    if (warp != 0) return;
-    const float est = tau_estimate(s_c, m, mx - 1.0f, kind, float(r));
-    if (kind == 0 || !tau_exact_check(s_c, m, double(est), kind, &tau)) {
-      // generic alpha, or a support the float32 estimate got wrong: float64
-      // Newton from the left (from a_max - 1, or from just below the estimate
-      // when that is still left of the root)
-      const double t0 = fmax(double(mx) - 1.0, double(est) - 1e-3 * (1.0 + fabs(double(est))));
-      tau = solve_tau<false>(s_c, m, t0, double(mx) - 1.0, -INFINITY, kind, r, red);
+    for (int i = 0; i < kRowReg; ++i) {
+      const int j = i * kThreads + tid;
+      xr[i] = j < n ? a_of(__ldcg(z + j), am1) : -INFINITY;
+      mx = fmaxf(mx, xr[i]);
     }
   } else {
-    tau = solve_tau<true>(s_a, n, double(mx) - 1.0, double(mx) - 1.0, lo, kind, r, red);
+#pragma unroll 4
+    for (int j = tid; j < n; j += kThreads) mx = fmaxf(mx, a_of(__ldcg(z + j), am1));
+  }
+  mx = warp_max_f(mx);
+  if (lane == 0) s_mx[warp] = mx;
+  __syncthreads();
+  mx = s_mx[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, s_mx[w]);
+  const int64_t row = int64_t(b) * a.H_q + gq;
+  float tau = __int_as_float(0x7fc00000);                 // NaN: no finite logit
+  if (mx > -INFINITY) {
+    const int kind = alpha_kind(a.alpha);
+    const float r = 1.0f / am1;
+    // gather a > a_max - 1 (with a margin for the rounding of a_max - 1);
+    // warp w takes entries i * kThreads + 32 w + lane, i ascending
+    const float lo = (mx - 1.0f) - 1e-6f * (1.0f + fabsf(mx));
+    int got = 0;
+    auto gather = [&](float x) {
+      const bool take = x > lo;
+      const unsigned bal = __ballot_sync(kFull, take);
+      const int pos = got + __popc(bal & ((1u << lane) - 1u));
+      if (take && pos < kCand) s_c[warp][pos] = x;
+      got += __popc(bal);
+    };
+    if (in_reg) {
+#pragma unroll
+      for (int i = 0; i < kRowReg; ++i) gather(xr[i]);
+    } else {
+      for (int j0 = 0; j0 < n; j0 += kThreads) {
+        const int j = j0 + tid;
+        gather(j < n ? a_of(__ldcg(z + j), am1) : -INFINITY);
+      }
+    }
+    if (lane == 0) s_n[warp] = got;
+    __syncthreads();
+    int m = 0;
+    bool fits = true;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) { m += s_n[w]; fits &= s_n[w] <= kCand; }
+    if (!fits) {                                            // many near-equal logits
+      tau = solve_row(z, n, am1, mx - 1.0f, lo, kind, r, red);
+    } else if (kind == 0 || m > kSortMax) {
+      if (warp != 0) return;
+      tau = solve_gathered(s_c, s_n, mx - 1.0f, kind, r);
+    } else if (m > kRankDirect) {
+      // each warp sorts its own candidates, then an entry's rank is its place
+      // in its run plus the entries above it in the other runs (ties: runs
+      // in warp order), every rank distinct
+      {
+        float v[8];
+        const int nw = s_n[warp];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = lane * 8 + i;
+          v[i] = e < nw ? s_c[warp][e] : -INFINITY;
+        }
+        warp_sort256_desc(v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s_c[warp][lane * 8 + i] = v[i];
+      }
+      __syncthreads();
+      for (int ci = tid; ci < m; ci += kThreads) {
+        int w = 0, off = 0;
+        while (ci >= off + s_n[w]) off += s_n[w++];
+        const int l = ci - off;
+        const float x = s_c[w][l];
+        int rank = l;
+        for (int u = 0; u < kWarps; ++u)
+          if (u != w) rank += count_above(s_c[u], s_n[u], x, u < w);
+        s_srt[rank] = x - mx;
+      }
+      __syncthreads();
+      if (warp != 0) return;
+      tau = mx + tau_sorted(s_srt, m, kind);
+    } else {
+      // rank of each candidate among all: larger value first, ties by gather position
+      for (int ci = tid; ci < m; ci += kThreads) {
+        int w = 0, off = 0;
+        while (ci >= off + s_n[w]) off += s_n[w++];
+        const int gi = w * kCand + (ci - off);
+        const float x = s_c[w][ci - off];
+        int rank = 0;
+        for (int v = 0; v < kWarps; ++v) {
+          const int nv = s_n[v];
+          for (int jj = 0; jj < nv; ++jj) {
+            const float y = s_c[v][jj];
+            rank += (y > x) | ((y == x) & (v * kCand + jj < gi));
+          }
+        }
+        s_srt[rank] = x - mx;
+      }
+      __syncthreads();
+      if (warp != 0) return;
+      tau = mx + tau_sorted(s_srt, m, kind);
+    }
   }
   if (tid == 0) {
-    a.tau[row] = float(tau);
-    if (a.tau_out) a.tau_out[row] = float(tau);
+    a.tau[row] = tau;
+    if (a.tau_out) a.tau_out[row] = tau;
   }
 }
 
 template <typename T, int D, int kG>
-__global__ void __launch_bounds__(kPvThreads, 2) entmax_pv_kernel(EntArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
   using E = Elem<T>;
   constexpr int DPL = D / 32;                              // dims per lane: 4 (D 128) or 2 (D 64)
   constexpr int kU = kG > 8 ? 4 : 8;                       // V rows in flight per warp
   extern __shared__ float4 smem_f4[];
   float* s_red = reinterpret_cast<float*>(smem_f4);       // [warps][G][D], then [warps][G]
-  int2* s_ent = reinterpret_cast<int2*>(s_red + kPvWarps * a.G * (D + 1));
+  int2* s_ent = reinterpret_cast<int2*>(s_red + kWarps * a.G * (D + 1));
   __shared__ float s_tau[kG];
+  __shared__ float s_l[kG];
+  __shared__ int s_last;
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int G = a.G;
-  if (tid < G) s_tau[tid] = a.tau[int64_t(b) * a.H_q + h * G + tid];
+  // the selection and lengths come from before the logits pass: resolve the
+  // entries this CTA touches to (block, fill) before waiting for the thresholds
   int c = a.cnt[b * a.H_kv + h];
   c = max(0, min(c, a.sel_stride));
   const int n = c << a.ps_shift;
@@ -315,10 +448,9 @@ __global__ void __launch_bounds__(kPvThreads, 2) entmax_pv_kernel(EntArgs a) {
   const int n_pages_req = L > 0 ? (L + a.ps - 1) >> a.ps_shift : 0;
   const int32_t* sel = a.sel + int64_t(b * a.H_kv + h) * a.sel_stride;
   const int32_t* btb = a.bt + int64_t(b) * a.bt_stride;
-  // the selection entries this CTA touches, resolved to (block, fill) once
   const int e_lo = t_lo >> a.ps_shift;
   const int e_n = t_hi > t_lo ? min(((t_hi - 1) >> a.ps_shift) - e_lo + 1, a.ent_cap) : 0;
-  for (int i = tid; i < e_n; i += kPvThreads) {
+  for (int i = tid; i < e_n; i += kThreads) {
     const int page = sel[e_lo + i];
     int blk = -1, fill = 0;
     if (page >= 0 && page < n_pages_req && page < a.bt_stride) {
@@ -327,11 +459,15 @@ __global__ void __launch_bounds__(kPvThreads, 2) entmax_pv_kernel(EntArgs a) {
     }
     s_ent[i] = make_int2(blk, fill);
   }
+  pdl_wait();                                              // the thresholds are written
+  if (tid < G) s_tau[tid] = __ldcg(&a.tau[int64_t(b) * a.H_q + h * G + tid]);
   __syncthreads();
 
   const float am1 = a.alpha - 1.0f;
   const int kind = alpha_kind(a.alpha);
   const float r = 1.0f / am1;
+  const float* zb = a.logits + (int64_t(b) * a.H_q + int64_t(h) * G) * a.logits_stride;
+
   float acc[kG][DPL], psum[kG];
 #pragma unroll
   for (int g = 0; g < kG; ++g) {
@@ -339,9 +475,8 @@ __global__ void __launch_bounds__(kPvThreads, 2) entmax_pv_kernel(EntArgs a) {
 #pragma unroll
     for (int d = 0; d < DPL; ++d) acc[g][d] = 0.f;
   }
-  const float* zb = a.logits + (int64_t(b) * a.H_q + int64_t(h) * G) * a.logits_stride;
   const T* vbase = static_cast<const T*>(a.v);
-  for (int base = t_lo + warp * 32; base < t_hi; base += kPvWarps * 32) {
+  for (int base = t_lo + warp * 32; base < t_hi; base += kWarps * 32) {
     // p of token base + lane for every head of the group
     const int j = base + lane;
     float p[kG];
@@ -350,7 +485,7 @@ __global__ void __launch_bounds__(kPvThreads, 2) entmax_pv_kernel(EntArgs a) {
     for (int g = 0; g < kG; ++g) {
       p[g] = 0.f;
       if (g < G && j < t_hi) {
-        const float zz = zb[int64_t(g) * a.logits_stride + j];
+        const float zz = __ldcg(zb + int64_t(g) * a.logits_stride + j);
         const float x = am1 * zz - s_tau[g];
         if (zz > -INFINITY && zz < INFINITY && x > 0.f)
           p[g] = kind == 2 ? x : (kind == 1 ? x * x : powf(x, r));
@@ -416,38 +551,52 @@ __global__ void __launch_bounds__(kPvThreads, 2) entmax_pv_kernel(EntArgs a) {
     if (g < G) {
 #pragma unroll
       for (int d = 0; d < DPL; ++d) s_red[(warp * G + g) * D + lane * DPL + d] = acc[g][d];
-      if (lane == 0) s_red[kPvWarps * G * D + warp * G + g] = ps;
+      if (lane == 0) s_red[kWarps * G * D + warp * G + g] = ps;
     }
   }
   __syncthreads();
   const int64_t prow = (int64_t(b) * a.H_q + int64_t(h) * G) * a.nsplit;   // (b, head h*G, split 0)
-  for (int idx = tid; idx < G * D; idx += kPvThreads) {
+  for (int idx = tid; idx < G * D; idx += kThreads) {
     float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kPvWarps; ++w) sum += s_red[w * G * D + idx];
+    for (int w = 0; w < kWarps; ++w) sum += s_red[w * G * D + idx];
     const int g = idx / D, d = idx % D;
     a.part_o[((prow + int64_t(g) * a.nsplit) + split) * D + d] = sum;
   }
   if (tid < G) {
     float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kPvWarps; ++w) sum += s_red[kPvWarps * G * D + w * G + tid];
+    for (int w = 0; w < kWarps; ++w) sum += s_red[kWarps * G * D + w * G + tid];
     a.part_l[prow + int64_t(tid) * a.nsplit + split] = sum;
   }
-}
-
-template <typename T, int D>
-__global__ void __launch_bounds__(D) entmax_finish_kernel(EntArgs a) {
-  using E = Elem<T>;
-  const int gq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  const int64_t row = int64_t(b) * a.H_q + gq;
-  float o = 0.f, l = 0.f;
-  for (int s = 0; s < a.nsplit; ++s) {
-    o += a.part_o[(row * a.nsplit + s) * D + d];
-    l += a.part_l[row * a.nsplit + s];
+  // the last split of this (request, KV head) adds the partials in split order
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int done = atomicAdd(&a.tickets[b * a.H_kv + h], 1);
+    s_last = done == a.nsplit - 1;
   }
-  const float y = l > 0.f ? o / l : 0.f;                   // no kept token: 0
-  reinterpret_cast<uint16_t*>(a.out)[row * D + d] = E::from_f(y);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid < G) {
+    float l = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < a.nsplit; ++s) l += __ldcg(&a.part_l[prow + int64_t(tid) * a.nsplit + s]);
+    s_l[tid] = l;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * D; idx += kThreads) {
+    const int g = idx / D, d = idx % D;
+    const float* src = a.part_o + (prow + int64_t(g) * a.nsplit) * D + d;
+    float o = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < a.nsplit; ++s) o += __ldcg(src + int64_t(s) * D);
+    const float l = s_l[g];
+    const float y = l > 0.f ? o / l : 0.f;                 // no kept token: 0
+    reinterpret_cast<uint16_t*>(a.out)[(int64_t(b) * a.H_q + int64_t(h) * G + g) * D + d] = E::from_f(y);
+  }
+  if (tid == 0) a.tickets[b * a.H_kv + h] = 0;             // ready for the next call
 }
 
 int device_sms() {
@@ -465,18 +614,18 @@ int device_sms() {
 
 struct EntLayout {
   int nsplit, ent_cap;
-  size_t logits, tau, part_o, part_l, total;
+  size_t logits, tau, part_o, part_l, tickets, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// splits: about two CTAs per SM over all (request, KV head) units, at least
-// 128 tokens a split
+// splits: as many as fit two CTAs per SM in one wave over all (request, KV
+// head) units, at least 128 tokens a split
 EntLayout ent_layout(int B, int H_kv, int H_q, int D, int ps, int sel_stride, int sms) {
   EntLayout w;
   const int64_t rows = int64_t(sel_stride) * ps;
   const int units = B * H_kv;
-  int ns = (2 * sms + units - 1) / units;
+  int ns = (2 * sms) / units;
   const int64_t by_len = (rows + 127) / 128;
   if (ns > by_len) ns = int(by_len);
   if (ns > 64) ns = 64;
@@ -485,32 +634,33 @@ EntLayout ent_layout(int B, int H_kv, int H_q, int D, int ps, int sel_stride, in
   const int64_t per = (((rows + ns - 1) / ns) + 31) & ~int64_t(31);
   w.ent_cap = int(per / ps + 2);
   size_t off = 0;
-  w.logits = off; off = align256(off + size_t(B) * H_q * rows * sizeof(float));
-  w.tau = off;    off = align256(off + size_t(B) * H_q * sizeof(float));
-  w.part_o = off; off = align256(off + size_t(B) * H_q * ns * D * sizeof(float));
-  w.part_l = off; off = align256(off + size_t(B) * H_q * ns * sizeof(float));
+  w.logits = off;  off = align256(off + size_t(B) * H_q * rows * sizeof(float));
+  w.tau = off;     off = align256(off + size_t(B) * H_q * sizeof(float));
+  w.part_o = off;  off = align256(off + size_t(B) * H_q * ns * D * sizeof(float));
+  w.part_l = off;  off = align256(off + size_t(B) * H_q * ns * sizeof(float));
+  w.tickets = off; off = align256(off + size_t(B) * H_kv * sizeof(int32_t));
   w.total = off;
   return w;
 }
 
-int g_tau_smem[64];
-int g_pv_smem[12][64];
+int g_att_smem[12][64];
 
 template <typename T, int D, int kG>
-sa_status launch_pv(const EntArgs& a, dim3 grid, cudaStream_t s, int* attr) {
-  const int smem = (kPvWarps * a.G * (D + 1)) * int(sizeof(float)) + a.ent_cap * int(sizeof(int2));
-  if (!ensure_smem(entmax_pv_kernel<T, D, kG>, smem, attr)) return SA_ERR_CUDA;
-  entmax_pv_kernel<T, D, kG><<<grid, kPvThreads, smem, s>>>(a);
-  if (launch_status() != SA_OK) return SA_ERR_CUDA;
-  entmax_finish_kernel<T, D><<<dim3(unsigned(a.H_q), grid.z), D, 0, s>>>(a);
-  return launch_status();
+sa_status launch_attend(const EntArgs& a, dim3 grid, cudaStream_t s, int* attr) {
+  const int smem = kWarps * a.G * (D + 1) * int(sizeof(float)) + a.ent_cap * int(sizeof(int2));
+  if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  if (!ensure_smem(entmax_attend_kernel<T, D, kG>, smem, attr)) return SA_ERR_CUDA;
+  return launch_ex(entmax_attend_kernel<T, D, kG>, grid, dim3(kThreads), size_t(smem), s, true, 1u,
+                   a) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
 }
 
 template <typename T, int D>
-sa_status launch_pv_g(const EntArgs& a, dim3 grid, cudaStream_t s, int slot) {
-  if (a.G <= 4) return launch_pv<T, D, 4>(a, grid, s, g_pv_smem[slot * 3 + 0]);
-  if (a.G <= 8) return launch_pv<T, D, 8>(a, grid, s, g_pv_smem[slot * 3 + 1]);
-  return launch_pv<T, D, 16>(a, grid, s, g_pv_smem[slot * 3 + 2]);
+sa_status launch_attend_g(const EntArgs& a, dim3 grid, cudaStream_t s, int slot) {
+  if (a.G <= 4) return launch_attend<T, D, 4>(a, grid, s, g_att_smem[slot * 3 + 0]);
+  if (a.G <= 8) return launch_attend<T, D, 8>(a, grid, s, g_att_smem[slot * 3 + 1]);
+  return launch_attend<T, D, 16>(a, grid, s, g_att_smem[slot * 3 + 2]);
 }
 
 }  // namespace
@@ -543,14 +693,20 @@ extern "C" sa_status sa_sparse_decode_entmax(const sa_cache* cache, const sa_bat
   const int G = num_q_heads / cache->num_kv_heads;
   if (G > 16) return SA_ERR_UNSUPPORTED;
   const int64_t rows = int64_t(sel_stride) * cache->page_size;
-  if (rows * int64_t(sizeof(float)) > 160 * 1024) return SA_ERR_UNSUPPORTED;   // a row of a in shared memory
+  if (rows > (int64_t(1) << 24)) return SA_ERR_UNSUPPORTED;
   if (logits && logits_stride < rows) return SA_ERR_INVALID_ARG;
   const EntLayout w = ent_layout(batch->batch, cache->num_kv_heads, num_q_heads, cache->head_dim,
                                  cache->page_size, sel_stride, device_sms());
   if (!workspace || workspace_bytes < w.total) return SA_ERR_WORKSPACE;
+  const int kmax = G <= 4 ? 4 : (G <= 8 ? 8 : 16);
+  const int64_t smem = int64_t(kWarps) * G * (cache->head_dim + 1) * 4 + int64_t(w.ent_cap) * 8;
+  if (smem > 227 * 1024 || kmax < G) return SA_ERR_UNSUPPORTED;   // (checked before any launch)
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* lg = logits ? logits : reinterpret_cast<float*>(ws + w.logits);
   const int lg_stride = logits ? logits_stride : int(rows);
+  // the split counters start at zero (a zero-filled workspace); each call's
+  // last CTA per (request, KV head) leaves its counter at zero again
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   // (1) the logits of every selected token (K only)
   st = decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, nullptr, lg,
                    lg_stride, nullptr, 0, dev_status, stream, /*allow_cluster=*/false, /*pdl=*/false,
@@ -560,21 +716,20 @@ extern "C" sa_status sa_sparse_decode_entmax(const sa_cache* cache, const sa_bat
   a.v = cache->v; a.bt = batch->block_table; a.seq_lens = batch->seq_lens; a.sel = sel_idx;
   a.cnt = sel_cnt; a.logits = lg; a.tau = reinterpret_cast<float*>(ws + w.tau); a.tau_out = tau;
   a.part_o = reinterpret_cast<float*>(ws + w.part_o); a.part_l = reinterpret_cast<float*>(ws + w.part_l);
+  a.tickets = reinterpret_cast<int32_t*>(ws + w.tickets);
   a.out = out; a.status = dev_status;
   a.H_kv = cache->num_kv_heads; a.H_q = num_q_heads; a.G = G; a.ps = cache->page_size;
   a.ps_shift = log2i(cache->page_size); a.num_blocks = cache->num_blocks;
   a.bt_stride = batch->bt_stride; a.sel_stride = sel_stride; a.logits_stride = lg_stride;
   a.nsplit = w.nsplit; a.ent_cap = w.ent_cap; a.alpha = alpha;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   // (2) tau per (request, query head)
-  const int tsmem = int(rows * sizeof(float));
-  if (!ensure_smem(entmax_tau_kernel, tsmem, g_tau_smem)) return SA_ERR_CUDA;
-  entmax_tau_kernel<<<dim3(unsigned(num_q_heads), unsigned(batch->batch)), kTauThreads, tsmem, s>>>(a);
-  if ((st = launch_status()) != SA_OK) return st;
-  // (3) the kept tokens' sum_j p_j v_j per split, (4) the splits added and normalised
+  if (launch_ex(entmax_tau_kernel, dim3(unsigned(num_q_heads), unsigned(batch->batch)), dim3(kThreads),
+                0, s, true, 1u, a) != cudaSuccess)
+    return SA_ERR_CUDA;
+  // (3) the kept tokens' sum_j p_j v_j per split, the last split normalising
   const dim3 grid(unsigned(w.nsplit), unsigned(cache->num_kv_heads), unsigned(batch->batch));
   const bool bf = cache->dtype == SA_BF16;
   if (cache->head_dim == 128)
-    return bf ? launch_pv_g<__nv_bfloat16, 128>(a, grid, s, 0) : launch_pv_g<__half, 128>(a, grid, s, 1);
-  return bf ? launch_pv_g<__nv_bfloat16, 64>(a, grid, s, 2) : launch_pv_g<__half, 64>(a, grid, s, 3);
+    return bf ? launch_attend_g<__nv_bfloat16, 128>(a, grid, s, 0) : launch_attend_g<__half, 128>(a, grid, s, 1);
+  return bf ? launch_attend_g<__nv_bfloat16, 64>(a, grid, s, 2) : launch_attend_g<__half, 64>(a, grid, s, 3);
 }

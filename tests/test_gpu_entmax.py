@@ -172,6 +172,34 @@ def test_support_of_one_returns_the_value_row_exactly():
     assert checked >= c.B * c.H_q // 2, checked
 
 
+def test_counters_return_to_zero_and_repeat_calls_agree():
+    """The split counters are back at zero after every call, and a call on the
+    same inputs gives the same bits."""
+    from sparse_paged_kv_page_gb300 import sa_sparse_decode_entmax, alloc_entmax_workspace
+    wl = make_workload(config(5, small=True))
+    dec = make_decoder(wl)
+    c = wl.cfg
+    sel, cnt = _selection(wl, np.random.default_rng(6), c.topk)
+    q = dev_bits(wl.q(0), c.dtype)
+    ws = alloc_entmax_workspace(c.B, c.H_kv, c.H_q, c.D, c.ps, c.topk)
+    sel_t = torch.from_numpy(sel.astype(np.int32)).cuda()
+    cnt_t = torch.from_numpy(cnt.astype(np.int32)).cuda()
+    outs = []
+    for _ in range(3):
+        out = torch.empty((c.B, c.H_q, c.D), dtype=dec.dtype, device="cuda")
+        sa_sparse_decode_entmax(dec.cache.struct, dec.batch, q, c.H_q, sel_t, cnt_t, c.topk, 1.5,
+                                dec.scale, out, workspace=ws, dev_status=dec.dev_status)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert all(torch.equal(outs[0].view(torch.int16), o.view(torch.int16)) for o in outs[1:])
+    # the counters are the workspace's last region
+    from sparse_paged_kv_page_gb300 import sa_entmax_workspace_size
+    n = sa_entmax_workspace_size(c.B, c.H_kv, c.H_q, c.D, c.ps, c.topk)
+    tail = -(-(c.B * c.H_kv * 4) // 256) * 256
+    assert int(ws[n - tail:n].to(torch.int32).sum().item()) == 0
+    assert dev_status(dec) == 0
+
+
 def test_empty_selection_gives_zero_and_nan():
     wl = make_workload(config(1, small=True))
     dec = make_decoder(wl)
@@ -193,7 +221,7 @@ def test_entmax_rejects_before_launching():
     cnt = torch.ones((c.B, c.H_kv), dtype=torch.int32, device="cuda")
     out = torch.full((c.B, c.H_q, c.D), 7.0, dtype=dec.dtype, device="cuda")
     q = dev_bits(wl.q(0), c.dtype)
-    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")          # zero-filled, as required
     for alpha, st in ((1.0, 1), (2.5, 1), (float("nan"), 1)):
         with pytest.raises(SaError) as e:
             sa_sparse_decode_entmax(dec.cache.struct, dec.batch, q, c.H_q, sel, cnt, 4, alpha,
@@ -230,5 +258,25 @@ def test_many_candidates_take_the_block_solver(alpha):
             for h in range(c.H_kv):
                 n = len(O.selected_positions(sel[b, h, :cnt[b, h]], L, c.ps))
                 want = -1.0 / n if alpha == 2.0 else -1.0 / np.sqrt(n)
-                assert np.allclose(t_np[b, h * c.G:(h + 1) * c.G], want, rtol=1e-6, atol=0)
+                assert np.allclose(t_np[b, h * c.G:(h + 1) * c.G], want, rtol=1e-5, atol=0)
+    assert dev_status(dec) == 0
+
+
+@pytest.mark.parametrize("alpha,spread", [(1.5, 0.75), (2.0, 0.38), (1.5, 1.0)])
+def test_hundreds_of_candidates_sorted_and_merged(alpha, spread):
+    """Logits spread so that a few hundred entries of each row lie within
+    1 / (alpha - 1) of the top one: the threshold kernel sorts per warp and
+    merges; the result must still match the oracle."""
+    cfg = config(3, small=True).replace(len_range=(2600, 3000), topk=170)
+    wl = make_workload(cfg)
+    dec = make_decoder(wl)
+    c = wl.cfg
+    sel, cnt = _selection(wl, np.random.default_rng(9), c.topk)
+    qb = wl.q(0)
+    scale = spread * c.D ** -0.5
+    out, tau, lg = _run(dec, dev_bits(qb, c.dtype), sel, cnt, c.topk, alpha, scale=scale)
+    z = lg.cpu().numpy()
+    m = (np.isfinite(z) & ((alpha - 1) * z > (alpha - 1) * np.nanmax(np.where(np.isfinite(z), z, -np.inf), -1, keepdims=True) - 1)).sum(-1)
+    assert np.median(m) > 64 and m.max() <= 2048, (np.median(m), m.max())
+    _check(wl, qb, sel, cnt, out, tau, lg, alpha, scale)
     assert dev_status(dec) == 0
