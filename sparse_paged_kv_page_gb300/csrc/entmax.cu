@@ -38,7 +38,7 @@ constexpr int kCand = 256;               // candidates each warp of the tau kern
 constexpr int kMaxIter = 100;
 constexpr int kRowReg = 16;              // row entries per thread the tau kernel keeps in registers
 constexpr int kSortMax = kWarps * kCand; // every gathered candidate can be ranked
-constexpr int kRankDirect = 64;          // up to this many candidates: rank by direct counting
+constexpr int kRankDirect = 128;         // up to this many candidates: rank by direct counting
 static_assert(kCand == 256, "the per-warp sort holds 8 candidates a lane");
 
 struct EntArgs {
@@ -200,35 +200,39 @@ __device__ float solve_row(const float* z, int n, float am1, float tau, float sk
 
 // One warp sorts 256 values descending, 8 per lane in blocked order (lane l
 // holds entries 8 l .. 8 l + 7): the bitonic network, pairs (e, e ^ j) inside
-// a lane swapped in registers, across lanes exchanged by shuffle.
-__device__ __forceinline__ void warp_sort256_desc(float (&v)[8]) {
+// a lane swapped in registers, across lanes exchanged by shuffle. The stage
+// loops stay rolled: the code runs once per CTA, so its size is its cost.
+template <int J>
+__device__ __forceinline__ void bitonic_in_lane(float (&v)[8], int lane, int k) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if ((i & J) == 0) {
+      const bool desc = ((lane * 8 + i) & k) == 0;
+      const float x = v[i], y = v[i | J];
+      v[i] = desc ? fmaxf(x, y) : fminf(x, y);
+      v[i | J] = desc ? fminf(x, y) : fmaxf(x, y);
+    }
+  }
+}
+
+__device__ void warp_sort256_desc(float (&v)[8]) {
   const int lane = threadIdx.x & 31;
-#pragma unroll
+#pragma unroll 1
   for (int k = 2; k <= 256; k <<= 1) {
+#pragma unroll 1
+    for (int j = k >> 1; j >= 8; j >>= 1) {
+      const int lj = j >> 3;
+      const bool lower = (lane & lj) == 0;                  // the smaller index of the pair
 #pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j >= 8) {
-        const int lj = j >> 3;
-        const bool lower = (lane & lj) == 0;              // the smaller index of the pair
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float o = __shfl_xor_sync(kFull, v[i], lj);
-          const bool desc = ((lane * 8 + i) & k) == 0;
-          v[i] = (lower == desc) ? fmaxf(v[i], o) : fminf(v[i], o);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if ((i & j) == 0) {
-            const int ip = i | j;
-            const bool desc = ((lane * 8 + i) & k) == 0;
-            const float x = v[i], y = v[ip];
-            v[i] = desc ? fmaxf(x, y) : fminf(x, y);
-            v[ip] = desc ? fminf(x, y) : fmaxf(x, y);
-          }
-        }
+      for (int i = 0; i < 8; ++i) {
+        const float o = __shfl_xor_sync(kFull, v[i], lj);
+        const bool desc = ((lane * 8 + i) & k) == 0;
+        v[i] = (lower == desc) ? fmaxf(v[i], o) : fminf(v[i], o);
       }
     }
+    if (k >= 8) bitonic_in_lane<4>(v, lane, k);
+    if (k >= 4) bitonic_in_lane<2>(v, lane, k);
+    bitonic_in_lane<1>(v, lane, k);
   }
 }
 
