@@ -23,7 +23,8 @@ Sources, cited by page title and section:
 * [vllmcpp] "test_ops_mla_chunked_context.cpp", vllm.cpp tests -- the
             double-precision single-shot attention oracle and the
             "MergeAttnStates" LSE edge-case test.
-* [entmax]  "EntmaxKV" README -- sections "How it works" (top-k strategy).
+* [entmax]  "EntmaxKV" README -- sections "How it works" (top-k and
+            Gaussian-aware strategies), "Quick start".
 
 Readings taken where the pages are silent (each restated where it is used):
 
@@ -315,6 +316,158 @@ def attention_entmax(q, k, v, scale: float, alpha: float):
         tau[g] = entmax_threshold(z[g], alpha)
         o[g] = entmax(z[g], alpha) @ v
     return o, tau, z
+
+
+# ---------------------------------------------------------------------------
+# N4: Gaussian-aware selection
+# ---------------------------------------------------------------------------
+def page_std(k_tok: np.ndarray, dtype: str) -> np.ndarray:
+    """Element-wise k_std of the f >= 1 valid keys of one page.
+
+    [entmax] "How it works" (mean / std per page for the Gaussian strategy)
+    and its k_mean / k_std refresh: the population standard deviation
+    sqrt((1/f) sum (k - mean)^2) around the exact mean, rounded once to the
+    cache dtype (stored like k_mean). k_tok: float64 [f, D].
+    """
+    mean = k_tok.mean(0)
+    return round_to_kdt(np.sqrt(((k_tok - mean) ** 2).mean(0)), dtype)
+
+
+def head_gauss_stats(k_head_bits, L: int, ps: int, dtype: str):
+    """k_mean, k_std and the fill of every page of one (request, KV head).
+
+    k_head_bits: uint16 [L, D]. Returns float64 [n, D], [n, D], int [n]."""
+    k = decode_kdt(k_head_bits[:L], dtype)
+    n = num_pages(L, ps)
+    me, sd = np.empty((n, k.shape[1])), np.empty((n, k.shape[1]))
+    fill = np.empty(n, dtype=np.int64)
+    for p in range(n):
+        rows = k[p * ps:min((p + 1) * ps, L)]
+        me[p] = round_to_kdt(rows.sum(0) / rows.shape[0], dtype)
+        sd[p] = page_std(rows, dtype)
+        fill[p] = rows.shape[0]
+    return me, sd, fill
+
+
+def gauss_page_moments(q, k_mean, k_std, scale: float):
+    """Query-conditioned moments of a page's scores z = scale * q . k.
+
+    [entmax] "How it works" (each page's scores modelled as a Gaussian) and
+    its query-conditioned page moments: with the key dimensions of a page
+    taken as independent (the statistics are per dimension),
+      m_p = scale * sum_d q_d mean_pd,   v_p = scale^2 * sum_d q_d^2 std_pd^2.
+    q: [D] (one query head); k_mean, k_std: [n, D]. Returns m, v [n].
+    """
+    q = np.asarray(q, np.float64)
+    return scale * (k_mean @ q), scale * scale * ((k_std ** 2) @ (q * q))
+
+
+def gauss_global_moments(m, v, fill):
+    """Mean and variance of all N = sum f_p scores of the page mixture
+    (page p holds f_p scores of mean m_p and variance v_p):
+    M = sum f m / N, V = sum f (v + m^2) / N - M^2. The single-Gaussian model
+    ([entmax] How it works: heads without ALiBi) is N(M, V)."""
+    f = np.asarray(fill, np.float64)
+    N = f.sum()
+    M = (f * m).sum() / N
+    V = max((f * (v + m * m)).sum() / N - M * M, 0.0)
+    return N, M, V
+
+
+def _phi(u):
+    return math.exp(-0.5 * u * u) / math.sqrt(2.0 * math.pi)
+
+
+def _Phi(u):
+    return 0.5 * math.erfc(-u / math.sqrt(2.0))
+
+
+def gauss_tail_moment(mu: float, sigma: float, t: float, alpha: float) -> float:
+    """E[((alpha - 1) Z - t)_+ ^ (1 / (alpha - 1))] for Z ~ N(mu, sigma^2),
+    alpha in {1.5, 2}: with a = (alpha - 1) Z ~ N(mu_a, s_a^2), c = mu_a - t
+    and u = c / s_a, the truncated moments of the normal give
+      alpha 2:   c Phi(u) + s_a phi(u)
+      alpha 1.5: (c^2 + s_a^2) Phi(u) + c s_a phi(u)
+    and ((c)_+)^r when sigma = 0."""
+    if alpha not in (1.5, 2.0):
+        raise ValueError("closed forms for alpha 1.5 and 2 only")
+    mu_a, s_a = (alpha - 1.0) * mu, (alpha - 1.0) * sigma
+    c = mu_a - t
+    if s_a == 0.0:
+        return max(c, 0.0) ** (1.0 / (alpha - 1.0))
+    u = c / s_a
+    if alpha == 2.0:
+        return c * _Phi(u) + s_a * _phi(u)
+    return (c * c + s_a * s_a) * _Phi(u) + c * s_a * _phi(u)
+
+
+def gauss_tau(N: float, M: float, V: float, alpha: float) -> float:
+    """tau_hat of the distributional entmax constraint ([entmax] How it works):
+    N scores drawn from N(M, V) should carry unit entmax mass,
+    N * E[((alpha - 1) Z - tau)_+ ^ (1 / (alpha - 1))] = 1. The left side
+    decreases strictly in tau (while positive); bisection on a bracket whose
+    ends are checked."""
+    sd = math.sqrt(V)
+    lo = (alpha - 1.0) * (M + 10.0 * sd) - 1.0
+    while N * gauss_tail_moment(M, sd, lo, alpha) < 1.0:
+        lo -= 1.0 + abs(lo)
+    hi = (alpha - 1.0) * (M + 12.0 * sd) + 1.0
+    while N * gauss_tail_moment(M, sd, hi, alpha) > 1.0:
+        hi += 1.0 + abs(hi)
+    for _ in range(200):
+        mid = 0.5 * (lo + hi)
+        if N * gauss_tail_moment(M, sd, mid, alpha) >= 1.0:
+            lo = mid
+        else:
+            hi = mid
+    return 0.5 * (lo + hi)
+
+
+def gauss_max_factor(f: int) -> float:
+    """kappa_f with E[max of f scores] <= m + kappa_f sqrt(v) for f scores of
+    mean m and variance v that are jointly Gaussian (any correlation):
+    sqrt(2 ln f); 0 for a single token. The pages select every page whose
+    estimated maximum can cross tau_hat; this bound is the estimate taken."""
+    return math.sqrt(2.0 * math.log(f)) if f > 1 else 0.0
+
+
+def gauss_select(m, v, fill, tau_hat: float, alpha: float) -> np.ndarray:
+    """Pages p with (alpha - 1) * (m_p + kappa_{f_p} sqrt(v_p)) > tau_hat, and
+    the tail page always ([entmax] How it works, Top-k: the tail is attended);
+    ascending. The count adapts to the distribution; no budget."""
+    n = len(m)
+    if n == 0:
+        return np.zeros(0, dtype=np.int64)
+    est = np.array([m[p] + gauss_max_factor(int(fill[p])) * math.sqrt(v[p]) for p in range(n)])
+    keep = (alpha - 1.0) * est > tau_hat
+    keep[n - 1] = True
+    return np.nonzero(keep)[0].astype(np.int64)
+
+
+def gauss_decode_unit(k_head_bits, v_head_bits, L: int, q_bits, *, ps: int, alpha: float,
+                      dtype: str, scale: float = 0.0):
+    """N4 for one query head of one request: page k_mean / k_std, the page
+    moments of this head's scores, tau_hat of the single Gaussian, threshold
+    selection (+ tail), then alpha-entmax attention over the selected pages'
+    valid tokens with the exact tau of that selection (the "corrected" tau).
+
+    k_head_bits, v_head_bits: uint16 [L, D] of the head's KV head; q_bits:
+    uint16 [D]. Returns dict(mean, std, fill, m, v, N, M, V, tau_hat, sel,
+    out [D], tau)."""
+    D = k_head_bits.shape[1]
+    sc = scale if scale > 0 else default_scale(D)
+    q = decode_kdt(q_bits, dtype)
+    me, sd, fill = head_gauss_stats(k_head_bits, L, ps, dtype)
+    m, v = gauss_page_moments(q, me, sd, sc)
+    N, M, V = gauss_global_moments(m, v, fill)
+    th = gauss_tau(N, M, V, alpha)
+    sel = gauss_select(m, v, fill, th, alpha)
+    pos = selected_positions(sel, L, ps)
+    k = decode_kdt(k_head_bits[pos], dtype)
+    vv = decode_kdt(v_head_bits[pos], dtype)
+    o, tau, _ = attention_entmax(q[None, :], k, vv, sc, alpha)
+    return {"mean": me, "std": sd, "fill": fill, "m": m, "v": v, "N": N, "M": M, "V": V,
+            "tau_hat": th, "sel": sel, "out": o[0], "tau": float(tau[0])}
 
 
 # ---------------------------------------------------------------------------

@@ -707,3 +707,118 @@ def test_page_decode_unit_entmax_with_every_page_is_dense_entmax():
         assert np.all(r["out"] <= v.max(0) + 1e-12) and np.all(r["out"] >= v.min(0) - 1e-12)
     r1 = O.page_decode_unit(kb, vb, L, qb, ps=ps, topk=99, w_avg=1.0, w_peak=0.25, dtype="bf16")
     assert "lse" in r1
+
+
+# ---------------------------------------------------------------------------
+# N4 Gaussian-aware selection
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_gauss_tail_moment_matches_quadrature(alpha):
+    """The truncated-normal closed forms against numerical integration of the
+    defining expectation E[((alpha - 1) Z - t)_+^(1/(alpha - 1))]."""
+    from scipy import integrate
+    r = 1.0 / (alpha - 1.0)
+    for mu, sd, t in [(0.0, 1.0, 0.3), (0.7, 0.4, 0.1), (-1.2, 2.5, -0.4), (2.0, 0.3, 1.6),
+                      (0.0, 1.0, 2.5)]:
+        f = lambda z: max((alpha - 1.0) * z - t, 0.0) ** r * math.exp(-0.5 * ((z - mu) / sd) ** 2) / (sd * math.sqrt(2 * math.pi))
+        lo = t / (alpha - 1.0)
+        want = integrate.quad(f, lo, mu + 40 * sd, epsabs=1e-14, epsrel=1e-12, limit=200)[0]
+        got = O.gauss_tail_moment(mu, sd, t, alpha)
+        assert abs(got - want) <= 1e-9 * max(1.0, abs(want)), (mu, sd, t, got, want)
+    # no spread: the moment of a point mass
+    assert O.gauss_tail_moment(0.9, 0.0, 0.1, alpha) == pytest.approx(((alpha - 1) * 0.9 - 0.1) ** r)
+    assert O.gauss_tail_moment(0.1, 0.0, 0.5, alpha) == 0.0
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_gauss_tau_point_mass_and_sample_entmax(alpha):
+    # V = 0: N equal scores share the mass, N ((alpha-1) M - tau)^r = 1
+    for N, M in [(16, 0.4), (4096, -1.3), (1, 2.0)]:
+        want = (alpha - 1.0) * M - N ** (-(alpha - 1.0))
+        assert O.gauss_tau(N, M, 0.0, alpha) == pytest.approx(want, abs=1e-12)
+    # a large Gaussian sample: the exact entmax threshold of the sample,
+    # averaged over draws, agrees with the distributional tau_hat within its
+    # standard error
+    rng = np.random.default_rng(31)
+    N, M, sd, reps = 5000, 0.3, 0.8, 40
+    ts = [O.entmax_threshold(M + sd * rng.standard_normal(N), alpha) for _ in range(reps)]
+    se = np.std(ts) / math.sqrt(reps)
+    assert abs(np.mean(ts) - O.gauss_tau(N, M, sd * sd, alpha)) <= 4 * se
+    # more scores push the threshold up
+    assert O.gauss_tau(2 * N, M, sd * sd, alpha) > O.gauss_tau(N, M, sd * sd, alpha)
+
+
+def _hadamard(n):
+    h = np.array([[1.0]])
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def test_gauss_page_moments_exact_on_uncorrelated_pages():
+    """Pages whose keys are mean + std * (rows of a Hadamard matrix without
+    its constant column): per-dimension mean and population std are exactly
+    mean and std, the dimensions are exactly uncorrelated, so the diagonal
+    model's page moments are exactly the empirical mean and variance of the
+    page's scores, and the mixture moments those of all scores."""
+    H = _hadamard(16)[:, 1:]                          # 16 tokens x 15 dims, zero-mean orthogonal columns
+    rng = np.random.default_rng(5)
+    scale = 0.125
+    q = rng.integers(-8, 9, size=15) / 8.0
+    pages, ms, vs = [], [], []
+    for p in range(5):
+        mean = rng.integers(-16, 17, size=15) / 16.0
+        std = rng.integers(1, 9, size=15) / 8.0
+        keys = mean + std * H                          # exactly representable in bf16
+        assert np.array_equal(O.round_to_kdt(keys, "bf16"), keys)
+        got_std = O.page_std(keys, "bf16")
+        assert np.array_equal(got_std, std) and np.array_equal(keys.mean(0), mean)
+        m, v = O.gauss_page_moments(q, mean[None], got_std[None], scale)
+        z = scale * keys @ q
+        assert m[0] == pytest.approx(z.mean(), rel=1e-12, abs=1e-12)
+        assert v[0] == pytest.approx(z.var(), rel=1e-12)
+        pages.append(z); ms.append(m[0]); vs.append(v[0])
+    N, M, V = O.gauss_global_moments(np.array(ms), np.array(vs), np.full(5, 16))
+    allz = np.concatenate(pages)
+    assert N == 80 and M == pytest.approx(allz.mean(), abs=1e-12) and V == pytest.approx(allz.var(), rel=1e-12)
+
+
+def test_gauss_max_factor_bounds_the_expected_maximum():
+    # E[max of 2 standard normals] = 1 / sqrt(pi); Monte Carlo for larger f
+    assert 1.0 / math.sqrt(math.pi) <= O.gauss_max_factor(2)
+    rng = np.random.default_rng(2)
+    for f in (3, 8, 16):
+        emax = rng.standard_normal((200000, f)).max(1).mean()
+        assert emax <= O.gauss_max_factor(f)
+    assert O.gauss_max_factor(1) == 0.0
+
+
+def test_gauss_select_rule():
+    m = np.array([0.0, 3.0, -1.0, 0.5, 0.0])
+    v = np.array([1.0, 0.0, 0.0, 4.0, 0.0])
+    fill = np.array([16, 16, 1, 16, 3])
+    # (alpha - 1) * (m + sqrt(2 ln f) sqrt(v)) against tau_hat, tail always
+    est = [0 + math.sqrt(2 * math.log(16)), 3.0, -1.0, 0.5 + 2 * math.sqrt(2 * math.log(16)), 0.0]
+    for alpha, th in [(2.0, 2.9), (1.5, 1.49), (2.0, 100.0), (2.0, -5.0)]:
+        want = [p for p in range(5) if (alpha - 1) * est[p] > th or p == 4]
+        assert O.gauss_select(m, v, fill, th, alpha).tolist() == want
+    # a higher threshold keeps a subset
+    a = set(O.gauss_select(m, v, fill, 0.5, 2.0).tolist())
+    b = set(O.gauss_select(m, v, fill, 2.0, 2.0).tolist())
+    assert b <= a
+
+
+def test_gauss_decode_unit_one_page_is_dense_entmax():
+    """A request of one page selects it (the tail): the unit is entmax
+    attention over every token, with the exact tau of that selection."""
+    rng = np.random.default_rng(12)
+    L, D = 13, 32
+    kb = O.encode_kdt(rng.standard_normal((L, D)), "bf16")
+    vb = O.encode_kdt(rng.standard_normal((L, D)), "bf16")
+    qb = O.encode_kdt(rng.standard_normal(D), "bf16")
+    for alpha in (1.5, 2.0):
+        r = O.gauss_decode_unit(kb, vb, L, qb, ps=16, alpha=alpha, dtype="bf16")
+        k, v, q = (O.decode_kdt(x, "bf16") for x in (kb, vb, qb))
+        o, tau, _ = O.attention_entmax(q[None], k, v, D ** -0.5, alpha)
+        assert r["sel"].tolist() == [0]
+        assert np.array_equal(r["out"], o[0]) and r["tau"] == tau[0]
