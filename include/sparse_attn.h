@@ -20,8 +20,9 @@
  *                     scores, selection and attention per query head
  *   sa_h2o_prefill    H2O absorb / eviction of appended tokens with the new key
  *                     as the query (prefill side)
- *   sa_sparse_decode_entmax, sa_entmax_workspace_size
+ *   sa_sparse_decode_entmax, sa_sparse_decode_entmax_qh, sa_entmax_workspace_size
  *                     attention over the selection with alpha-entmax
+ *   sa_gauss_select   Gaussian-aware adaptive page selection per query head
  *
  * Sources (cited by page title and section):
  *   [vortex]  "flow: add H2O sparse attention (page-level and token-level,
@@ -97,6 +98,10 @@ typedef struct sa_cache {
   int32_t num_kv_heads;
   int32_t page_size;
   int32_t head_dim;
+  void* kstd;           /* nullable [num_blocks, num_kv_heads, head_dim], dtype: k_std, the
+                           population standard deviation of each dimension over the page's
+                           valid tokens (for sa_gauss_select); refreshed by sa_append_kv when
+                           present */
 } sa_cache;
 
 /* The batch: block table and lengths. */
@@ -482,11 +487,71 @@ sa_status sa_h2o_prefill(const sa_cache* cache, const sa_batch* batch, const int
                          float decay, float scale, int32_t* evicted, int32_t* evicted_cnt,
                          int32_t evicted_cap, int32_t* dev_status, void* stream);
 
+/*
+ * sa_sparse_decode_entmax_qh -- sa_sparse_decode_entmax with a selection per
+ * query head.
+ *
+ * [entmax] "How it works" (pages kept per query head; the selected pages
+ * attended exactly with alpha-entmax): query head g attends the pages of its
+ * own row, of its KV head g / G.
+ *   sel_idx  [batch, num_q_heads, sel_stride] int32, sel_cnt [batch, num_q_heads]
+ *   workspace  sa_entmax_workspace_size(batch, num_q_heads, num_q_heads,
+ *            head_dim, page_size, sel_stride) bytes (each query head a unit of
+ *            one head), zero-filled once
+ * Everything else as sa_sparse_decode_entmax.
+ */
+sa_status sa_sparse_decode_entmax_qh(const sa_cache* cache, const sa_batch* batch, const void* q,
+                                     int32_t num_q_heads, const int32_t* sel_idx,
+                                     const int32_t* sel_cnt, int32_t sel_stride, float alpha,
+                                     float scale, void* out, float* tau, float* logits,
+                                     int32_t logits_stride, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * sa_gauss_select -- Gaussian-aware page selection, one selection per query
+ * head.
+ *
+ * [entmax] "How it works" (Gaussian-aware strategy): each page's scores are
+ * modelled as a Gaussian from the per-page k_mean and k_std (without touching
+ * the cached tokens), the distributional entmax constraint is solved for the
+ * threshold tau_hat (one Gaussian for the whole context: heads without ALiBi),
+ * and every page whose estimated maximum can cross tau_hat is selected; the
+ * count adapts to the score distribution. With z = scale * q . k, f_p the
+ * page's valid tokens and the page's dimensions taken as independent:
+ *   m_p = scale sum_d q_d mean_pd,  v_p = scale^2 sum_d q_d^2 std_pd^2
+ *   N = sum f_p, M = sum f m / N, V = sum f (v + m^2) / N - M^2
+ *   tau_hat: N E[((alpha - 1) Z - tau_hat)_+ ^ (1 / (alpha - 1))] = 1, Z ~ N(M, V)
+ *   keep p  iff (alpha - 1)(m_p + sqrt(2 ln f_p) sqrt(v_p)) > tau_hat, or p is
+ *           the tail page (sqrt(2 ln f) bounds the expected maximum of f
+ *           Gaussian scores)
+ *   q        [batch, num_q_heads, head_dim], dtype
+ *   alpha    1.5 or 2 (the closed forms of the truncated moments), else
+ *            SA_ERR_UNSUPPORTED
+ *   scale    <= 0 selects head_dim ** -0.5
+ *   moments  float32 scratch [batch, num_q_heads, max_pages, 2] (m_p, v_p)
+ *   max_pages >= batch->bt_stride; sel_stride >= max_pages
+ *   sel_idx  [batch, num_q_heads, sel_stride] int32, ascending; sel_cnt
+ *            [batch, num_q_heads] (0 for an empty request)
+ *   tau_hat  nullable float32 [batch, num_q_heads] (in units of (alpha - 1) z)
+ * Needs cache->meta (k_mean) and cache->kstd, both refreshed by sa_append_kv.
+ * Pages whose block id is out of range are never kept (except the tail, left
+ * to the decode's own check) and set SA_DEV_BAD_BLOCK. The selection feeds
+ * sa_sparse_decode_entmax_qh, whose tau is exact over the selected tokens.
+ */
+sa_status sa_gauss_select(const sa_cache* cache, const sa_batch* batch, const void* q,
+                          int32_t num_q_heads, float alpha, float scale, float* moments,
+                          int32_t max_pages, int32_t* sel_idx, int32_t* sel_cnt,
+                          int32_t sel_stride, float* tau_hat, int32_t* dev_status, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* sa_status_string(sa_status status);
 
 /* Library version, e.g. "0.1.0" (static string). */
 const char* sa_version(void);
+
+/* sizeof(sa_cache) (which = 0) or sizeof(sa_batch) (which = 1) as built, so a
+ * binding can check its struct layout (host function; 0 for other values). */
+size_t sa_struct_size(int32_t which);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ SA_DEV_BAD_BLOCK, SA_DEV_OVERFLOW, SA_DEV_BAD_COUNT, SA_DEV_TIMEOUT = 1, 2, 4, 8
 class SaCache(ctypes.Structure):
     _fields_ = [("k", c_ptr), ("v", c_ptr), ("meta", c_ptr), ("dtype", c_i32),
                 ("num_blocks", c_i32), ("num_kv_heads", c_i32), ("page_size", c_i32),
-                ("head_dim", c_i32)]
+                ("head_dim", c_i32), ("kstd", c_ptr)]
 
 
 class SaBatch(ctypes.Structure):
@@ -69,6 +69,12 @@ SIGNATURES = {
     "sa_sparse_decode_entmax": (c_i32, [P_CACHE, P_BATCH, c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_f32,
                                         c_f32, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_size, c_ptr,
                                         c_ptr]),
+    "sa_sparse_decode_entmax_qh": (c_i32, [P_CACHE, P_BATCH, c_ptr, c_i32, c_ptr, c_ptr, c_i32,
+                                           c_f32, c_f32, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_size,
+                                           c_ptr, c_ptr]),
+    "sa_gauss_select": (c_i32, [P_CACHE, P_BATCH, c_ptr, c_i32, c_f32, c_f32, c_ptr, c_i32, c_ptr,
+                                c_ptr, c_i32, c_ptr, c_ptr, c_ptr]),
+    "sa_struct_size": (c_size, [c_i32]),
     "sa_status_string": (ctypes.c_char_p, [c_i32]),
     "sa_version": (ctypes.c_char_p, []),
 }

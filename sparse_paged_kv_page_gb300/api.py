@@ -21,8 +21,9 @@ __all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKV
            "sa_sparse_decode_noalloc_capacity", "sa_h2o_update", "sa_decode_step",
            "sa_select_topk_reserved", "sa_h2o_update_window", "sa_score_pages_qh",
            "sa_sparse_decode_qh", "sa_h2o_prefill", "sa_entmax_workspace_size",
-           "alloc_entmax_workspace", "sa_sparse_decode_entmax",
-           "sa_status_string",
+           "alloc_entmax_workspace", "sa_sparse_decode_entmax", "sa_sparse_decode_entmax_qh",
+           "sa_gauss_select",
+           "sa_status_string", "sa_struct_size",
            "sa_version", "alloc_decode_workspace"]
 
 _DT = {torch.bfloat16: _lib.SA_BF16, torch.float16: _lib.SA_FP16}
@@ -59,16 +60,20 @@ def _s(stream):
     return stream.cuda_stream
 
 
-def make_cache(k: torch.Tensor, v: torch.Tensor, meta: Optional[torch.Tensor]) -> SaCache:
-    """Struct view of pools [num_blocks, H_kv, page_size, D] and meta [num_blocks, H_kv, 3, D]."""
+def make_cache(k: torch.Tensor, v: torch.Tensor, meta: Optional[torch.Tensor],
+               kstd: Optional[torch.Tensor] = None) -> SaCache:
+    """Struct view of pools [num_blocks, H_kv, page_size, D], meta [num_blocks, H_kv, 3, D]
+    and (optional) kstd [num_blocks, H_kv, D]."""
     if k.dtype not in _DT or v.dtype != k.dtype or k.shape != v.shape or k.dim() != 4:
         raise ValueError("k, v must be bf16/fp16 [num_blocks, H_kv, page_size, D] of equal shape")
     nb, hkv, ps, d = k.shape
     if meta is not None and (meta.dtype != k.dtype or tuple(meta.shape) != (nb, hkv, 3, d)):
         raise ValueError("meta must be [num_blocks, H_kv, 3, D] in the pool dtype")
+    if kstd is not None and (kstd.dtype != k.dtype or tuple(kstd.shape) != (nb, hkv, d)):
+        raise ValueError("kstd must be [num_blocks, H_kv, D] in the pool dtype")
     c = SaCache(_p(k, name="k"), _p(v, name="v"), _p(meta, name="meta"), _DT[k.dtype], nb, hkv,
-                ps, d)
-    c._keep = (k, v, meta)
+                ps, d, _p(kstd, name="kstd"))
+    c._keep = (k, v, meta, kstd)
     return c
 
 
@@ -86,7 +91,7 @@ class PagedKVCache:
     """Device buffers of one paged cache (PyTorch allocates; kernels do the work)."""
 
     def __init__(self, num_blocks, num_kv_heads, page_size, head_dim, dtype=torch.bfloat16,
-                 device="cuda", with_meta=True, with_hh=False):
+                 device="cuda", with_meta=True, with_hh=False, with_std=False):
         shape = (num_blocks, num_kv_heads, page_size, head_dim)
         self.k = torch.empty(shape, dtype=dtype, device=device)
         self.v = torch.empty(shape, dtype=dtype, device=device)
@@ -94,11 +99,18 @@ class PagedKVCache:
                      if with_meta else None)
         self.hh = (torch.zeros((num_blocks * page_size, num_kv_heads), dtype=torch.bfloat16,
                                device=device) if with_hh else None)
-        self.struct = make_cache(self.k, self.v, self.meta)
+        self.kstd = (torch.empty((num_blocks, num_kv_heads, head_dim), dtype=dtype, device=device)
+                     if with_std else None)
+        self.struct = make_cache(self.k, self.v, self.meta, self.kstd)
 
 
 def sa_status_string(status: int) -> str:
     return _lib.load().sa_status_string(int(status)).decode()
+
+
+def sa_struct_size(which: int) -> int:
+    """sizeof(sa_cache) (0) or sizeof(sa_batch) (1) as the library was built."""
+    return int(_lib.load().sa_struct_size(int(which)))
 
 
 def sa_version() -> str:
@@ -229,6 +241,36 @@ def sa_sparse_decode_entmax(cache: SaCache, batch: SaBatch, q, num_q_heads: int,
         float(alpha), float(scale), _p(out, name="out"), _p(tau, torch.float32, "tau"),
         _p(logits, torch.float32, "logits"), int(logits_stride), _p(workspace, name="workspace"),
         wbytes, _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_sparse_decode_entmax_qh(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_idx,
+                               sel_cnt, sel_stride: int, alpha: float, scale: float, out, tau=None,
+                               logits=None, logits_stride: int = 0, workspace=None,
+                               dev_status=None, stream=None):
+    """sa_sparse_decode_entmax with a selection per query head: sel_idx [B, H_q, sel_stride]
+    (workspace: alloc_entmax_workspace(B, H_q, H_q, ...))."""
+    lib = _lib.load()
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("sa_sparse_decode_entmax_qh", lib.sa_sparse_decode_entmax_qh(
+        ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads),
+        _p(sel_idx, torch.int32, "sel_idx"), _p(sel_cnt, torch.int32, "sel_cnt"), int(sel_stride),
+        float(alpha), float(scale), _p(out, name="out"), _p(tau, torch.float32, "tau"),
+        _p(logits, torch.float32, "logits"), int(logits_stride), _p(workspace, name="workspace"),
+        wbytes, _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_gauss_select(cache: SaCache, batch: SaBatch, q, num_q_heads: int, alpha: float,
+                    scale: float, moments, max_pages: int, sel_idx, sel_cnt, sel_stride: int,
+                    tau_hat=None, dev_status=None, stream=None):
+    """Gaussian-aware selection per query head: moments float32 [B, H_q, max_pages, 2]
+    (scratch), sel_idx [B, H_q, sel_stride], sel_cnt [B, H_q], tau_hat [B, H_q]."""
+    lib = _lib.load()
+    _check("sa_gauss_select", lib.sa_gauss_select(
+        ctypes.byref(cache), ctypes.byref(batch), _p(q, name="q"), int(num_q_heads), float(alpha),
+        float(scale), _p(moments, torch.float32, "moments"), int(max_pages),
+        _p(sel_idx, torch.int32, "sel_idx"), _p(sel_cnt, torch.int32, "sel_cnt"), int(sel_stride),
+        _p(tau_hat, torch.float32, "tau_hat"), _p(dev_status, torch.int32, "dev_status"),
+        _s(stream)))
 
 
 def sa_sparse_decode_noalloc(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_idx,

@@ -13,3 +13,7 @@ extern "C" const char* sa_status_string(sa_status status) {
 }
 
 extern "C" const char* sa_version(void) { return "0.1.0"; }
+
+extern "C" size_t sa_struct_size(int32_t which) {
+  return which == 0 ? sizeof(sa_cache) : (which == 1 ? sizeof(sa_batch) : 0);
+}

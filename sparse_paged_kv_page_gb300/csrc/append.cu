@@ -1,12 +1,13 @@
 // sa_append_kv: write new keys / values into the paged pools and recompute
-// the element-wise statistics (k_min, k_max, k_mean) of every page touched.
+// the element-wise statistics (k_min, k_max, k_mean, and k_std where the cache
+// keeps it) of every page touched.
 //
 // "flow: add H2O sparse attention" (vortex_torch PR 6), "Page-level variants"
 // and "Token-level variants" point 2: the statistics are overwriting
 // reductions over the written page, and the H2O score slots written in the
 // step are reset to zero because recycled pool pages keep stale contents.
 // "EntmaxKV" README, "How it works": per-page key statistics refreshed on
-// append.
+// append (min / max for top-k, mean / std for the Gaussian strategy).
 //
 // One CTA per (touched page, request); thread (h, c) owns the column pair
 // [2c, 2c+1] of KV head h and loads all of the page's rows before using any,
@@ -37,6 +38,7 @@ struct AppendArgs {
   void* k;
   void* v;
   void* meta;
+  void* kstd;
   const void* k_new;
   const void* v_new;
   const int32_t* new_cu;
@@ -85,6 +87,35 @@ __device__ __forceinline__ bool mean_f32(float S, int f, uint16_t& out) {
   const uint16_t mag = fabsf(S) > fabsf(prod) ? uint16_t(lo + 1) : lo;
   out = uint16_t(mag | (S < 0.f ? 0x8000u : 0u));
   return true;
+}
+
+// k_std of the column pair [2c, 2c+1] of (block, head): sqrt((1/f) sum (x - mean)^2)
+// around the exact mean, in float64 (the f rows, new ones included, are this
+// thread's own pool writes or untouched), rounded once to the element type.
+// Only for caches that keep k_std; kept out of line so the common path keeps
+// its registers.
+template <typename T>
+__device__ __noinline__ void page_std_pair(const AppendArgs& a, const uint32_t* kp, int64_t tile,
+                                           int fill, int blk, int h, int c) {
+  using E = Elem<T>;
+  const int C = a.D / 2;
+  double s0 = 0.0, s1 = 0.0;
+  for (int s = 0; s < fill; ++s) {
+    const uint32_t x = kp[(tile + s) * C + c];
+    s0 += double(E::lo(x));
+    s1 += double(E::hi(x));
+  }
+  const double m0 = s0 / double(fill), m1 = s1 / double(fill);
+  double q0 = 0.0, q1 = 0.0;
+  for (int s = 0; s < fill; ++s) {
+    const uint32_t x = kp[(tile + s) * C + c];
+    const double d0 = double(E::lo(x)) - m0, d1 = double(E::hi(x)) - m1;
+    q0 = fma(d0, d0, q0);
+    q1 = fma(d1, d1, q1);
+  }
+  const uint16_t v0 = E::from_f64(sqrt(q0 / double(fill)));
+  const uint16_t v1 = E::from_f64(sqrt(q1 / double(fill)));
+  static_cast<uint32_t*>(a.kstd)[(int64_t(blk) * a.H + h) * C + c] = uint32_t(v0) | (uint32_t(v1) << 16);
 }
 
 // Recompute statistics of page p of request b (all heads) and write the new rows.
@@ -168,6 +199,7 @@ __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, 
     m[0] = E::pack(mn0, mn1);                             // exact: values are already dtype
     m[C] = E::pack(mx0, mx1);
     m[2 * C] = uint32_t(me0) | (uint32_t(me1) << 16);
+    if (a.kstd) page_std_pair<T>(a, kp, tile, fill, blk, h, c);
   }
   // H2O slots of the written tokens start at zero
   if (a.hh) {
@@ -287,7 +319,7 @@ sa_status sa::append_impl(const sa_cache* cache, const sa_batch* batch, const vo
   if (max_new_per_req == 0) return SA_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   AppendArgs a;
-  a.k = cache->k; a.v = cache->v; a.meta = cache->meta;
+  a.k = cache->k; a.v = cache->v; a.meta = cache->meta; a.kstd = cache->meta ? cache->kstd : nullptr;
   a.k_new = k_new; a.v_new = v_new; a.new_cu = new_cu;
   a.bt = batch->block_table; a.seq_lens = batch->seq_lens;
   a.hh = static_cast<uint16_t*>(hh); a.ret_pos = ret_pos; a.ret_cnt = ret_cnt;

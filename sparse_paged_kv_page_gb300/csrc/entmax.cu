@@ -56,6 +56,7 @@ struct EntArgs {
   void* out;
   int32_t* status;
   int H_kv, H_q, G, ps, ps_shift, num_blocks, bt_stride, sel_stride, logits_stride, nsplit, ent_cap;
+  int H_u, kv_div;       // selection units per request (H_kv, or H_q per query head) and per KV head
   float alpha;
 };
 
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(kThreads) entmax_tau_kernel(EntArgs a) {
   const int warp = tid >> 5, lane = tid & 31;
   pdl_trigger();                                          // the weighted-V kernel may start its prologue
   pdl_wait();                                             // the logits of this call are written
-  int c = a.cnt[b * a.H_kv + gq / a.G];
+  int c = a.cnt[b * a.H_u + gq / a.G];
   c = max(0, min(c, a.sel_stride));
   const int n = c << a.ps_shift;
   const float* z = a.logits + (int64_t(b) * a.H_q + gq) * a.logits_stride;
@@ -443,14 +444,15 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
   const int G = a.G;
   // the selection and lengths come from before the logits pass: resolve the
   // entries this CTA touches to (block, fill) before waiting for the thresholds
-  int c = a.cnt[b * a.H_kv + h];
+  const int kvh = h / a.kv_div;                           // the unit's KV head
+  int c = a.cnt[b * a.H_u + h];
   c = max(0, min(c, a.sel_stride));
   const int n = c << a.ps_shift;
   const int per = (((n + a.nsplit - 1) / a.nsplit) + 31) & ~31;
   const int t_lo = min(n, split * per), t_hi = min(n, t_lo + per);
   const int L = a.seq_lens[b];
   const int n_pages_req = L > 0 ? (L + a.ps - 1) >> a.ps_shift : 0;
-  const int32_t* sel = a.sel + int64_t(b * a.H_kv + h) * a.sel_stride;
+  const int32_t* sel = a.sel + int64_t(b * a.H_u + h) * a.sel_stride;
   const int32_t* btb = a.bt + int64_t(b) * a.bt_stride;
   const int e_lo = t_lo >> a.ps_shift;
   const int e_n = t_hi > t_lo ? min(((t_hi - 1) >> a.ps_shift) - e_lo + 1, a.ent_cap) : 0;
@@ -523,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
           const int jj = base + src[u];
           const int2 en = s_ent[(jj >> a.ps_shift) - e_lo];
           const int s = jj & (a.ps - 1);
-          const T* vrow = vbase + ((int64_t(en.x) * a.H_kv + h) * a.ps + s) * D + lane * DPL;
+          const T* vrow = vbase + ((int64_t(en.x) * a.H_kv + kvh) * a.ps + s) * D + lane * DPL;
           if constexpr (DPL == 4) {
             const uint2 w = __ldg(reinterpret_cast<const uint2*>(vrow));
             vv[u][0] = E::lo(w.x); vv[u][1] = E::hi(w.x); vv[u][2] = E::lo(w.y); vv[u][3] = E::hi(w.y);
@@ -577,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const int done = atomicAdd(&a.tickets[b * a.H_kv + h], 1);
+    const int done = atomicAdd(&a.tickets[b * a.H_u + h], 1);
     s_last = done == a.nsplit - 1;
   }
   __syncthreads();
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
     const float y = l > 0.f ? o / l : 0.f;                 // no kept token: 0
     reinterpret_cast<uint16_t*>(a.out)[(int64_t(b) * a.H_q + int64_t(h) * G + g) * D + d] = E::from_f(y);
   }
-  if (tid == 0) a.tickets[b * a.H_kv + h] = 0;             // ready for the next call
+  if (tid == 0) a.tickets[b * a.H_u + h] = 0;             // ready for the next call
 }
 
 int device_sms() {
@@ -647,7 +649,7 @@ EntLayout ent_layout(int B, int H_kv, int H_q, int D, int ps, int sel_stride, in
   return w;
 }
 
-int g_att_smem[12][64];
+int g_att_smem[16][64];
 
 template <typename T, int D, int kG>
 sa_status launch_attend(const EntArgs& a, dim3 grid, cudaStream_t s, int* attr) {
@@ -662,9 +664,10 @@ sa_status launch_attend(const EntArgs& a, dim3 grid, cudaStream_t s, int* attr) 
 
 template <typename T, int D>
 sa_status launch_attend_g(const EntArgs& a, dim3 grid, cudaStream_t s, int slot) {
-  if (a.G <= 4) return launch_attend<T, D, 4>(a, grid, s, g_att_smem[slot * 3 + 0]);
-  if (a.G <= 8) return launch_attend<T, D, 8>(a, grid, s, g_att_smem[slot * 3 + 1]);
-  return launch_attend<T, D, 16>(a, grid, s, g_att_smem[slot * 3 + 2]);
+  if (a.G == 1) return launch_attend<T, D, 1>(a, grid, s, g_att_smem[slot * 4 + 3]);
+  if (a.G <= 4) return launch_attend<T, D, 4>(a, grid, s, g_att_smem[slot * 4 + 0]);
+  if (a.G <= 8) return launch_attend<T, D, 8>(a, grid, s, g_att_smem[slot * 4 + 1]);
+  return launch_attend<T, D, 16>(a, grid, s, g_att_smem[slot * 4 + 2]);
 }
 
 }  // namespace
@@ -680,41 +683,45 @@ extern "C" size_t sa_entmax_workspace_size(int32_t batch, int32_t num_kv_heads, 
       .total;
 }
 
-extern "C" sa_status sa_sparse_decode_entmax(const sa_cache* cache, const sa_batch* batch,
-                                             const void* q, int32_t num_q_heads,
-                                             const int32_t* sel_idx, const int32_t* sel_cnt,
-                                             int32_t sel_stride, float alpha, float scale, void* out,
-                                             float* tau, float* logits, int32_t logits_stride,
-                                             void* workspace, size_t workspace_bytes,
-                                             int32_t* dev_status, void* stream) {
-  using namespace sa;
+namespace sa {
+namespace {
+
+// per_query_head: the selection has one row per query head (sel [B, H_q,
+// stride]); each query head is a unit of one head attending its own pages
+// of KV head g / G.
+sa_status entmax_impl(const sa_cache* cache, const sa_batch* batch, const void* q, int32_t num_q_heads,
+                      const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_stride, float alpha,
+                      float scale, void* out, float* tau, float* logits, int32_t logits_stride,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream,
+                      bool per_query_head) {
   sa_status st = check_cache(cache, true, false);
   if (st != SA_OK) return st;
   if ((st = check_batch(batch)) != SA_OK) return st;
   if (!q || !sel_idx || !sel_cnt || !out || sel_stride <= 0) return SA_ERR_INVALID_ARG;
   if (!(alpha > 1.0f && alpha <= 2.0f)) return SA_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
-  const int G = num_q_heads / cache->num_kv_heads;
-  if (G > 16) return SA_ERR_UNSUPPORTED;
+  const int G_kv = num_q_heads / cache->num_kv_heads;
+  if (G_kv > 16) return SA_ERR_UNSUPPORTED;
+  const int G = per_query_head ? 1 : G_kv;
+  const int H_u = per_query_head ? num_q_heads : cache->num_kv_heads;
   const int64_t rows = int64_t(sel_stride) * cache->page_size;
   if (rows > (int64_t(1) << 24)) return SA_ERR_UNSUPPORTED;
   if (logits && logits_stride < rows) return SA_ERR_INVALID_ARG;
-  const EntLayout w = ent_layout(batch->batch, cache->num_kv_heads, num_q_heads, cache->head_dim,
-                                 cache->page_size, sel_stride, device_sms());
+  const EntLayout w = ent_layout(batch->batch, H_u, num_q_heads, cache->head_dim, cache->page_size,
+                                 sel_stride, device_sms());
   if (!workspace || workspace_bytes < w.total) return SA_ERR_WORKSPACE;
-  const int kmax = G <= 4 ? 4 : (G <= 8 ? 8 : 16);
   const int64_t smem = int64_t(kWarps) * G * (cache->head_dim + 1) * 4 + int64_t(w.ent_cap) * 8;
-  if (smem > 227 * 1024 || kmax < G) return SA_ERR_UNSUPPORTED;   // (checked before any launch)
+  if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;       // (checked before any launch)
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* lg = logits ? logits : reinterpret_cast<float*>(ws + w.logits);
   const int lg_stride = logits ? logits_stride : int(rows);
   // the split counters start at zero (a zero-filled workspace); each call's
-  // last CTA per (request, KV head) leaves its counter at zero again
+  // last CTA per unit leaves its counter at zero again
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // (1) the logits of every selected token (K only)
   st = decode_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, scale, out, nullptr, lg,
                    lg_stride, nullptr, 0, dev_status, stream, /*allow_cluster=*/false, /*pdl=*/false,
-                   /*per_query_head=*/false, /*logits_only=*/true);
+                   per_query_head, /*logits_only=*/true);
   if (st != SA_OK) return st;
   EntArgs a;
   a.v = cache->v; a.bt = batch->block_table; a.seq_lens = batch->seq_lens; a.sel = sel_idx;
@@ -726,14 +733,41 @@ extern "C" sa_status sa_sparse_decode_entmax(const sa_cache* cache, const sa_bat
   a.ps_shift = log2i(cache->page_size); a.num_blocks = cache->num_blocks;
   a.bt_stride = batch->bt_stride; a.sel_stride = sel_stride; a.logits_stride = lg_stride;
   a.nsplit = w.nsplit; a.ent_cap = w.ent_cap; a.alpha = alpha;
+  a.H_u = H_u; a.kv_div = per_query_head ? G_kv : 1;
   // (2) tau per (request, query head)
   if (launch_ex(entmax_tau_kernel, dim3(unsigned(num_q_heads), unsigned(batch->batch)), dim3(kThreads),
                 0, s, true, 1u, a) != cudaSuccess)
     return SA_ERR_CUDA;
   // (3) the kept tokens' sum_j p_j v_j per split, the last split normalising
-  const dim3 grid(unsigned(w.nsplit), unsigned(cache->num_kv_heads), unsigned(batch->batch));
+  const dim3 grid(unsigned(w.nsplit), unsigned(H_u), unsigned(batch->batch));
   const bool bf = cache->dtype == SA_BF16;
   if (cache->head_dim == 128)
     return bf ? launch_attend_g<__nv_bfloat16, 128>(a, grid, s, 0) : launch_attend_g<__half, 128>(a, grid, s, 1);
   return bf ? launch_attend_g<__nv_bfloat16, 64>(a, grid, s, 2) : launch_attend_g<__half, 64>(a, grid, s, 3);
+}
+
+}  // namespace
+}  // namespace sa
+
+extern "C" sa_status sa_sparse_decode_entmax(const sa_cache* cache, const sa_batch* batch,
+                                             const void* q, int32_t num_q_heads,
+                                             const int32_t* sel_idx, const int32_t* sel_cnt,
+                                             int32_t sel_stride, float alpha, float scale, void* out,
+                                             float* tau, float* logits, int32_t logits_stride,
+                                             void* workspace, size_t workspace_bytes,
+                                             int32_t* dev_status, void* stream) {
+  return sa::entmax_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, alpha, scale, out,
+                         tau, logits, logits_stride, workspace, workspace_bytes, dev_status, stream, false);
+}
+
+extern "C" sa_status sa_sparse_decode_entmax_qh(const sa_cache* cache, const sa_batch* batch,
+                                                const void* q, int32_t num_q_heads,
+                                                const int32_t* sel_idx, const int32_t* sel_cnt,
+                                                int32_t sel_stride, float alpha, float scale,
+                                                void* out, float* tau, float* logits,
+                                                int32_t logits_stride, void* workspace,
+                                                size_t workspace_bytes, int32_t* dev_status,
+                                                void* stream) {
+  return sa::entmax_impl(cache, batch, q, num_q_heads, sel_idx, sel_cnt, sel_stride, alpha, scale, out,
+                         tau, logits, logits_stride, workspace, workspace_bytes, dev_status, stream, true);
 }

@@ -9,6 +9,9 @@ Token level (page_size 1):   append (+ retained list) -> sparse decode over
 alpha-entmax (1 < alpha <= 2, page level): append -> score -> select ->
                              ``sa_sparse_decode_entmax`` (the selection
                              normalised by alpha-entmax instead of softmax).
+Gaussian-aware (alpha 1.5 or 2, page level): append (k_mean, k_std) ->
+                             ``sa_gauss_select`` (per query head, adaptive
+                             count) -> ``sa_sparse_decode_entmax_qh``.
 
 PyTorch only allocates the buffers and supplies the stream; every step runs in
 the native kernels. ``capture()`` records one step into a CUDA graph whose
@@ -25,7 +28,7 @@ from .api import (PagedKVCache, alloc_decode_workspace, alloc_entmax_workspace, 
                   sa_append_kv, sa_decode_step, sa_h2o_prefill, sa_h2o_update,
                   sa_h2o_update_window, sa_score_pages, sa_score_pages_qh,
                   sa_select_topk_reserved, sa_sparse_decode, sa_sparse_decode_entmax,
-                  sa_sparse_decode_qh)
+                  sa_sparse_decode_entmax_qh, sa_gauss_select, sa_sparse_decode_qh)
 
 
 class SparseDecoder:
@@ -35,7 +38,7 @@ class SparseDecoder:
                  budget: int = 0, n_sink: int = 0, grace: int = 0, decay: float = 1.0,
                  ret_cap: int = 0, n_bos: int = 0, n_eos: int = 1, window_softmax: bool = False,
                  per_query_head: bool = False, proxy_prefill: bool = False, alpha: float = 1.0,
-                 device="cuda"):
+                 gaussian: bool = False, device="cuda"):
         self.B, self.H_q, self.H_kv, self.D = batch, num_q_heads, num_kv_heads, head_dim
         self.ps, self.dtype, self.device = page_size, dtype, torch.device(device)
         self.token_level = page_size == 1 and ret_cap > 0
@@ -49,11 +52,18 @@ class SparseDecoder:
         rows = num_q_heads if self.qh else num_kv_heads
         # alpha-entmax instead of softmax over the selection (page level, per KV head)
         self.alpha = float(alpha)
-        self.entmax = self.alpha != 1.0
+        # Gaussian-aware adaptive selection per query head, attended with alpha-entmax
+        self.gaussian = gaussian
+        if gaussian and (page_size == 1 or self.alpha not in (1.5, 2.0) or per_query_head):
+            raise ValueError("Gaussian-aware selection needs alpha 1.5 or 2 at the page level")
+        self.entmax = self.alpha != 1.0 and not gaussian
         if self.entmax and (self.token_level or self.qh or not 1.0 < self.alpha <= 2.0):
             raise ValueError("entmax decoding needs 1 < alpha <= 2, page level, per-KV-head selection")
+        if gaussian:
+            topk = max(topk, 1)
         self.cache = PagedKVCache(num_blocks, num_kv_heads, page_size, head_dim, dtype, device,
-                                  with_meta=not self.token_level, with_hh=self.token_level)
+                                  with_meta=not self.token_level, with_hh=self.token_level,
+                                  with_std=gaussian)
         i32 = dict(dtype=torch.int32, device=device)
         self.block_table = torch.zeros((batch, bt_stride), **i32)
         self.seq_lens = torch.zeros((batch,), **i32)
@@ -82,6 +92,17 @@ class SparseDecoder:
         self.workspace = alloc_decode_workspace(batch, rows if not self.token_level else num_kv_heads,
                                                 num_q_heads, head_dim, page_size, self.sel_stride,
                                                 device)
+        if gaussian:
+            # every page may qualify: selections as long as the table, one per query head
+            self.sel_stride = bt_stride
+            self.moments = torch.empty((batch, num_q_heads, bt_stride, 2), dtype=torch.float32,
+                                       device=device)
+            self.sel_idx = torch.zeros((batch, num_q_heads, bt_stride), **i32)
+            self.sel_cnt = torch.zeros((batch, num_q_heads), **i32)
+            self.tau_hat = torch.empty((batch, num_q_heads), dtype=torch.float32, device=device)
+            self.tau = torch.empty((batch, num_q_heads), dtype=torch.float32, device=device)
+            self.ent_ws = alloc_entmax_workspace(batch, num_q_heads, num_q_heads, head_dim,
+                                                 page_size, bt_stride, device)
         if self.entmax:
             self.ent_ws = alloc_entmax_workspace(batch, num_kv_heads, num_q_heads, head_dim,
                                                  page_size, self.sel_stride, device)
@@ -144,6 +165,14 @@ class SparseDecoder:
                           self.ret_cap, self.budget, self.n_sink, self.grace, self.decay,
                           evicted=self.evicted, evicted_cnt=self.evicted_cnt,
                           dev_status=self.dev_status)
+        elif self.gaussian:
+            sa_gauss_select(self.cache.struct, self.batch, q, self.H_q, self.alpha, self.scale,
+                            self.moments, self.max_pages, self.sel_idx, self.sel_cnt,
+                            self.sel_stride, tau_hat=self.tau_hat, dev_status=self.dev_status)
+            sa_sparse_decode_entmax_qh(self.cache.struct, self.batch, q, self.H_q, self.sel_idx,
+                                       self.sel_cnt, self.sel_stride, self.alpha, self.scale,
+                                       self.out, tau=self.tau, workspace=self.ent_ws,
+                                       dev_status=self.dev_status)
         elif self.qh:
             sa_score_pages_qh(self.cache.struct, self.batch, q, self.H_q, self.w_avg, self.w_peak,
                               self.scores, self.max_pages, dev_status=self.dev_status)
@@ -173,7 +202,7 @@ class SparseDecoder:
 
     def step(self, q: torch.Tensor, k_new: Optional[torch.Tensor] = None,
              v_new: Optional[torch.Tensor] = None):
-        if self.token_level or self.qh or self.entmax:
+        if self.token_level or self.qh or self.entmax or self.gaussian:
             if k_new is not None:
                 self.append(k_new, v_new)
             return self.attend(q)

@@ -48,6 +48,15 @@ def test_host_only_calls(lib):
                               0, 1, None, None, 0.0, None, None, None, 0, None, None) == 1
 
 
+def test_struct_layouts_match_the_binding(lib):
+    import ctypes
+    import sparse_paged_kv_page_gb300 as S
+    from sparse_paged_kv_page_gb300 import _lib
+    assert S.sa_struct_size(0) == ctypes.sizeof(_lib.SaCache)
+    assert S.sa_struct_size(1) == ctypes.sizeof(_lib.SaBatch)
+    assert _lib.SaCache.kstd.offset == ctypes.sizeof(_lib.SaCache) - ctypes.sizeof(ctypes.c_void_p)
+
+
 def test_product_package_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "sparse_paged_kv_page_gb300")
     for dirpath, _, files in os.walk(pkg):
