@@ -89,6 +89,14 @@ def entmax_step_bytes(cfg, lens, v_rows):
     return tot + v_rows * cfg.D * e + 2 * cfg.B * cfg.H_q * cfg.D * e
 
 
+def gauss_step_bytes(cfg, lens, sel_pages, v_rows):
+    """Gaussian-aware step: the k_mean and k_std rows of every page, K of the
+    pages each query head selected, V of the rows each head keeps, q and out."""
+    e = 2
+    stats = sum(-(-L // cfg.ps) for L in lens) * cfg.H_kv * 2 * cfg.D * e
+    return stats + sel_pages * cfg.ps * cfg.D * e + v_rows * cfg.D * e + 2 * cfg.B * cfg.H_q * cfg.D * e
+
+
 def entmax_kept(dec, alpha):
     """V rows the last step read, and the mean support per query head, from
     the step's own logits and thresholds."""
@@ -97,15 +105,17 @@ def entmax_kept(dec, alpha):
     tau = dec.tau.cpu().numpy().astype(np.float64)
     cnt = dec.sel_cnt.cpu().numpy()
     B, Hq, R = z.shape
-    G = Hq // cnt.shape[1]
+    G = Hq // cnt.shape[1]                    # 1 with a selection per query head
     with np.errstate(invalid="ignore"):
         keep = np.isfinite(z) & ((alpha - 1.0) * z - tau[:, :, None] > 0)
-    rows = 0
+    rows, sup = 0, []
     for b in range(B):
         for h in range(cnt.shape[1]):
             n = int(cnt[b, h]) * dec.ps
-            rows += int(keep[b, h * G:(h + 1) * G, :n].any(0).sum())
-    return rows, float(keep.sum(-1).mean())
+            k = keep[b, h * G:(h + 1) * G, :n]
+            rows += int(k.any(0).sum())
+            sup.extend(k.sum(-1).tolist())
+    return rows, float(np.mean(sup))
 
 
 def h2o_step_bytes(cfg, cnts):
@@ -229,6 +239,9 @@ def _worker_task(task):
     t = time.perf_counter()
     if kind == "page":
         O.page_decode_unit(ks, vs, L, qg, **kw)
+    elif kind == "gauss":
+        for g in range(qg.shape[0]):                        # each query head selects for itself
+            O.gauss_decode_unit(ks, vs, L, qg[g], **kw)
     else:
         O.h2o_unit_step(hh, pos, ks, vs, qg, **kw)
     return time.perf_counter() - t
@@ -237,11 +250,11 @@ def _worker_task(task):
 class OracleRunner:
     """The float64 oracle on the host cores, one unit per spawned worker."""
 
-    def __init__(self, wl, workers, alpha=1.0):
+    def __init__(self, wl, workers, alpha=1.0, gaussian=False):
         import multiprocessing as mp
         import tempfile
         import numpy as np
-        self.wl, self.workers, self.alpha = wl, workers, alpha
+        self.wl, self.workers, self.alpha, self.gaussian = wl, workers, alpha, gaussian
         self.dir = tempfile.mkdtemp(prefix="sa_oracle_")
         spec = {}
         for name, arr in (("k", wl.k_pre), ("v", wl.v_pre)):
@@ -270,6 +283,9 @@ class OracleRunner:
                 kw = dict(dtype=c.dtype, decay=c.decay, budget=c.budget, n_sink=c.n_sink,
                           grace=c.grace, scale=c.scale)
                 out.append((b, h, lo, hi, ek, ev, L, qg, "h2o", kw, np.zeros(n), np.arange(L - n, L)))
+            elif self.gaussian:
+                kw = dict(ps=c.ps, alpha=self.alpha, dtype=c.dtype, scale=c.scale)
+                out.append((b, h, lo, hi, ek, ev, L, qg, "gauss", kw, None, None))
             else:
                 kw = dict(ps=c.ps, topk=c.topk, w_avg=c.w_avg, w_peak=c.w_peak, dtype=c.dtype,
                           scale=c.scale, alpha=self.alpha)
@@ -292,9 +308,9 @@ def units_of(cfg):
     return [(b, h) for b in range(cfg.B) for h in range(cfg.H_kv)]
 
 
-def cpu_baseline(wl, full_steps, workers, alpha=1.0):
+def cpu_baseline(wl, full_steps, workers, alpha=1.0, gaussian=False):
     """Full steps of the oracle (every unit), on `workers` processes."""
-    r = OracleRunner(wl, workers, alpha)
+    r = OracleRunner(wl, workers, alpha, gaussian)
     try:
         r.run(r.tasks(0, units_of(wl.cfg)[:workers]))          # warm the workers
         walls = [r.run(r.tasks(s, units_of(wl.cfg))) for s in range(full_steps)]
@@ -336,7 +352,9 @@ def run_gpu(args, rank, world):
                   ret_cap=int(wl.prefill_lens.max()) + n_in + 4)
     else:
         kw.update(topk=c.topk, w_avg=c.w_avg, w_peak=c.w_peak,
-                  per_query_head=args.per_query_head, alpha=args.entmax or 1.0)
+                  per_query_head=args.per_query_head,
+                  alpha=(args.entmax or 1.5) if args.gaussian else (args.entmax or 1.0),
+                  gaussian=args.gaussian)
     dec = SparseDecoder(**kw)
     fill_stale(dec.cache.k, "normal3", 11)
     fill_stale(dec.cache.v, "normal3", 12)
@@ -418,6 +436,14 @@ def run_gpu(args, rank, world):
     if token:
         # retained tokens attended per (request, KV head): budget + 1 after the first step
         bytes_per_step = h2o_step_bytes(c, [min(n + 1, c.budget + 1) for n in cnt_start])
+    elif args.gaussian:
+        v_rows, support = entmax_kept(dec, dec.alpha)
+        pages = int(dec.sel_cnt.sum().item())
+        bytes_per_step = gauss_step_bytes(c, [L + args.steps for L in lens_start], pages, v_rows)
+        ent = {"alpha": dec.alpha, "selection": "gaussian-aware, per query head",
+               "pages_selected_last_step": pages,
+               "mean_pages_per_query_head": pages / (c.B * c.H_q),
+               "v_rows_read_last_step": v_rows, "mean_support_per_query_head": support}
     elif args.entmax:
         v_rows, support = entmax_kept(dec, args.entmax)
         bytes_per_step = entmax_step_bytes(c, [L + args.steps for L in lens_start], v_rows)
@@ -435,7 +461,8 @@ def run_gpu(args, rank, world):
     # the GPU busy while the host enqueues the calls, so the events time the
     # kernels back to back rather than the host.
     kern = {}
-    names = (["append"] if append else []) + (["decode", "h2o"] if token else ["score", "select", "decode"])
+    names = (["append"] if append else []) + (["decode", "h2o"] if token else
+                                               (["select", "decode"] if args.gaussian else ["score", "select", "decode"]))
     acc = {n: [] for n in names}
     lens_reps = [int(x) for x in dec.seq_lens.cpu().tolist()]
     for i in range(args.kernel_reps):
@@ -459,6 +486,17 @@ def run_gpu(args, rank, world):
                             dec.ret_cap, c.budget, c.n_sink, c.grace, c.decay,
                             evicted=dec.evicted, evicted_cnt=dec.evicted_cnt,
                             dev_status=dec.dev_status)
+            j += 1; e[j].record(stream)
+        elif args.gaussian:
+            S.sa_gauss_select(dec.cache.struct, dec.batch, dec.q_buf, c.H_q, dec.alpha, c.scale,
+                              dec.moments, dec.max_pages, dec.sel_idx, dec.sel_cnt, dec.sel_stride,
+                              tau_hat=dec.tau_hat, dev_status=dec.dev_status)
+            j += 1; e[j].record(stream)
+            S.sa_sparse_decode_entmax_qh(dec.cache.struct, dec.batch, dec.q_buf, c.H_q, dec.sel_idx,
+                                         dec.sel_cnt, dec.sel_stride, dec.alpha, c.scale, dec.out,
+                                         tau=dec.tau, logits=dec.logits,
+                                         logits_stride=dec.sel_stride * c.ps, workspace=dec.ent_ws,
+                                         dev_status=dec.dev_status)
             j += 1; e[j].record(stream)
         else:
             qh = args.per_query_head
@@ -514,7 +552,8 @@ def run_gpu(args, rank, world):
 
     max_ms = dist_max(ms, world, dev)
     max_median_ms = dist_max(statistics.median(step_ms), world, dev)
-    launches = (1 if append else 0) + (2 if token else 3) + (3 if args.entmax else 0)
+    launches = (1 if append else 0) + (2 if token else (5 if args.gaussian else 3)) + \
+        (3 if args.entmax and not args.gaussian else 0)
     return dict(ent=ent, ms=ms, max_ms=max_ms, wall=wall, clocks=clk.summary(), bytes=bytes_per_step,
                 kern=kern, status=status, score_ab=score_ab, e2e=e2e, cfg=c, wl=wl,
                 launches_per_step=launches, step_ms_min=min(step_ms), step_ms_max=max(step_ms),
@@ -596,6 +635,9 @@ def main():
                     help="time the prefill-side H2O absorb / eviction of the token-level workload")
     ap.add_argument("--entmax", type=float, default=0.0,
                     help="attend the selection with alpha-entmax (1 < alpha <= 2) instead of softmax")
+    ap.add_argument("--gaussian", action="store_true",
+                    help="Gaussian-aware adaptive selection per query head, attended with "
+                         "alpha-entmax (alpha = --entmax, default 1.5)")
     ap.add_argument("--per-query-head", action="store_true",
                     help="select pages per query head (score, select, attend one row per query head)")
     args = ap.parse_args()
@@ -612,7 +654,8 @@ def main():
         if rank != 0:
             return
         wl = make_workload(cfg, extra_steps=2)
-        r = OracleRunner(wl, workers, args.entmax or 1.0)
+        r = OracleRunner(wl, workers, (args.entmax or 1.5) if args.gaussian else (args.entmax or 1.0),
+                         args.gaussian)
         try:
             units = units_of(cfg)
             r.run(r.tasks(0, units[:workers]))
@@ -654,7 +697,12 @@ def main():
     step_gbs = res["bytes"] / (res["ms"] * 1e-3) / 1e9
     roof = None
     if res["kern"]:
-        if c.ps > 1:
+        if args.gaussian:
+            ab = res["score_ab"] * 2 // 3                   # k_mean and k_std rows, not k_min / k_max
+            kms = res["kern"]["select"]
+            tr = None
+            kname = "gauss_moments_kernel + gauss_select_kernel (sa_gauss_select)"
+        elif c.ps > 1:
             ab = res["score_ab"]
             kms = res["kern"]["score"]
             tr = traffic_from_profile("score.cu", "score_pages.long_context_gqa.md") \
@@ -672,7 +720,9 @@ def main():
                 "kernel_ms": res["kern"]}
     cpu = None
     if world == 1 and not args.no_cpu:
-        walls = cpu_baseline(res["wl"], args.cpu_steps, workers, args.entmax or 1.0)
+        walls = cpu_baseline(res["wl"], args.cpu_steps, workers,
+                             (args.entmax or 1.5) if args.gaussian else (args.entmax or 1.0),
+                             args.gaussian)
         cpu = {"value": 1.0 / statistics.mean(walls), "unit": "steps/s", "cores": workers,
                "kind": "oracle",
                "sample": (f"{len(walls)} full step(s): all {c.B * c.H_kv} (request, KV head) "
@@ -685,7 +735,9 @@ def main():
         "dtype": c.dtype, "data": "synthetic",
         "config": {"workload": describe(c) + (", pages selected per query head"
                                               if args.per_query_head else "")
-                   + (f", {args.entmax}-entmax instead of softmax" if args.entmax else ""),
+                   + (", Gaussian-aware selection per query head, "
+                      f"{args.entmax or 1.5}-entmax" if args.gaussian else
+                      (f", {args.entmax}-entmax instead of softmax" if args.entmax else "")),
                    "l2": "flushed between steps outside the events: 256 MB write, then a 256 MB read so the flush's dirty lines are written back before the step",
                    "timing": "CUDA events around each step (graph replay); the step's q / k_new / v_new are copied from the HBM-resident input set into its input buffers before the events",
                    "parallelism": f"independent batch per GPU x{world}"},

@@ -89,38 +89,104 @@ __device__ __forceinline__ bool mean_f32(float S, int f, uint16_t& out) {
   return true;
 }
 
-// k_std of the column pair [2c, 2c+1] of (block, head): sqrt((1/f) sum (x - mean)^2)
-// around the exact mean, in float64 (the f rows, new ones included, are this
-// thread's own pool writes or untouched), rounded once to the element type.
-// Only for caches that keep k_std; kept out of line so the common path keeps
-// its registers.
+// k_std of one column over its f rows: the population std sqrt((1/f) sum
+// (x - mean)^2) around the exact mean, rounded once to the element type.
+// float32 two-pass: with m the float32 mean (error dm <= (f + 1) eps sum|x| / f)
+// the computed sum of squared deviations q differs from the true one by at
+// most f dm^2 (the centre's error enters squared, the deviations summing to
+// zero) plus (f + 3) eps q of rounding, so the std's relative error is below
+// half that (+ eps). The float32 result is kept when every value within twice
+// that bound rounds to the same element; otherwise float64 decides. x: the
+// column's values (half kHi of each word), f <= kRowBatch of them.
+template <typename T, bool kHi>
+__device__ __forceinline__ uint16_t std_column(const uint32_t (&w)[kRowBatch], int fill) {
+  using E = Elem<T>;
+  constexpr float eps = 0x1p-24f;
+  float sum = 0.f, sabs = 0.f, xmin = INFINITY, xmax = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < kRowBatch; ++s) {
+    if (s < fill) {
+      const float x = kHi ? E::hi(w[s]) : E::lo(w[s]);
+      sum += x;
+      sabs += fabsf(x);
+      xmin = fminf(xmin, x);
+      xmax = fmaxf(xmax, x);
+    }
+  }
+  if (xmin == xmax) return E::from_f(0.f);                 // every row equal
+  const float f = float(fill);
+  const float m = sum / f;
+  float q = 0.f;
+#pragma unroll
+  for (int s = 0; s < kRowBatch; ++s) {
+    if (s < fill) {
+      const float d = (kHi ? E::hi(w[s]) : E::lo(w[s])) - m;
+      q = fmaf(d, d, q);
+    }
+  }
+  const float dm = (f + 1.f) * eps * sabs / f;
+  const float rel = 0.5f * (f * dm * dm / q + (f + 3.f) * eps) + eps;
+  const float sd = sqrtf(q / f);
+  if (q > 0x1p-100f && rel < 0x1p-12f) {
+    const uint16_t lo = E::from_f(sd * (1.f - 2.f * rel)), hi = E::from_f(sd * (1.f + 2.f * rel));
+    if (lo == hi) return lo;
+  }
+  double s64 = 0.0;                                        // undecided: float64
+#pragma unroll
+  for (int s = 0; s < kRowBatch; ++s)
+    if (s < fill) s64 += double(kHi ? E::hi(w[s]) : E::lo(w[s]));
+  const double m64 = s64 / double(fill);
+  double q64 = 0.0;
+#pragma unroll
+  for (int s = 0; s < kRowBatch; ++s) {
+    if (s < fill) {
+      const double d = double(kHi ? E::hi(w[s]) : E::lo(w[s])) - m64;
+      q64 = fma(d, d, q64);
+    }
+  }
+  return E::from_f64(sqrt(q64 / double(fill)));
+}
+
+// float64 k_std of one column over more rows than one batch (pages above 16 tokens)
+template <typename T, bool kHi>
+__device__ uint16_t std_column_long(const uint32_t* rows, int C, int fill) {
+  using E = Elem<T>;
+  double s64 = 0.0;
+  for (int s = 0; s < fill; ++s) s64 += double(kHi ? E::hi(rows[int64_t(s) * C]) : E::lo(rows[int64_t(s) * C]));
+  const double m64 = s64 / double(fill);
+  double q64 = 0.0;
+  for (int s = 0; s < fill; ++s) {
+    const double d = double(kHi ? E::hi(rows[int64_t(s) * C]) : E::lo(rows[int64_t(s) * C])) - m64;
+    q64 = fma(d, d, q64);
+  }
+  return E::from_f64(sqrt(q64 / double(fill)));
+}
+
+// k_std of the column pair [2c, 2c+1] of (block, head); the f rows, new ones
+// included, are this thread's own pool writes or untouched. Only for caches
+// that keep k_std; kept out of line so the common path keeps its registers.
 template <typename T>
 __device__ __noinline__ void page_std_pair(const AppendArgs& a, const uint32_t* kp, int64_t tile,
                                            int fill, int blk, int h, int c) {
-  using E = Elem<T>;
   const int C = a.D / 2;
-  double s0 = 0.0, s1 = 0.0;
-  for (int s = 0; s < fill; ++s) {
-    const uint32_t x = kp[(tile + s) * C + c];
-    s0 += double(E::lo(x));
-    s1 += double(E::hi(x));
+  const uint32_t* rows = kp + tile * C + c;
+  uint16_t v0, v1;
+  if (fill <= kRowBatch) {
+    uint32_t w[kRowBatch];
+#pragma unroll
+    for (int s = 0; s < kRowBatch; ++s) w[s] = s < fill ? rows[int64_t(s) * C] : 0u;   // one batch of loads
+    v0 = std_column<T, false>(w, fill);
+    v1 = std_column<T, true>(w, fill);
+  } else {
+    v0 = std_column_long<T, false>(rows, C, fill);
+    v1 = std_column_long<T, true>(rows, C, fill);
   }
-  const double m0 = s0 / double(fill), m1 = s1 / double(fill);
-  double q0 = 0.0, q1 = 0.0;
-  for (int s = 0; s < fill; ++s) {
-    const uint32_t x = kp[(tile + s) * C + c];
-    const double d0 = double(E::lo(x)) - m0, d1 = double(E::hi(x)) - m1;
-    q0 = fma(d0, d0, q0);
-    q1 = fma(d1, d1, q1);
-  }
-  const uint16_t v0 = E::from_f64(sqrt(q0 / double(fill)));
-  const uint16_t v1 = E::from_f64(sqrt(q1 / double(fill)));
   static_cast<uint32_t*>(a.kstd)[(int64_t(blk) * a.H + h) * C + c] = uint32_t(v0) | (uint32_t(v1) << 16);
 }
 
 // Recompute statistics of page p of request b (all heads) and write the new rows.
 // Thread (h, c) owns the column pair [2c, 2c+1] of KV head h (NT threads loop).
-template <typename T, int NT>
+template <typename T, int NT, bool kStd>
 __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, int L_old, int L_new,
                                              int row0) {
   using E = Elem<T>;
@@ -199,7 +265,7 @@ __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, 
     m[0] = E::pack(mn0, mn1);                             // exact: values are already dtype
     m[C] = E::pack(mx0, mx1);
     m[2 * C] = uint32_t(me0) | (uint32_t(me1) << 16);
-    if (a.kstd) page_std_pair<T>(a, kp, tile, fill, blk, h, c);
+    if constexpr (kStd) page_std_pair<T>(a, kp, tile, fill, blk, h, c);
   }
   // H2O slots of the written tokens start at zero
   if (a.hh) {
@@ -246,28 +312,28 @@ __device__ __forceinline__ bool plan(const AppendArgs& a, int b, bool report, in
 }
 
 // Grid (touched pages, B); lengths advanced by advance_kernel afterwards.
-template <typename T>
+template <typename T, bool kStd>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
   const int b = blockIdx.y, i = blockIdx.x;
   int L_old, n, row0;
   if (!plan(a, b, i == 0 && threadIdx.x == 0, L_old, n, row0)) return;
   const int p = L_old / a.ps + i;
   if (p > (L_old + n - 1) / a.ps) return;
-  refresh_page<T, kAppendThreads>(a, b, p, L_old, L_old + n, row0);
+  refresh_page<T, kAppendThreads, kStd>(a, b, p, L_old, L_old + n, row0);
 }
 
 // Grid (B): a request's (at most two) pages, then its length, in one CTA.
 // At most 128 registers a thread: with the page scorer's two CTAs resident,
 // the sub-partitions holding three of its warps have exactly one 128-register
 // warp's worth of registers left, so this kernel can run beside the scorer.
-template <typename T>
+template <typename T, bool kStd>
 __global__ void __launch_bounds__(kFusedThreads, 4) append_fused_kernel(AppendArgs a) {
   const int b = blockIdx.x;
   int L_old, n, row0;
   const bool any = plan(a, b, threadIdx.x == 0, L_old, n, row0);
   if (any)
     for (int p = L_old / a.ps; p <= (L_old + n - 1) / a.ps; ++p)
-      refresh_page<T, kFusedThreads>(a, b, p, L_old, L_old + n, row0);
+      refresh_page<T, kFusedThreads, kStd>(a, b, p, L_old, L_old + n, row0);
   __syncthreads();                                          // every read of the old length is done
   if (any) {
     for (int h = threadIdx.x; h < a.H && a.ret_cnt; h += kFusedThreads) {
@@ -329,20 +395,19 @@ sa_status sa::append_impl(const sa_cache* cache, const sa_batch* batch, const vo
   a.max_new = max_new_per_req; a.ret_cap = ret_pos ? ret_cap : 0;
   const bool bf = cache->dtype == SA_BF16;
   if (max_new_per_req <= a.ps) {                            // touches at most two pages per request
-    static int g_fused_attr[2][64];
-    if (bf ? !ensure_smem(append_fused_kernel<__nv_bfloat16>, 0, g_fused_attr[0])
-           : !ensure_smem(append_fused_kernel<__half>, 0, g_fused_attr[1]))
-      return SA_ERR_CUDA;
-    const cudaError_t e =
-        bf ? launch_ex(append_fused_kernel<__nv_bfloat16>, dim3(batch->batch), dim3(kFusedThreads), 0, s, pdl, 1, a)
-           : launch_ex(append_fused_kernel<__half>, dim3(batch->batch), dim3(kFusedThreads), 0, s, pdl, 1, a);
+    static int g_fused_attr[4][64];
+    auto kern = bf ? (a.kstd ? append_fused_kernel<__nv_bfloat16, true> : append_fused_kernel<__nv_bfloat16, false>)
+                   : (a.kstd ? append_fused_kernel<__half, true> : append_fused_kernel<__half, false>);
+    if (!ensure_smem(kern, 0, g_fused_attr[(bf ? 0 : 2) + (a.kstd ? 1 : 0)])) return SA_ERR_CUDA;
+    const cudaError_t e = launch_ex(kern, dim3(batch->batch), dim3(kFusedThreads), 0, s, pdl, 1, a);
     return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
   }
   const int64_t pages = (int64_t(max_new_per_req) + a.ps - 1) / a.ps + 1;
   if (pages > 0x7fffffff) return SA_ERR_INVALID_ARG;
   dim3 grid(unsigned(pages), unsigned(batch->batch));
-  if (bf) append_kernel<__nv_bfloat16><<<grid, kAppendThreads, 0, s>>>(a);
-  else append_kernel<__half><<<grid, kAppendThreads, 0, s>>>(a);
+  auto kern = bf ? (a.kstd ? append_kernel<__nv_bfloat16, true> : append_kernel<__nv_bfloat16, false>)
+                 : (a.kstd ? append_kernel<__half, true> : append_kernel<__half, false>);
+  kern<<<grid, kAppendThreads, 0, s>>>(a);
   if ((st = launch_status()) != SA_OK) return st;
   advance_kernel<<<1, 256, 0, s>>>(batch->seq_lens, new_cu, ret_cnt, batch->batch, a.H,
                                    max_new_per_req, int64_t(batch->bt_stride) * a.ps, a.ret_cap);

@@ -10,7 +10,8 @@
 //
 // Two launches:
 //  (1) gauss_moments_kernel: one thread per page of a (request, KV head),
-//      q of the G heads in shared memory; with the page's dimensions taken as
+//      scale q of the G heads in shared memory; with the page's dimensions
+//      taken as
 //      independent, a query head's scores z = scale q . k on page p have
 //        m_p = sum_d (scale q_d) mean_pd,  v_p = sum_d (scale q_d)^2 std_pd^2.
 //  (2) gauss_select_kernel: one CTA per (request, query head). The page
@@ -46,6 +47,7 @@ struct GaussArgs {
   float* tau_hat;        // nullable [B, H_q]
   int32_t* status;
   int H_kv, H_q, G, ps, ps_shift, num_blocks, bt_stride, max_pages, sel_stride;
+  int est_in_smem;       // the selection kernel keeps every page's estimate in shared memory
   float scale, alpha;
 };
 
@@ -57,8 +59,7 @@ __global__ void __launch_bounds__(kMomThreads) gauss_moments_kernel(GaussArgs a)
   const int G = a.G;
   const uint16_t* qb = static_cast<const uint16_t*>(a.q) + (int64_t(b) * a.H_q + int64_t(h) * G) * D;
   for (int i = tid; i < G * D; i += kMomThreads) {
-    const uint16_t x = qb[i];
-    reinterpret_cast<float*>(s_q)[(i / D) * D + (i % D)] = a.scale * E::lo(uint32_t(x));
+    reinterpret_cast<float*>(s_q)[i] = a.scale * E::lo(uint32_t(qb[i]));
   }
   __syncthreads();
   const int L = a.seq_lens[b];
@@ -144,6 +145,12 @@ __device__ __forceinline__ void tail_moment(float mu_a, float s_a, float t, bool
   }
 }
 
+// the page's estimated maximum score m + sqrt(2 ln f) sqrt(v)
+__device__ __forceinline__ float est_max(float2 mv, int f) {
+  const float kappa = f > 1 ? sqrtf(2.0f * logf(float(f))) : 0.f;
+  return mv.x + kappa * sqrtf(fmaxf(mv.y, 0.f));
+}
+
 __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) {
   __shared__ double s_red[kSelWarps][3];
   __shared__ int s_cnt[kSelWarps];
@@ -163,12 +170,18 @@ __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) 
     }
     return;
   }
-  // the mixture's moments
+  // the mixture's moments; each page's estimated maximum kept for the selection
+  extern __shared__ float s_est[];                          // [max_pages] when it fits, else unused
+  const bool cached = a.est_in_smem;
   float f_s = 0.f, s1 = 0.f, c1 = 0.f, s2 = 0.f, c2 = 0.f;
+#pragma unroll 4
   for (int p = tid; p < n; p += kSelThreads) {
     const float2 mv = mom[p];
-    if (!(mv.x > -INFINITY && mv.x < INFINITY)) continue;
-    const float f = float(min(a.ps, L - (p << a.ps_shift)));
+    const bool ok = mv.x > -INFINITY && mv.x < INFINITY;
+    const int fi = min(a.ps, L - (p << a.ps_shift));
+    if (cached) s_est[p] = ok ? est_max(mv, fi) : -INFINITY;
+    if (!ok) continue;
+    const float f = float(fi);
     f_s += f;
     csum(s1, c1, f * mv.x);
     csum(s2, c2, f * (mv.y + mv.x * mv.x));
@@ -209,11 +222,15 @@ __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) 
   const float tau = s_tau, am1 = a.alpha - 1.0f;
   auto keep_of = [&](int p) -> bool {
     if (p == n - 1) return true;                            // the tail page
-    const float2 mv = mom[p];
-    if (!(mv.x > -INFINITY && mv.x < INFINITY)) return false;
-    const int f = min(a.ps, L - (p << a.ps_shift));
-    const float kappa = f > 1 ? sqrtf(2.0f * logf(float(f))) : 0.f;
-    return am1 * (mv.x + kappa * sqrtf(fmaxf(mv.y, 0.f))) > tau;
+    float e;
+    if (cached) {
+      e = s_est[p];
+    } else {
+      const float2 mv = mom[p];
+      if (!(mv.x > -INFINITY && mv.x < INFINITY)) return false;
+      e = est_max(mv, min(a.ps, L - (p << a.ps_shift)));
+    }
+    return am1 * e > tau;
   };
   // kept pages in page order: warp w owns pages [w seg, (w + 1) seg)
   const int seg = (((n + kSelWarps - 1) / kSelWarps) + 31) & ~31;
@@ -241,17 +258,20 @@ __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) 
   if (tid == 0) a.cnt[row] = total;
 }
 
+int g_mom_smem[12][64];
+
 template <typename T, int D, int kG>
-sa_status launch_moments(const GaussArgs& a, dim3 grid, cudaStream_t s) {
+sa_status launch_moments(const GaussArgs& a, dim3 grid, cudaStream_t s, int* attr) {
+  if (!ensure_smem(gauss_moments_kernel<T, D, kG>, 0, attr)) return SA_ERR_CUDA;
   gauss_moments_kernel<T, D, kG><<<grid, kMomThreads, 0, s>>>(a);
   return launch_status();
 }
 
 template <typename T, int D>
-sa_status launch_moments_g(const GaussArgs& a, dim3 grid, cudaStream_t s) {
-  if (a.G <= 4) return launch_moments<T, D, 4>(a, grid, s);
-  if (a.G <= 8) return launch_moments<T, D, 8>(a, grid, s);
-  return launch_moments<T, D, 16>(a, grid, s);
+sa_status launch_moments_g(const GaussArgs& a, dim3 grid, cudaStream_t s, int slot) {
+  if (a.G <= 4) return launch_moments<T, D, 4>(a, grid, s, g_mom_smem[slot * 3 + 0]);
+  if (a.G <= 8) return launch_moments<T, D, 8>(a, grid, s, g_mom_smem[slot * 3 + 1]);
+  return launch_moments<T, D, 16>(a, grid, s, g_mom_smem[slot * 3 + 2]);
 }
 
 }  // namespace
@@ -287,10 +307,15 @@ extern "C" sa_status sa_gauss_select(const sa_cache* cache, const sa_batch* batc
                    unsigned(batch->batch));
   const bool bf = cache->dtype == SA_BF16;
   if (cache->head_dim == 128)
-    st = bf ? launch_moments_g<__nv_bfloat16, 128>(a, mgrid, s) : launch_moments_g<__half, 128>(a, mgrid, s);
+    st = bf ? launch_moments_g<__nv_bfloat16, 128>(a, mgrid, s, 0) : launch_moments_g<__half, 128>(a, mgrid, s, 1);
   else
-    st = bf ? launch_moments_g<__nv_bfloat16, 64>(a, mgrid, s) : launch_moments_g<__half, 64>(a, mgrid, s);
+    st = bf ? launch_moments_g<__nv_bfloat16, 64>(a, mgrid, s, 2) : launch_moments_g<__half, 64>(a, mgrid, s, 3);
   if (st != SA_OK) return st;
-  gauss_select_kernel<<<dim3(unsigned(num_q_heads), unsigned(batch->batch)), kSelThreads, 0, s>>>(a);
+  static int g_sel_smem[64];
+  const int est_bytes = max_pages * int(sizeof(float));
+  a.est_in_smem = est_bytes <= 160 * 1024;
+  const int smem = a.est_in_smem ? est_bytes : 0;
+  if (!ensure_smem(gauss_select_kernel, smem, g_sel_smem)) return SA_ERR_CUDA;
+  gauss_select_kernel<<<dim3(unsigned(num_q_heads), unsigned(batch->batch)), kSelThreads, smem, s>>>(a);
   return launch_status();
 }

@@ -101,6 +101,8 @@ class SparseDecoder:
             self.sel_cnt = torch.zeros((batch, num_q_heads), **i32)
             self.tau_hat = torch.empty((batch, num_q_heads), dtype=torch.float32, device=device)
             self.tau = torch.empty((batch, num_q_heads), dtype=torch.float32, device=device)
+            self.logits = torch.empty((batch, num_q_heads, bt_stride * page_size),
+                                      dtype=torch.float32, device=device)
             self.ent_ws = alloc_entmax_workspace(batch, num_q_heads, num_q_heads, head_dim,
                                                  page_size, bt_stride, device)
         if self.entmax:
@@ -171,8 +173,9 @@ class SparseDecoder:
                             self.sel_stride, tau_hat=self.tau_hat, dev_status=self.dev_status)
             sa_sparse_decode_entmax_qh(self.cache.struct, self.batch, q, self.H_q, self.sel_idx,
                                        self.sel_cnt, self.sel_stride, self.alpha, self.scale,
-                                       self.out, tau=self.tau, workspace=self.ent_ws,
-                                       dev_status=self.dev_status)
+                                       self.out, tau=self.tau, logits=self.logits,
+                                       logits_stride=self.sel_stride * self.ps,
+                                       workspace=self.ent_ws, dev_status=self.dev_status)
         elif self.qh:
             sa_score_pages_qh(self.cache.struct, self.batch, q, self.H_q, self.w_avg, self.w_peak,
                               self.scores, self.max_pages, dev_status=self.dev_status)

@@ -199,3 +199,36 @@ def test_full_long_context_entmax(alpha):
 
     _graph_steps(dec, wl, 4, True, check)
     assert dev_status(dec) == 0
+
+
+def test_full_long_context_gaussian():
+    """The long-context workload with Gaussian-aware selection per query head
+    (graph replay, one-token appends): sampled heads' moments, threshold and
+    selection against the oracle, and the attention over the GPU's selection."""
+    from test_gpu_gauss import _check_selection
+    wl = make_workload(config(5))
+    c = wl.cfg
+    dec = make_decoder(wl, stale="nan", extra=dict(gaussian=True, alpha=1.5))
+    heads = [(0, 0), (1, 17), (3, 63)]
+    sc = c.scale if c.scale > 0 else O.default_scale(c.D)
+
+    def check(t):
+        assert torch.isfinite(dec.out.float()).all()
+        cnt = dec.sel_cnt.cpu().numpy()
+        assert np.all(cnt >= 1)
+        if t not in (0, 2):
+            return
+        assert _check_selection(dec, wl, t + 1, wl.q(t), 1.5, heads) >= len(heads) - 1
+        sel = dec.sel_idx.cpu().numpy()
+        out = dec.out.float().cpu().numpy()
+        for b, gq in heads:
+            h = gq // c.G
+            L = wl.seq_len(b, t + 1)
+            pos = O.selected_positions(sel[b, gq, :cnt[b, gq]], L, c.ps)
+            k = O.decode_kdt(wl.k_seq(b, t + 1)[:, h, :][pos], c.dtype)
+            v = O.decode_kdt(wl.v_seq(b, t + 1)[:, h, :][pos], c.dtype)
+            o, _, _ = O.attention_entmax(O.decode_kdt(wl.q(t)[b, gq], c.dtype)[None], k, v, sc, 1.5)
+            assert_attention(out[b, gq][None], o)
+
+    _graph_steps(dec, wl, 3, True, check)
+    assert dev_status(dec) == 0
