@@ -39,6 +39,7 @@ constexpr int kMaxIter = 100;
 constexpr int kRowReg = 16;              // row entries per thread the tau kernel keeps in registers
 constexpr int kSortMax = kWarps * kCand; // every gathered candidate can be ranked
 constexpr int kRankDirect = 128;         // up to this many candidates: rank by direct counting
+constexpr int kPrefilterRounds = 3;      // Newton rounds that thin a larger candidate set first
 static_assert(kCand == 256, "the per-warp sort holds 8 candidates a lane");
 
 struct EntArgs {
@@ -370,7 +371,50 @@ __global__ void __launch_bounds__(kThreads) entmax_tau_kernel(EntArgs a) {
     } else if (kind == 0 || m > kSortMax) {
       if (warp != 0) return;
       tau = solve_gathered(s_c, s_n, mx - 1.0f, kind, r);
-    } else if (m > kRankDirect) {
+    } else {
+      if (m > kRankDirect) {
+        // Shrink the set first: Newton's method from a_max - 1 stays left of
+        // the root, so after a few rounds every support member still lies
+        // above the iterate (less a margin for float32 rounding) and the
+        // entries at or below it can be dropped.
+        if (warp == 0) {
+          float t = mx - 1.0f;
+          for (int it = 0; it < kPrefilterRounds; ++it) {
+            Sums su = {0.f, 0.f, 0.f, INFINITY, -INFINITY};
+            float c0 = 0.f, c1 = 0.f;
+            for (int w = 0; w < kWarps; ++w)
+              for (int j = lane; j < s_n[w]; j += 32) add_entry(s_c[w][j], t, kind, r, su, c0, c1);
+            su.p0 = warp_sum_f(su.p0 + c0);
+            su.p1 = warp_sum_f(su.p1 + c1);
+            const float f = su.p0 - 1.f;
+            if (!(f > 0.f) || !(su.p1 > 0.f)) break;
+            t += f / (r * su.p1);
+          }
+          if (lane == 0) s_mx[0] = t - 1e-4f * (1.f + fabsf(t));
+        }
+        __syncthreads();
+        const float t_lo = s_mx[0];
+        // each warp compacts its own run in place (order kept; writes never pass reads)
+        const int nw = s_n[warp];
+        int kept = 0;
+        for (int j0 = 0; j0 < nw; j0 += 32) {
+          const int j = j0 + lane;
+          const float x = j < nw ? s_c[warp][j] : -INFINITY;
+          const bool take = x > t_lo;
+          const unsigned bal = __ballot_sync(kFull, take);
+          __syncwarp();
+          if (take) s_c[warp][kept + __popc(bal & ((1u << lane) - 1u))] = x;
+          kept += __popc(bal);
+          __syncwarp();
+        }
+        __syncthreads();                                    // every warp has read the old counts
+        if (lane == 0) s_n[warp] = kept;
+        __syncthreads();
+        m = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) m += s_n[w];
+      }
+      if (m > kRankDirect) {
       // each warp sorts its own candidates, then an entry's rank is its place
       // in its run plus the entries above it in the other runs (ties: runs
       // in warp order), every rank distinct
@@ -400,7 +444,7 @@ __global__ void __launch_bounds__(kThreads) entmax_tau_kernel(EntArgs a) {
       __syncthreads();
       if (warp != 0) return;
       tau = mx + tau_sorted(s_srt, m, kind);
-    } else {
+      } else {
       // rank of each candidate among all: larger value first, ties by gather position
       for (int ci = tid; ci < m; ci += kThreads) {
         int w = 0, off = 0;
@@ -420,6 +464,7 @@ __global__ void __launch_bounds__(kThreads) entmax_tau_kernel(EntArgs a) {
       __syncthreads();
       if (warp != 0) return;
       tau = mx + tau_sorted(s_srt, m, kind);
+      }
     }
   }
   if (tid == 0) {
