@@ -23,6 +23,8 @@
  *   sa_sparse_decode_entmax, sa_sparse_decode_entmax_qh, sa_entmax_workspace_size
  *                     attention over the selection with alpha-entmax
  *   sa_gauss_select   Gaussian-aware adaptive page selection per query head
+ *   sa_shard_lengths, sa_shard_selection, sa_merge_states
+ *                     sequence sharding: page ranges per shard, merged states
  *
  * Sources (cited by page title and section):
  *   [vortex]  "flow: add H2O sparse attention (page-level and token-level,
@@ -542,6 +544,41 @@ sa_status sa_gauss_select(const sa_cache* cache, const sa_batch* batch, const vo
                           int32_t num_q_heads, float alpha, float scale, float* moments,
                           int32_t max_pages, int32_t* sel_idx, int32_t* sel_cnt,
                           int32_t sel_stride, float* tau_hat, int32_t* dev_status, void* stream);
+
+/*
+ * Sequence sharding -- the pages of every request split into contiguous
+ * ranges [page_lo, page_hi) held by different shards (devices).
+ *
+ * [vllmcpp] MergeAttnStates: attention over a split of the keys is exact once
+ * the partial states are merged by log-sum-exp. [entmax] "Top-k": the
+ * selection is over the whole request, tail forced. A sharded step: each
+ * shard computes the lengths of its range (sa_shard_lengths), scores its
+ * pages with sa_score_pages on a batch view (block_table + page_lo, the same
+ * bt_stride, its lengths), the score slices are gathered into one row per
+ * (request, KV head) (the exchange), one sa_select_topk runs over the whole
+ * rows, each shard takes its part of the selection (sa_shard_selection) and
+ * attends it with sa_sparse_decode (o and lse), and the parts are merged by
+ * sa_merge_states. Appends are not sharded here.
+ *
+ * sa_shard_lengths: shard_lens[b] = clamp(seq_lens[b] - page_lo * page_size,
+ *   0, (page_hi - page_lo) * page_size); device arrays [batch] int32.
+ * sa_shard_selection: for each of num_units rows of sel_idx [num_units,
+ *   sel_stride] (counts sel_cnt), the entries with page_lo <= p < page_hi as
+ *   p - page_lo, in order, into shard_idx [num_units, shard_stride] and
+ *   shard_cnt; entries beyond shard_stride set SA_DEV_OVERFLOW.
+ * sa_merge_states: o_parts [num_shards, rows, head_dim] (dtype), lse_parts
+ *   [num_shards, rows] float32 (natural log; -inf for an empty part) ->
+ *   out [rows, head_dim] (dtype) and lse (nullable) [rows]; all parts empty
+ *   gives o = 0, lse = -inf.
+ */
+sa_status sa_shard_lengths(const int32_t* seq_lens, int32_t batch, int32_t page_size, int32_t page_lo,
+                           int32_t page_hi, int32_t* shard_lens, void* stream);
+sa_status sa_shard_selection(const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_stride,
+                             int32_t num_units, int32_t page_lo, int32_t page_hi, int32_t* shard_idx,
+                             int32_t* shard_cnt, int32_t shard_stride, int32_t* dev_status,
+                             void* stream);
+sa_status sa_merge_states(const void* o_parts, const float* lse_parts, int32_t num_shards, int32_t rows,
+                          int32_t head_dim, int32_t dtype, void* out, float* lse, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* sa_status_string(sa_status status);

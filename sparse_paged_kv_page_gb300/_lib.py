@@ -74,6 +74,10 @@ SIGNATURES = {
                                            c_ptr, c_ptr]),
     "sa_gauss_select": (c_i32, [P_CACHE, P_BATCH, c_ptr, c_i32, c_f32, c_f32, c_ptr, c_i32, c_ptr,
                                 c_ptr, c_i32, c_ptr, c_ptr, c_ptr]),
+    "sa_shard_lengths": (c_i32, [c_ptr, c_i32, c_i32, c_i32, c_i32, c_ptr, c_ptr]),
+    "sa_shard_selection": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_i32, c_i32, c_ptr, c_ptr, c_i32, c_ptr,
+                                   c_ptr]),
+    "sa_merge_states": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_i32, c_i32, c_ptr, c_ptr, c_ptr]),
     "sa_struct_size": (c_size, [c_i32]),
     "sa_status_string": (ctypes.c_char_p, [c_i32]),
     "sa_version": (ctypes.c_char_p, []),

@@ -22,7 +22,8 @@ __all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKV
            "sa_select_topk_reserved", "sa_h2o_update_window", "sa_score_pages_qh",
            "sa_sparse_decode_qh", "sa_h2o_prefill", "sa_entmax_workspace_size",
            "alloc_entmax_workspace", "sa_sparse_decode_entmax", "sa_sparse_decode_entmax_qh",
-           "sa_gauss_select",
+           "sa_gauss_select", "sa_shard_lengths", "sa_shard_selection", "sa_merge_states",
+           "batch_view",
            "sa_status_string", "sa_struct_size",
            "sa_version", "alloc_decode_workspace"]
 
@@ -271,6 +272,46 @@ def sa_gauss_select(cache: SaCache, batch: SaBatch, q, num_q_heads: int, alpha: 
         _p(sel_idx, torch.int32, "sel_idx"), _p(sel_cnt, torch.int32, "sel_cnt"), int(sel_stride),
         _p(tau_hat, torch.float32, "tau_hat"), _p(dev_status, torch.int32, "dev_status"),
         _s(stream)))
+
+
+def sa_shard_lengths(seq_lens, batch: int, page_size: int, page_lo: int, page_hi: int, shard_lens,
+                     stream=None):
+    _check("sa_shard_lengths", _lib.load().sa_shard_lengths(
+        _p(seq_lens, torch.int32, "seq_lens"), int(batch), int(page_size), int(page_lo), int(page_hi),
+        _p(shard_lens, torch.int32, "shard_lens"), _s(stream)))
+
+
+def sa_shard_selection(sel_idx, sel_cnt, sel_stride: int, num_units: int, page_lo: int, page_hi: int,
+                       shard_idx, shard_cnt, shard_stride: int, dev_status=None, stream=None):
+    _check("sa_shard_selection", _lib.load().sa_shard_selection(
+        _p(sel_idx, torch.int32, "sel_idx"), _p(sel_cnt, torch.int32, "sel_cnt"), int(sel_stride),
+        int(num_units), int(page_lo), int(page_hi), _p(shard_idx, torch.int32, "shard_idx"),
+        _p(shard_cnt, torch.int32, "shard_cnt"), int(shard_stride),
+        _p(dev_status, torch.int32, "dev_status"), _s(stream)))
+
+
+def sa_merge_states(o_parts, lse_parts, num_shards: int, rows: int, head_dim: int, out, lse=None,
+                    stream=None):
+    if o_parts.dtype not in _DT or out.dtype != o_parts.dtype:
+        raise ValueError("o_parts and out must share a bf16/fp16 dtype")
+    _check("sa_merge_states", _lib.load().sa_merge_states(
+        _p(o_parts, name="o_parts"), _p(lse_parts, torch.float32, "lse_parts"), int(num_shards),
+        int(rows), int(head_dim), _DT[o_parts.dtype], _p(out, name="out"),
+        _p(lse, torch.float32, "lse"), _s(stream)))
+
+
+def batch_view(block_table: torch.Tensor, seq_lens: torch.Tensor, page_lo: int) -> SaBatch:
+    """Struct view of pages [page_lo, ...) of every row of block_table [B, bt_stride]
+    (the same row stride), with the shard's own lengths seq_lens [B]."""
+    if block_table.dtype != torch.int32 or not block_table.is_contiguous() or block_table.dim() != 2:
+        raise ValueError("block_table must be contiguous int32 [B, bt_stride]")
+    if not 0 <= page_lo < block_table.shape[1]:
+        raise ValueError("page_lo outside the table")
+    b = SaBatch(ctypes.c_void_p(block_table.data_ptr() + 4 * int(page_lo)),
+                _p(seq_lens, torch.int32, "seq_lens"), int(block_table.shape[0]),
+                int(block_table.shape[1]))
+    b._keep = (block_table, seq_lens)
+    return b
 
 
 def sa_sparse_decode_noalloc(cache: SaCache, batch: SaBatch, q, num_q_heads: int, sel_idx,

@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "_sparse_attn.so")
 SOURCES = ["append.cu", "score.cu", "select.cu", "decode.cu", "h2o.cu", "h2o_proxy.cu", "step.cu",
-           "entmax.cu", "gauss.cu", "api.cu"]
+           "entmax.cu", "gauss.cu", "shard.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
                  "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

@@ -1,0 +1,98 @@
+"""Sequence sharding of the page-level read path on one GPU: every request's
+pages split over S page ranges of one cache, each range scored and attended
+as its own shard, one top-k over the gathered score rows, the partial states
+merged by log-sum-exp ("MergeAttnStates" of the vllm.cpp chunked-context
+test). The scores and the selection must equal the unsharded step's bit for
+bit; the output must match the oracle's attention over that selection.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from sa_synth import config, make_workload
+from gpu_util import make_decoder, dev_bits, dev_status, host_bits, assert_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("cid,S", [(5, 2), (5, 3), (3, 4), (2, 5), (1, 3)])
+def test_sharded_step_equals_the_unsharded_one(cid, S):
+    from sparse_paged_kv_page_gb300.shard import SequenceShards
+    wl = make_workload(config(cid, small=True))
+    c = wl.cfg
+    dec = make_decoder(wl)
+    sh = SequenceShards(dec, S)
+    q = dev_bits(wl.q(0), c.dtype)
+    out_s = sh.attend(q).clone()
+    lse_s = sh.lse.clone()
+    dec.attend(q)
+    torch.cuda.synchronize()
+    scores_d, scores_s = dec.scores.cpu().numpy(), sh.scores.cpu().numpy()
+    for b in range(c.B):
+        n = O.num_pages(int(wl.prefill_lens[b]), c.ps)
+        assert np.array_equal(scores_d[b, :, :n].view(np.uint32), scores_s[b, :, :n].view(np.uint32))
+    assert torch.equal(dec.sel_cnt, sh.sel_cnt)
+    for b in range(c.B):
+        for h in range(c.H_kv):
+            k = int(dec.sel_cnt[b, h])
+            assert torch.equal(dec.sel_idx[b, h, :k], sh.sel_idx[b, h, :k])
+    # every selected page went to exactly one shard
+    got = sum(int(x.sum()) for x in sh.shard_cnt)
+    assert got == int(sh.sel_cnt.sum())
+    # the merged output against the oracle over the same selection
+    sel = sh.sel_idx.cpu().numpy()
+    cnt = sh.sel_cnt.cpu().numpy()
+    o = out_s.float().cpu().numpy()
+    lse = lse_s.cpu().numpy()
+    sc = c.scale if c.scale > 0 else O.default_scale(c.D)
+    qb = wl.q(0)
+    for b in range(c.B):
+        L = int(wl.prefill_lens[b])
+        for h in range(c.H_kv):
+            pos = O.selected_positions(sel[b, h, :cnt[b, h]], L, c.ps)
+            k = O.decode_kdt(wl.k_seq(b)[:, h, :][pos], c.dtype)
+            v = O.decode_kdt(wl.v_seq(b)[:, h, :][pos], c.dtype)
+            rows = slice(h * c.G, (h + 1) * c.G)
+            ow, lw, _ = O.attention(O.decode_kdt(qb[b, rows], c.dtype), k, v, sc)
+            assert_attention(o[b, rows], ow, lse[b, rows], lw)
+    assert dev_status(dec) == 0
+
+
+def test_merge_states_against_the_oracle():
+    from sparse_paged_kv_page_gb300 import sa_merge_states
+    rng = np.random.default_rng(3)
+    S, rows, D = 4, 37, 128
+    o_parts = rng.standard_normal((S, rows, D)).astype(np.float32)
+    lse = rng.normal(0, 3, size=(S, rows)).astype(np.float32)
+    lse[1, :5] = -np.inf                                   # empty parts
+    lse[:, 7] = -np.inf                                    # every part empty
+    lse[2, 9] = np.inf                                     # counted as empty
+    ob = torch.from_numpy(o_parts).to(torch.bfloat16).cuda()
+    out = torch.empty((rows, D), dtype=torch.bfloat16, device="cuda")
+    lse_out = torch.empty(rows, device="cuda")
+    sa_merge_states(ob, torch.from_numpy(lse).cuda(), S, rows, D, out, lse=lse_out)
+    torch.cuda.synchronize()
+    o_in = ob.float().cpu().numpy().astype(np.float64)
+    want = np.zeros((rows, D)); wl = np.zeros(rows)
+    for r in range(rows):
+        w_o, w_l = O.merge_partials(o_in[:, r][:, None, :], lse[:, r][:, None])
+        want[r], wl[r] = w_o[0], w_l[0]
+    assert_attention(out.float().cpu().numpy(), want, lse_out.cpu().numpy(), wl, atol=1e-2, rtol=1e-2)
+    assert torch.all(out[7].float() == 0) and lse_out[7].item() == -np.inf
+
+
+def test_shard_selection_splits_in_order():
+    from sparse_paged_kv_page_gb300 import sa_shard_selection
+    sel = torch.tensor([[0, 3, 4, 9, 10, 15, -1, -1], [2, 5, 6, 7, 8, 11, 12, 13]], dtype=torch.int32,
+                       device="cuda")
+    cnt = torch.tensor([6, 8], dtype=torch.int32, device="cuda")
+    ranges = [(0, 5), (5, 10), (10, 16)]
+    want = [[[0, 3, 4], [2]], [[4], [0, 1, 2, 3]], [[0, 5], [1, 2, 3]]]
+    for (lo, hi), w in zip(ranges, want):
+        idx = torch.full((2, 8), -7, dtype=torch.int32, device="cuda")
+        c = torch.zeros(2, dtype=torch.int32, device="cuda")
+        sa_shard_selection(sel, cnt, 8, 2, lo, hi, idx, c, 8)
+        torch.cuda.synchronize()
+        for u in range(2):
+            assert idx[u, :int(c[u])].tolist() == w[u]

@@ -91,3 +91,43 @@ def test_reference_arm_is_rank_zero_only():
                        timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def _gather_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    from sparse_paged_kv_page_gb300.shard import gather_slices, page_ranges
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # the score rows of 3 requests x 2 KV heads over 12 pages, split by rank
+        full = torch.arange(3 * 2 * 12, dtype=torch.float32).reshape(3, 2, 12)
+        lo, hi = page_ranges(12, world)[rank]
+        got = gather_slices(full[:, :, lo:hi].clone(), dim=2)
+        q.put((rank, torch.equal(got, full)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sequence_shards_exchange_score_rows_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gather_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=240) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(0, True), (1, True)]
+
+
+def test_page_ranges_cover_the_pages():
+    sys.path.insert(0, ROOT)
+    from sparse_paged_kv_page_gb300.shard import page_ranges
+    for n, s in [(12, 2), (13, 5), (1, 1), (8194, 3)]:
+        r = page_ranges(n, s)
+        assert r[0][0] == 0 and r[-1][1] == n and all(a[1] == b[0] for a, b in zip(r, r[1:]))
+        assert max(h - l for l, h in r) - min(h - l for l, h in r) <= 1
