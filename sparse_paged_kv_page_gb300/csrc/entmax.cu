@@ -23,8 +23,11 @@
 //      KV head): each warp tests 32 tokens at a time against the G heads' tau
 //      and loads V rows only for tokens some head of the group keeps
 //      (entmax is sparse), accumulating sum_j p_j v_j and sum_j p_j in fp32;
-//      the last CTA of a (request, KV head) adds the splits in a fixed order
-//      and divides by sum_j p_j (1 up to the rounding of tau).
+//      the splits of a (request, KV head), at most 8, form a thread-block
+//      cluster and add their partials over distributed shared memory in a
+//      fixed order (where a cluster cannot launch, the last CTA adds them
+//      from the workspace), dividing by sum_j p_j (1 up to the rounding of
+//      tau).
 #include "common.cuh"
 #include "host.h"
 
@@ -33,6 +36,7 @@ namespace {
 
 
 constexpr int kThreads = 256;
+constexpr int kMaxClusterSplits = 8;     // splits of a unit merged inside one (portable) cluster
 constexpr int kWarps = kThreads / 32;
 constexpr int kCand = 256;               // candidates each warp of the tau kernel gathers (beyond: the row is streamed)
 constexpr int kMaxIter = 100;
@@ -473,7 +477,7 @@ __global__ void __launch_bounds__(kThreads) entmax_tau_kernel(EntArgs a) {
   }
 }
 
-template <typename T, int D, int kG>
+template <typename T, int D, int kG, bool kCluster>
 __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
   using E = Elem<T>;
   constexpr int DPL = D / 32;                              // dims per lane: 4 (D 128) or 2 (D 64)
@@ -620,6 +624,57 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
     for (int w = 0; w < kWarps; ++w) sum += s_red[kWarps * G * D + w * G + tid];
     a.part_l[prow + int64_t(tid) * a.nsplit + split] = sum;
   }
+  T* outp = static_cast<T*>(a.out) + (int64_t(b) * a.H_q + int64_t(h) * G) * D;
+  if (a.nsplit == 1) {                                     // one split: normalise and write
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      float o = 0.f, l = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        o += s_red[w * G * D + idx];
+        l += s_red[kWarps * G * D + w * G + idx / D];
+      }
+      reinterpret_cast<uint16_t*>(outp)[idx] = E::from_f(l > 0.f ? o / l : 0.f);
+    }
+    return;
+  }
+  if constexpr (kCluster) {
+    // The unit's splits form one cluster: each leaves its partial (sum p v,
+    // sum p) in its own shared memory; after a cluster barrier each CTA adds
+    // a 1/nsplit slice of the G*D outputs over every peer's partial (DSMEM,
+    // all loads in flight at once); a second barrier keeps the partials alive
+    // until every peer has read them.
+    float* s_cl = reinterpret_cast<float*>(s_ent + a.ent_cap);   // [G][D], then [G]
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      float o = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) o += s_red[w * G * D + idx];
+      s_cl[idx] = o;
+    }
+    if (tid < G) {
+      float l = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) l += s_red[kWarps * G * D + w * G + tid];
+      s_cl[G * D + tid] = l;
+    }
+    cluster_sync();
+    const int ns = a.nsplit, n_el = G * D, chunk = (n_el + ns - 1) / ns;
+    const int e0 = int(cluster_rank()) * chunk, e1 = min(n_el, e0 + chunk);
+    const uint32_t base = smem_u32(s_cl);
+    for (int idx = e0 + tid; idx < e1; idx += kThreads) {
+      float ov[kMaxClusterSplits], lv[kMaxClusterSplits];
+#pragma unroll
+      for (int r = 0; r < kMaxClusterSplits; ++r) {
+        ov[r] = r < ns ? dsmem_ld_f32(dsmem_map(base + 4u * idx, r)) : 0.f;
+        lv[r] = r < ns ? dsmem_ld_f32(dsmem_map(base + 4u * (n_el + idx / D), r)) : 0.f;
+      }
+      float o = 0.f, l = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxClusterSplits; ++r) { o += ov[r]; l += lv[r]; }   // split order
+      reinterpret_cast<uint16_t*>(outp)[idx] = E::from_f(l > 0.f ? o / l : 0.f);
+    }
+    cluster_sync();
+    return;
+  }
   // the last split of this (request, KV head) adds the partials in split order
   __threadfence();
   __syncthreads();
@@ -645,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
     for (int s = 0; s < a.nsplit; ++s) o += __ldcg(src + int64_t(s) * D);
     const float l = s_l[g];
     const float y = l > 0.f ? o / l : 0.f;                 // no kept token: 0
-    reinterpret_cast<uint16_t*>(a.out)[(int64_t(b) * a.H_q + int64_t(h) * G + g) * D + d] = E::from_f(y);
+    reinterpret_cast<uint16_t*>(outp)[g * D + d] = E::from_f(y);
   }
   if (tid == 0) a.tickets[b * a.H_u + h] = 0;             // ready for the next call
 }
@@ -671,7 +726,7 @@ struct EntLayout {
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // splits: as many as fit two CTAs per SM in one wave over all (request, KV
-// head) units, at least 128 tokens a split
+// head) units, at least 128 tokens a split, at most one cluster's worth
 EntLayout ent_layout(int B, int H_kv, int H_q, int D, int ps, int sel_stride, int sms) {
   EntLayout w;
   const int64_t rows = int64_t(sel_stride) * ps;
@@ -679,7 +734,7 @@ EntLayout ent_layout(int B, int H_kv, int H_q, int D, int ps, int sel_stride, in
   int ns = (2 * sms) / units;
   const int64_t by_len = (rows + 127) / 128;
   if (ns > by_len) ns = int(by_len);
-  if (ns > 64) ns = 64;
+  if (ns > kMaxClusterSplits) ns = kMaxClusterSplits;
   if (ns < 1) ns = 1;
   w.nsplit = ns;
   const int64_t per = (((rows + ns - 1) / ns) + 31) & ~int64_t(31);
@@ -694,17 +749,23 @@ EntLayout ent_layout(int B, int H_kv, int H_q, int D, int ps, int sel_stride, in
   return w;
 }
 
-int g_att_smem[16][64];
+int g_att_smem[16][128];                  // [variant][device] ticket kernels, [variant][64 + device] cluster
 
 template <typename T, int D, int kG>
 sa_status launch_attend(const EntArgs& a, dim3 grid, cudaStream_t s, int* attr) {
-  const int smem = kWarps * a.G * (D + 1) * int(sizeof(float)) + a.ent_cap * int(sizeof(int2));
+  const int smem = (kWarps + 1) * a.G * (D + 1) * int(sizeof(float)) + a.ent_cap * int(sizeof(int2));
   if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;
-  if (!ensure_smem(entmax_attend_kernel<T, D, kG>, smem, attr)) return SA_ERR_CUDA;
-  return launch_ex(entmax_attend_kernel<T, D, kG>, grid, dim3(kThreads), size_t(smem), s, true, 1u,
-                   a) == cudaSuccess
-             ? SA_OK
-             : SA_ERR_CUDA;
+  if (a.nsplit > 1) {                                      // the cluster merge where it can launch
+    auto kc = entmax_attend_kernel<T, D, kG, true>;
+    if (ensure_smem(kc, smem, attr + 64) &&
+        launch_ex(kc, grid, dim3(kThreads), size_t(smem), s, true, unsigned(a.nsplit), a) == cudaSuccess)
+      return SA_OK;
+    (void)cudaGetLastError();                              // refused: the ticket merge
+  }
+  auto kt = entmax_attend_kernel<T, D, kG, false>;
+  if (!ensure_smem(kt, smem, attr)) return SA_ERR_CUDA;
+  return launch_ex(kt, grid, dim3(kThreads), size_t(smem), s, true, 1u, a) == cudaSuccess ? SA_OK
+                                                                                      : SA_ERR_CUDA;
 }
 
 template <typename T, int D>
@@ -755,7 +816,7 @@ sa_status entmax_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   const EntLayout w = ent_layout(batch->batch, H_u, num_q_heads, cache->head_dim, cache->page_size,
                                  sel_stride, device_sms());
   if (!workspace || workspace_bytes < w.total) return SA_ERR_WORKSPACE;
-  const int64_t smem = int64_t(kWarps) * G * (cache->head_dim + 1) * 4 + int64_t(w.ent_cap) * 8;
+  const int64_t smem = int64_t(kWarps + 1) * G * (cache->head_dim + 1) * 4 + int64_t(w.ent_cap) * 8;
   if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;       // (checked before any launch)
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* lg = logits ? logits : reinterpret_cast<float*>(ws + w.logits);
