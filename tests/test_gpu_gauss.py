@@ -188,3 +188,38 @@ def test_gauss_select_rejects_before_launching():
         sa_gauss_select(plain.cache.struct, plain.batch, q, c.H_q, 1.5, dec.scale, dec.moments,
                         dec.max_pages, dec.sel_idx, dec.sel_cnt, dec.sel_stride)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("alpha", [1.5, 2.0])
+def test_gaussian_head_dim_64_and_an_empty_request(alpha):
+    """D = 64, and a batch whose first request holds no tokens: that request
+    selects nothing (count 0, tau_hat NaN) and its output is 0; the others
+    match the oracle."""
+    cfg = config(3, small=True).replace(D=64, len_range=(40, 700))
+    wl = make_workload(cfg)
+    c = wl.cfg
+    dec = make_decoder(wl, extra=dict(gaussian=True, alpha=alpha))
+    lens = dec.seq_lens.clone()
+    dec.seq_lens[0] = 0                                     # an empty request
+    q = dev_bits(wl.q(0), c.dtype)
+    dec.attend(q)
+    torch.cuda.synchronize()
+    assert int(dec.sel_cnt[0].abs().sum()) == 0
+    assert torch.isnan(dec.tau_hat[0]).all()
+    assert torch.all(dec.out[0].float() == 0)
+    heads = [(b, g) for b in range(1, c.B) for g in range(c.H_q)]
+    assert _check_selection(dec, wl, 0, wl.q(0), alpha, heads) >= 0.9 * len(heads)
+    sel = dec.sel_idx.cpu().numpy()
+    cnt = dec.sel_cnt.cpu().numpy()
+    out = dec.out.float().cpu().numpy()
+    sc = _scale(c)
+    for b, gq in heads:
+        h = gq // c.G
+        L = int(wl.prefill_lens[b])
+        pos = O.selected_positions(sel[b, gq, :cnt[b, gq]], L, c.ps)
+        k = O.decode_kdt(wl.k_seq(b)[:, h, :][pos], c.dtype)
+        v = O.decode_kdt(wl.v_seq(b)[:, h, :][pos], c.dtype)
+        o, _, _ = O.attention_entmax(O.decode_kdt(wl.q(0)[b, gq], c.dtype)[None], k, v, sc, alpha)
+        assert_attention(out[b, gq][None], o)
+    dec.seq_lens.copy_(lens)
+    assert dev_status(dec) == 0

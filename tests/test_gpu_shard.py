@@ -96,3 +96,27 @@ def test_shard_selection_splits_in_order():
         torch.cuda.synchronize()
         for u in range(2):
             assert idx[u, :int(c[u])].tolist() == w[u]
+
+
+def test_sharded_step_with_an_empty_request_and_empty_shards():
+    """Ragged requests over many shards leave some shards with no pages of a
+    request (and one request with none at all): those parts carry lse = -inf
+    and the merge still matches the unsharded step."""
+    from sparse_paged_kv_page_gb300.shard import SequenceShards
+    wl = make_workload(config(3, small=True))
+    c = wl.cfg
+    dec = make_decoder(wl)
+    dec.seq_lens[1] = 0
+    sh = SequenceShards(dec, 7)
+    q = dev_bits(wl.q(0), c.dtype)
+    out_s = sh.attend(q).clone()
+    lse_s = sh.lse.clone()
+    dec.attend(q)
+    torch.cuda.synchronize()
+    assert torch.equal(dec.sel_cnt, sh.sel_cnt) and int(sh.sel_cnt[1].abs().sum()) == 0
+    assert torch.all(out_s[1].float() == 0) and torch.all(lse_s[1] == -float("inf"))
+    for b in (0, 2):
+        ok = torch.isfinite(dec.lse[b])
+        assert torch.allclose(lse_s[b][ok], dec.lse[b][ok], atol=1e-3)
+        assert torch.allclose(out_s[b].float(), dec.out[b].float(), atol=2e-2, rtol=2e-2)
+    assert dev_status(dec) == 0
