@@ -130,14 +130,6 @@ struct Elem<__half> {
 // ---------------------------------------------------------------------------
 // memory helpers
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
