@@ -10,8 +10,8 @@
 //
 // Two launches:
 //  (1) gauss_moments_kernel: one thread per page of a (request, KV head),
-//      scale q of the G heads in shared memory; with the page's dimensions
-//      taken as
+//      reading a whole 32-byte sector of its mean and std rows per step, scale
+//      q of the G heads in shared memory; with the page's dimensions taken as
 //      independent, a query head's scores z = scale q . k on page p have
 //        m_p = sum_d (scale q_d) mean_pd,  v_p = sum_d (scale q_d)^2 std_pd^2.
 //  (2) gauss_select_kernel: one CTA per (request, query head). The page
@@ -80,13 +80,16 @@ __global__ void __launch_bounds__(kMomThreads) gauss_moments_kernel(GaussArgs a)
                                                    ((int64_t(blk) * a.H_kv + h) * 3 + 2) * D);
   const uint4* sd = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.kstd) +
                                                    (int64_t(blk) * a.H_kv + h) * D);
+  // a full 32-byte sector of each row per step (16 dimensions)
 #pragma unroll 2
-  for (int c = 0; c < D / 8; ++c) {
-    const uint4 um = __ldg(mu + c), us = __ldg(sd + c);
-    const uint32_t wm[4] = {um.x, um.y, um.z, um.w}, ws[4] = {us.x, us.y, us.z, us.w};
-    float xm[8], xs[8];
+  for (int c = 0; c < D / 16; ++c) {
+    const uint4 um0 = __ldg(mu + 2 * c), um1 = __ldg(mu + 2 * c + 1);
+    const uint4 us0 = __ldg(sd + 2 * c), us1 = __ldg(sd + 2 * c + 1);
+    const uint32_t wm[8] = {um0.x, um0.y, um0.z, um0.w, um1.x, um1.y, um1.z, um1.w};
+    const uint32_t ws[8] = {us0.x, us0.y, us0.z, us0.w, us1.x, us1.y, us1.z, us1.w};
+    float xm[16], xs[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
       xm[2 * i] = E::lo(wm[i]); xm[2 * i + 1] = E::hi(wm[i]);
       const float s0 = E::lo(ws[i]), s1 = E::hi(ws[i]);
       xs[2 * i] = s0 * s0; xs[2 * i + 1] = s1 * s1;
@@ -94,12 +97,15 @@ __global__ void __launch_bounds__(kMomThreads) gauss_moments_kernel(GaussArgs a)
 #pragma unroll
     for (int g = 0; g < kG; ++g) {
       if (g < G) {
-        const float4 q0 = s_q[g][2 * c], q1 = s_q[g][2 * c + 1];
-        const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          m[g] = fmaf(qq[i], xm[i], m[g]);
-          v[g] = fmaf(qq[i] * qq[i], xs[i], v[g]);
+        for (int h4 = 0; h4 < 4; ++h4) {
+          const float4 qv = s_q[g][4 * c + h4];
+          const float qq[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            m[g] = fmaf(qq[i], xm[4 * h4 + i], m[g]);
+            v[g] = fmaf(qq[i] * qq[i], xs[4 * h4 + i], v[g]);
+          }
         }
       }
     }
