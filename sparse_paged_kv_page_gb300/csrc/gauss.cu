@@ -151,9 +151,10 @@ __device__ __forceinline__ void tail_moment(float mu_a, float s_a, float t, bool
   }
 }
 
-// the page's estimated maximum score m + sqrt(2 ln f) sqrt(v)
-__device__ __forceinline__ float est_max(float2 mv, int f) {
-  const float kappa = f > 1 ? sqrtf(2.0f * logf(float(f))) : 0.f;
+// the page's estimated maximum score m + sqrt(2 ln f) sqrt(v); kappa_full is
+// sqrt(2 ln page_size), every page but the tail being full
+__device__ __forceinline__ float est_max(float2 mv, int f, int ps, float kappa_full) {
+  const float kappa = f == ps ? kappa_full : (f > 1 ? sqrtf(2.0f * logf(float(f))) : 0.f);
   return mv.x + kappa * sqrtf(fmaxf(mv.y, 0.f));
 }
 
@@ -179,13 +180,14 @@ __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) 
   // the mixture's moments; each page's estimated maximum kept for the selection
   extern __shared__ float s_est[];                          // [max_pages] when it fits, else unused
   const bool cached = a.est_in_smem;
+  const float kappa_full = a.ps > 1 ? sqrtf(2.0f * logf(float(a.ps))) : 0.f;
   float f_s = 0.f, s1 = 0.f, c1 = 0.f, s2 = 0.f, c2 = 0.f;
-#pragma unroll 4
+#pragma unroll 8
   for (int p = tid; p < n; p += kSelThreads) {
-    const float2 mv = mom[p];
+    const float2 mv = __ldcg(mom + p);
     const bool ok = mv.x > -INFINITY && mv.x < INFINITY;
     const int fi = min(a.ps, L - (p << a.ps_shift));
-    if (cached) s_est[p] = ok ? est_max(mv, fi) : -INFINITY;
+    if (cached) s_est[p] = ok ? est_max(mv, fi, a.ps, kappa_full) : -INFINITY;
     if (!ok) continue;
     const float f = float(fi);
     f_s += f;
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) 
     } else {
       const float2 mv = mom[p];
       if (!(mv.x > -INFINITY && mv.x < INFINITY)) return false;
-      e = est_max(mv, min(a.ps, L - (p << a.ps_shift)));
+      e = est_max(mv, min(a.ps, L - (p << a.ps_shift)), a.ps, kappa_full);
     }
     return am1 * e > tau;
   };
