@@ -265,7 +265,14 @@ __device__ __forceinline__ void refresh_page(const AppendArgs& a, int b, int p, 
     m[0] = E::pack(mn0, mn1);                             // exact: values are already dtype
     m[C] = E::pack(mx0, mx1);
     m[2 * C] = uint32_t(me0) | (uint32_t(me1) << 16);
-    if constexpr (kStd) page_std_pair<T>(a, kp, tile, fill, blk, h, c);
+    if constexpr (kStd) {
+      if (fill <= kRowBatch) {                            // the rows are still in registers
+        const uint16_t v0 = std_column<T, false>(r, fill), v1 = std_column<T, true>(r, fill);
+        static_cast<uint32_t*>(a.kstd)[(int64_t(blk) * H + h) * C + c] = uint32_t(v0) | (uint32_t(v1) << 16);
+      } else {
+        page_std_pair<T>(a, kp, tile, fill, blk, h, c);
+      }
+    }
   }
   // H2O slots of the written tokens start at zero
   if (a.hh) {
