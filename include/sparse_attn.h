@@ -53,6 +53,9 @@
  *   never trap. The kernel sets sticky bits in the caller's int32 status word
  *   `dev_status` (nullable: then not recorded), skips the bad unit's memory
  *   access, and finishes; the caller reads the word when convenient.
+ * Alignment: the pools (k, v, meta, kstd) and q start on 16-byte boundaries
+ *   (the kernels read them in 16-byte units); a misaligned one is rejected
+ *   with SA_ERR_INVALID_ARG.
  * Layout: pools are [num_blocks, num_kv_heads, page_size, head_dim] (one
  *   contiguous (block, head) tile), row-major; this differs from vLLM's
  *   [2, num_blocks, page_size, H_kv, D] (cited by [entmax] "How it works")
@@ -537,7 +540,11 @@ sa_status sa_sparse_decode_entmax_qh(const sa_cache* cache, const sa_batch* batc
  *   tau_hat  nullable float32 [batch, num_q_heads] (in units of (alpha - 1) z)
  * Needs cache->meta (k_mean) and cache->kstd, both refreshed by sa_append_kv.
  * Pages whose block id is out of range are never kept (except the tail, left
- * to the decode's own check) and set SA_DEV_BAD_BLOCK. The selection feeds
+ * to the decode's own check) and set SA_DEV_BAD_BLOCK; a request with more
+ * pages than bt_stride sets SA_DEV_OVERFLOW and is read up to its row's end.
+ * bf16 caches run m_p and v_p on the tensor cores (the squares split exactly
+ * into two bf16 terms, every product exact, float32 sums); fp16 caches in
+ * float32 FMAs. The selection feeds
  * sa_sparse_decode_entmax_qh, whose tau is exact over the selected tokens.
  */
 sa_status sa_gauss_select(const sa_cache* cache, const sa_batch* batch, const void* q,

@@ -603,19 +603,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }  // ticket merge
 }
 
-int num_sms() {
-  static int sms[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!sms[dev]) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      v = 148;
-    sms[dev] = v;
-  }
-  return sms[dev];
-}
-
 // Splits per (request, KV head): one wave of resident CTAs, at most one split
 // per tile, and enough splits that a CTA's entry table stays small.
 int choose_nsplit(int units, int max_tiles, int ps, int sms) {
@@ -735,6 +722,7 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   if (st != SA_OK) return st;
   if ((st = check_batch(batch)) != SA_OK) return st;
   if (!q || !sel_idx || !sel_cnt || !out || sel_stride <= 0) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q)) return SA_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
   const int G_kv = num_q_heads / cache->num_kv_heads;
   if (G_kv > 16) return SA_ERR_UNSUPPORTED;
@@ -746,7 +734,7 @@ sa_status decode_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   if (logits && logits_stride < rows) return SA_ERR_INVALID_ARG;
   const int units = batch->batch * H_u;
   const int max_tiles = int((rows + 15) / 16);
-  const int ns = choose_nsplit(units, max_tiles, cache->page_size, num_sms());
+  const int ns = choose_nsplit(units, max_tiles, cache->page_size, sm_count());
   const WsLayout w = ws_layout(units, G, cache->head_dim, ns);
   if (logits_only && !logits) return SA_ERR_INVALID_ARG;
   if (ns > 1 && !logits_only && (!workspace || workspace_bytes < w.total)) return SA_ERR_WORKSPACE;
@@ -788,7 +776,7 @@ extern "C" size_t sa_decode_workspace_size(int32_t batch, int32_t num_kv_heads, 
   const int units = batch * num_kv_heads;
   const int64_t max_tiles = (int64_t(sel_stride) * page_size + 15) / 16;
   const int ns = choose_nsplit(units, int(max_tiles > (1 << 30) ? (1 << 30) : max_tiles), page_size,
-                               num_sms());
+                               sm_count());
   return ws_layout(units, num_q_heads / num_kv_heads, head_dim, ns).total;
 }
 

@@ -705,19 +705,6 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
   if (tid == 0) a.tickets[b * a.H_u + h] = 0;             // ready for the next call
 }
 
-int device_sms() {
-  static int sms[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!sms[dev]) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      v = 148;
-    sms[dev] = v;
-  }
-  return sms[dev];
-}
-
 struct EntLayout {
   int nsplit, ent_cap;
   size_t logits, tau, part_o, part_l, tickets, total;
@@ -785,7 +772,7 @@ extern "C" size_t sa_entmax_workspace_size(int32_t batch, int32_t num_kv_heads, 
   if (batch <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
       sel_stride <= 0 || num_q_heads % num_kv_heads)
     return 0;
-  return ent_layout(batch, num_kv_heads, num_q_heads, head_dim, page_size, sel_stride, device_sms())
+  return ent_layout(batch, num_kv_heads, num_q_heads, head_dim, page_size, sel_stride, sm_count())
       .total;
 }
 
@@ -804,6 +791,7 @@ sa_status entmax_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   if (st != SA_OK) return st;
   if ((st = check_batch(batch)) != SA_OK) return st;
   if (!q || !sel_idx || !sel_cnt || !out || sel_stride <= 0) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q)) return SA_ERR_INVALID_ARG;
   if (!(alpha > 1.0f && alpha <= 2.0f)) return SA_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
   const int G_kv = num_q_heads / cache->num_kv_heads;
@@ -814,7 +802,7 @@ sa_status entmax_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   if (rows > (int64_t(1) << 24)) return SA_ERR_UNSUPPORTED;
   if (logits && logits_stride < rows) return SA_ERR_INVALID_ARG;
   const EntLayout w = ent_layout(batch->batch, H_u, num_q_heads, cache->head_dim, cache->page_size,
-                                 sel_stride, device_sms());
+                                 sel_stride, sm_count());
   if (!workspace || workspace_bytes < w.total) return SA_ERR_WORKSPACE;
   const int64_t smem = int64_t(kWarps + 1) * G * (cache->head_dim + 1) * 4 + int64_t(w.ent_cap) * 8;
   if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;       // (checked before any launch)

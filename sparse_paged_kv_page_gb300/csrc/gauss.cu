@@ -9,11 +9,20 @@
 // kept (as the top-k strategy's budget counts it).
 //
 // Two launches:
-//  (1) gauss_moments_kernel: one thread per page of a (request, KV head),
-//      reading a whole 32-byte sector of its mean and std rows per step, scale
-//      q of the G heads in shared memory; with the page's dimensions taken as
-//      independent, a query head's scores z = scale q . k on page p have
-//        m_p = sum_d (scale q_d) mean_pd,  v_p = sum_d (scale q_d)^2 std_pd^2.
+//  (1) the page moments. With the page's dimensions taken as independent, a
+//      query head's scores z = scale q . k on page p have
+//        m_p = scale sum_d q_d mean_pd,  v_p = scale^2 sum_d q_d^2 std_pd^2,
+//      for the G heads of a KV head a small dense product over the pages.
+//      bf16 caches (gauss_moments_mma_kernel): on the tensor cores, with the
+//      squares split exactly into two bf16 terms (a bf16 has 8 significant
+//      bits, its square at most 16: hi = round(x^2), lo = x^2 - hi, both
+//      bf16), so v = sum (qh + ql)(sh + sl) is four products of bf16 values,
+//      each exact in float32, accumulated in float32 like m = sum q mean.
+//      Persistent CTAs, one producer warp gathering each page's mean and std
+//      rows by bulk copies into a shared-memory ring, four consumer warps of
+//      8 pages each, the query fragments in registers. fp16 caches
+//      (gauss_moments_kernel): one thread per page in float32 FMAs (the square
+//      of an fp16 value can leave fp16's range, so it is not split).
 //  (2) gauss_select_kernel: one CTA per (request, query head). The page
 //      mixture's moments N = sum f_p, M = sum f m / N, V = sum f (v + m^2) / N
 //      - M^2 (compensated float32 per thread, float64 across threads) define
@@ -46,7 +55,7 @@ struct GaussArgs {
   int32_t* cnt;          // [B, H_q]
   float* tau_hat;        // nullable [B, H_q]
   int32_t* status;
-  int H_kv, H_q, G, ps, ps_shift, num_blocks, bt_stride, max_pages, sel_stride;
+  int B, H_kv, H_q, G, ps, ps_shift, num_blocks, bt_stride, max_pages, sel_stride;
   int est_in_smem;       // the selection kernel keeps every page's estimate in shared memory
   float scale, alpha;
 };
@@ -63,7 +72,7 @@ __global__ void __launch_bounds__(kMomThreads) gauss_moments_kernel(GaussArgs a)
   }
   __syncthreads();
   const int L = a.seq_lens[b];
-  const int n = min(L > 0 ? (L + a.ps - 1) >> a.ps_shift : 0, a.max_pages);
+  const int n = min(L > 0 ? (L + a.ps - 1) >> a.ps_shift : 0, a.bt_stride);   // max_pages >= bt_stride
   const int p = blockIdx.x * kMomThreads + tid;
   if (p >= n) return;
   float m[kG], v[kG];
@@ -113,6 +122,154 @@ __global__ void __launch_bounds__(kMomThreads) gauss_moments_kernel(GaussArgs a)
 #pragma unroll
   for (int g = 0; g < kG; ++g)
     if (g < G) a.mom[(mrow + g) * a.max_pages + p] = make_float2(m[g], v[g]);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 page moments on the tensor cores
+// ---------------------------------------------------------------------------
+#ifndef SA_GMOM_MINB
+#define SA_GMOM_MINB 1
+#endif
+#ifndef SA_GMOM_GROUPS
+#define SA_GMOM_GROUPS 2
+#endif
+constexpr int kMmaWarps = 4;
+constexpr int kMmaGroups = SA_GMOM_GROUPS;                 // 8-page groups per warp
+
+// x * x rounded to bf16, per half, and the exact remainder x * x - round(x * x)
+__device__ __forceinline__ void bf16x2_square_split(uint32_t x, uint32_t& hi, uint32_t& lo) {
+  asm("mul.rn.bf16x2 %0, %1, %1;" : "=r"(hi) : "r"(x));
+  asm("fma.rn.bf16x2 %0, %1, %1, %2;" : "=r"(lo) : "r"(x), "r"(hi ^ 0x80008000u));
+}
+
+// One warp per run of kMmaGroups groups of 8 pages of one (request, KV head);
+// per group m16n8k16 products with the 8 pages as the n columns. The sum over
+// k may take the dimensions in any order, so each lane reads its page's rows
+// directly in 16-byte pieces: lane (g4, t4) loads, of page g4 of the group,
+// the pieces at byte offsets 64 i + 16 t4 of the mean and std rows (the four
+// lanes of a page read 64 contiguous bytes per load step), and piece i fills
+// its B fragments of k steps 2 i (first 4 dimensions) and 2 i + 1 (next 4);
+// q's A fragments, built once per warp, take the same order. A rows: kG <= 8:
+// row g holds q_g and q_g^2 hi, row g + 8 zero and q_g^2 lo; kG == 16: rows g
+// and g + 8 are heads g and g + 8, q^2 hi and lo in two tiles. The C
+// fragment gives lane (g4, t4) head g4 (and g4 + 8) at pages 2 t4, 2 t4 + 1.
+template <int D, int kG>
+__global__ void __launch_bounds__(32 * kMmaWarps, SA_GMOM_MINB) gauss_moments_mma_kernel(GaussArgs a) {
+  using E = Elem<__nv_bfloat16>;
+  constexpr int NP = D / 32;                               // pieces per lane per row
+  constexpr int KS = D / 16;                               // k steps
+  constexpr int kTiles = kG > 8 ? 2 : 1;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g4 = lane >> 2, t4 = lane & 3;
+  const int L = a.seq_lens[b];
+  const int n_all = L > 0 ? (L + a.ps - 1) >> a.ps_shift : 0;
+  if (n_all > a.bt_stride && blockIdx.x == 0 && h == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
+  const int n = min(n_all, a.bt_stride);                   // max_pages >= bt_stride
+  const int base = (blockIdx.x * kMmaWarps + warp) * (8 * kMmaGroups);
+  if (base >= n) return;
+
+  // block ids of every group (lane g4 of a quad: page g4)
+  int blk[kMmaGroups];
+#pragma unroll
+  for (int gi = 0; gi < kMmaGroups; ++gi) {
+    const int p = base + 8 * gi + g4;
+    blk[gi] = p < n ? a.bt[int64_t(b) * a.bt_stride + p] : -1;
+  }
+  // q fragments in the pieces' k order
+  uint32_t am[KS][4], av[kTiles][KS][4];
+  {
+    const uint4* q4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
+                                                     (int64_t(b) * a.H_q + int64_t(h) * a.G) * D);
+    const bool r0 = g4 < a.G, r1 = kG > 8 && g4 + 8 < a.G;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 u0 = r0 ? q4[(g4 * D) / 8 + 4 * i + t4] : z;
+      const uint4 u1 = r1 ? q4[((g4 + 8) * D) / 8 + 4 * i + t4] : z;
+      const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int kk = 2 * i + hf;
+        uint32_t h0, l0, h2, l2;
+        bf16x2_square_split(w0[2 * hf], h0, l0);
+        bf16x2_square_split(w0[2 * hf + 1], h2, l2);
+        am[kk][0] = w0[2 * hf]; am[kk][2] = w0[2 * hf + 1];
+        if constexpr (kG > 8) {
+          uint32_t h1, l1, h3, l3;
+          bf16x2_square_split(w1[2 * hf], h1, l1);
+          bf16x2_square_split(w1[2 * hf + 1], h3, l3);
+          am[kk][1] = w1[2 * hf]; am[kk][3] = w1[2 * hf + 1];
+          av[0][kk][0] = h0; av[0][kk][1] = h1; av[0][kk][2] = h2; av[0][kk][3] = h3;
+          av[kTiles - 1][kk][0] = l0; av[kTiles - 1][kk][1] = l1;
+          av[kTiles - 1][kk][2] = l2; av[kTiles - 1][kk][3] = l3;
+        } else {
+          am[kk][1] = 0u; am[kk][3] = 0u;
+          av[0][kk][0] = h0; av[0][kk][1] = l0; av[0][kk][2] = h2; av[0][kk][3] = l2;
+        }
+      }
+    }
+  }
+  const uint4* meta4 = static_cast<const uint4*>(a.meta);
+  const uint4* std4 = static_cast<const uint4*>(a.kstd);
+  auto good = [&](int bk) { return bk >= 0 && bk < a.num_blocks; };
+  auto load = [&](int bk, uint4 (&pm)[NP], uint4 (&pv)[NP]) {
+    const int64_t ph = int64_t(bk) * a.H_kv + h;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      pm[i] = good(bk) ? __ldg(meta4 + (ph * 3 + 2) * (D / 8) + 4 * i + t4) : make_uint4(0u, 0u, 0u, 0u);
+      pv[i] = good(bk) ? __ldg(std4 + ph * (D / 8) + 4 * i + t4) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  const float sc = a.scale, sc2 = a.scale * a.scale;
+  uint4 cm_[NP], cs_[NP];
+  load(blk[0], cm_, cs_);
+#pragma unroll
+  for (int gi = 0; gi < kMmaGroups; ++gi) {
+    const int p0 = base + 8 * gi;
+    if (p0 >= n) break;
+    uint4 nm[NP], ns[NP];
+    if (gi + 1 < kMmaGroups) load(blk[gi + 1], nm, ns);    // the next group's rows in flight
+    const int pl = p0 + g4;
+    if (pl < n && !good(blk[gi]) && t4 == 0) flag(a.status, SA_DEV_BAD_BLOCK);
+    const uint32_t ok = __ballot_sync(kFull, good(blk[gi]));
+    float cm[4] = {0.f, 0.f, 0.f, 0.f}, cv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const uint32_t wm[4] = {cm_[i].x, cm_[i].y, cm_[i].z, cm_[i].w};
+      const uint32_t ws[4] = {cs_[i].x, cs_[i].y, cs_[i].z, cs_[i].w};
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int kk = 2 * i + hf;
+        uint32_t sh0, sl0, sh1, sl1;
+        bf16x2_square_split(ws[2 * hf], sh0, sl0);
+        bf16x2_square_split(ws[2 * hf + 1], sh1, sl1);
+        E::mma(cm, am[kk], wm[2 * hf], wm[2 * hf + 1]);
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t) {
+          E::mma(cv, av[t][kk], sh0, sh1);
+          E::mma(cv, av[t][kk], sl0, sl1);
+        }
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < kTiles; ++hh) {
+      const int g = g4 + 8 * hh;
+      if (g >= a.G) continue;
+      float2* out = a.mom + (int64_t(b) * a.H_q + int64_t(h) * a.G + g) * a.max_pages + p0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = 2 * t4 + e;
+        if (p0 + j >= n) continue;
+        const float m = kG > 8 ? cm[2 * hh + e] : cm[e];
+        const float v = kG > 8 ? cv[2 * hh + e] : cv[e] + cv[2 + e];
+        out[j] = ((ok >> (4 * j)) & 1u) ? make_float2(sc * m, sc2 * v) : make_float2(-INFINITY, 0.f);
+      }
+    }
+    if (gi + 1 < kMmaGroups) {
+#pragma unroll
+      for (int i = 0; i < NP; ++i) { cm_[i] = nm[i]; cs_[i] = ns[i]; }
+    }
+  }
 }
 
 // s += x with the rounding error carried in c (Kahan-Babuska-Neumaier)
@@ -166,8 +323,8 @@ __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) 
   const int warp = tid >> 5, lane = tid & 31;
   const int L = a.seq_lens[b];
   const int n_all = L > 0 ? (L + a.ps - 1) >> a.ps_shift : 0;
-  if (n_all > a.max_pages && tid == 0) flag(a.status, SA_DEV_OVERFLOW);
-  const int n = min(n_all, a.max_pages);
+  if (n_all > a.bt_stride && tid == 0) flag(a.status, SA_DEV_OVERFLOW);
+  const int n = min(n_all, a.bt_stride);                    // max_pages >= bt_stride
   const int64_t row = int64_t(b) * a.H_q + gq;
   const float2* mom = a.mom + row * a.max_pages;
   if (n == 0) {
@@ -275,6 +432,13 @@ sa_status launch_moments(const GaussArgs& a, dim3 grid, cudaStream_t s, int* att
   return launch_status();
 }
 
+template <int D>
+sa_status launch_moments_mma(const GaussArgs& a, dim3 grid, cudaStream_t s) {
+  if (a.G <= 8) gauss_moments_mma_kernel<D, 8><<<grid, 32 * kMmaWarps, 0, s>>>(a);
+  else gauss_moments_mma_kernel<D, 16><<<grid, 32 * kMmaWarps, 0, s>>>(a);
+  return launch_status();
+}
+
 template <typename T, int D>
 sa_status launch_moments_g(const GaussArgs& a, dim3 grid, cudaStream_t s, int slot) {
   if (a.G <= 4) return launch_moments<T, D, 4>(a, grid, s, g_mom_smem[slot * 3 + 0]);
@@ -295,6 +459,7 @@ extern "C" sa_status sa_gauss_select(const sa_cache* cache, const sa_batch* batc
   if (st != SA_OK) return st;
   if ((st = check_batch(batch)) != SA_OK) return st;
   if (!cache->kstd || !q || !moments || !sel_idx || !sel_cnt) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q)) return SA_ERR_INVALID_ARG;
   if (max_pages <= 0 || max_pages < batch->bt_stride || sel_stride < max_pages) return SA_ERR_INVALID_ARG;
   if (!(alpha == 1.5f || alpha == 2.0f)) return SA_ERR_UNSUPPORTED;   // closed forms of the tail moments
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
@@ -305,19 +470,23 @@ extern "C" sa_status sa_gauss_select(const sa_cache* cache, const sa_batch* batc
   a.meta = cache->meta; a.kstd = cache->kstd; a.q = q; a.bt = batch->block_table;
   a.seq_lens = batch->seq_lens; a.mom = reinterpret_cast<float2*>(moments); a.sel = sel_idx;
   a.cnt = sel_cnt; a.tau_hat = tau_hat; a.status = dev_status;
-  a.H_kv = cache->num_kv_heads; a.H_q = num_q_heads; a.G = G; a.ps = cache->page_size;
+  a.B = batch->batch; a.H_kv = cache->num_kv_heads; a.H_q = num_q_heads; a.G = G; a.ps = cache->page_size;
   a.ps_shift = log2i(cache->page_size); a.num_blocks = cache->num_blocks;
   a.bt_stride = batch->bt_stride; a.max_pages = max_pages; a.sel_stride = sel_stride;
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf(float(cache->head_dim));
   a.alpha = alpha;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const dim3 mgrid(unsigned((max_pages + kMomThreads - 1) / kMomThreads), unsigned(cache->num_kv_heads),
-                   unsigned(batch->batch));
   const bool bf = cache->dtype == SA_BF16;
-  if (cache->head_dim == 128)
-    st = bf ? launch_moments_g<__nv_bfloat16, 128>(a, mgrid, s, 0) : launch_moments_g<__half, 128>(a, mgrid, s, 1);
-  else
-    st = bf ? launch_moments_g<__nv_bfloat16, 64>(a, mgrid, s, 2) : launch_moments_g<__half, 64>(a, mgrid, s, 3);
+  if (bf) {
+    const int per_cta = 8 * kMmaGroups * kMmaWarps;
+    const dim3 grid(unsigned((batch->bt_stride + per_cta - 1) / per_cta), unsigned(cache->num_kv_heads),
+                    unsigned(batch->batch));
+    st = cache->head_dim == 128 ? launch_moments_mma<128>(a, grid, s) : launch_moments_mma<64>(a, grid, s);
+  } else {
+    const dim3 mgrid(unsigned((batch->bt_stride + kMomThreads - 1) / kMomThreads), unsigned(cache->num_kv_heads),
+                     unsigned(batch->batch));
+    st = cache->head_dim == 128 ? launch_moments_g<__half, 128>(a, mgrid, s, 1) : launch_moments_g<__half, 64>(a, mgrid, s, 3);
+  }
   if (st != SA_OK) return st;
   static int g_sel_smem[64];
   const int est_bytes = max_pages * int(sizeof(float));

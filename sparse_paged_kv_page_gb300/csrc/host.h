@@ -19,8 +19,13 @@ inline int log2i(int x) {
   return s;
 }
 
+// vector loads and bulk copies read whole 16-byte units
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 inline sa_status check_cache(const sa_cache* c, bool need_kv, bool need_meta) {
   if (!c) return SA_ERR_INVALID_ARG;
+  if (!aligned16(c->k) || !aligned16(c->v) || !aligned16(c->meta) || !aligned16(c->kstd))
+    return SA_ERR_INVALID_ARG;
   if (c->dtype != SA_BF16 && c->dtype != SA_FP16) return SA_ERR_INVALID_ARG;
   if (c->num_blocks <= 0 || c->num_kv_heads <= 0) return SA_ERR_INVALID_ARG;
   if (!is_pow2(c->page_size) || c->page_size > 128) return SA_ERR_UNSUPPORTED;
@@ -34,6 +39,20 @@ inline sa_status check_batch(const sa_batch* b) {
   if (!b || !b->block_table || !b->seq_lens) return SA_ERR_INVALID_ARG;
   if (b->batch <= 0 || b->bt_stride <= 0) return SA_ERR_INVALID_ARG;
   return SA_OK;
+}
+
+// SMs of the current device (cached per device; 148 if it cannot be read)
+inline int sm_count() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!sms[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    sms[dev] = v;
+  }
+  return sms[dev];
 }
 
 inline sa_status launch_status() {

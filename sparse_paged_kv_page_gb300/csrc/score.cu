@@ -389,19 +389,6 @@ sa_status launch_score(const ScoreArgs& a, int grid, cudaStream_t s, int* cache)
   return launch_status();
 }
 
-int sm_count() {
-  static int sms[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!sms[dev]) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-      v = 148;
-    sms[dev] = v;
-  }
-  return sms[dev];
-}
-
 }  // namespace
 }  // namespace sa
 
@@ -413,6 +400,7 @@ sa_status sa::score_impl(const sa_cache* cache, const sa_batch* batch, const voi
   if (st != SA_OK) return st;
   if ((st = check_batch(batch)) != SA_OK) return st;
   if (!q || !scores || max_pages <= 0) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q)) return SA_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
   const int G = num_q_heads / cache->num_kv_heads;
   if (G > 16) return SA_ERR_UNSUPPORTED;

@@ -33,6 +33,7 @@ extern "C" sa_status sa_decode_step(const sa_cache* cache, const sa_batch* batch
   if (!q || !scores || !sel_idx || !sel_cnt || !out || max_pages <= 0 || topk <= 0 ||
       max_new_per_req < 0 || n_bos < 0 || n_eos < 1 || n_bos + n_eos > topk)
     return SA_ERR_INVALID_ARG;
+  if (!aligned16(q)) return SA_ERR_INVALID_ARG;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return SA_ERR_INVALID_ARG;
   if (num_q_heads / cache->num_kv_heads > 16) return SA_ERR_UNSUPPORTED;
   if (batch->batch > 1024 || max_pages > 45056) return SA_ERR_UNSUPPORTED;

@@ -48,6 +48,31 @@ def test_host_only_calls(lib):
                               0, 1, None, None, 0.0, None, None, None, 0, None, None) == 1
 
 
+def test_misaligned_pointers_are_rejected_on_the_host(lib):
+    """Pools and q must start on 16-byte boundaries; the check runs before any
+    launch (the pointer values are never dereferenced on the host)."""
+    import ctypes
+    from sparse_paged_kv_page_gb300 import _lib
+    lens = ctypes.c_void_p(0x10000)
+    bt = ctypes.c_void_p(0x20000)
+    batch = _lib.SaBatch(block_table=bt, seq_lens=lens, batch=1, bt_stride=4)
+    good = dict(k=ctypes.c_void_p(0x100000), v=ctypes.c_void_p(0x200000), meta=ctypes.c_void_p(0x300000),
+                dtype=0, num_blocks=4, num_kv_heads=1, page_size=16, head_dim=128, kstd=None)
+    q = ctypes.c_void_p(0x400000)
+    scores = ctypes.c_void_p(0x500000)
+    for field in ("k", "v", "meta", "q"):
+        kw = dict(good)
+        qq = q
+        if field == "q":
+            qq = ctypes.c_void_p(0x400008)
+        else:
+            kw[field] = ctypes.c_void_p(kw[field].value + 8)
+        cache = _lib.SaCache(**kw)
+        st = lib.sa_score_pages(ctypes.byref(cache), ctypes.byref(batch), qq, 1, 1.0, 0.25, scores, 4,
+                                None, None)
+        assert st == 1, field
+
+
 def test_struct_layouts_match_the_binding(lib):
     import ctypes
     import sparse_paged_kv_page_gb300 as S

@@ -223,3 +223,73 @@ def test_gaussian_head_dim_64_and_an_empty_request(alpha):
         assert_attention(out[b, gq][None], o)
     dec.seq_lens.copy_(lens)
     assert dev_status(dec) == 0
+
+
+@pytest.mark.parametrize("H_q,H_kv", [(32, 2), (2, 2), (12, 2)])
+def test_gaussian_query_groups(H_q, H_kv):
+    """Groups of 16, 1 and 6 query heads per KV head (the moments' two tile
+    shapes, empty rows of a tile): moments, tau_hat, selection and attention
+    against the oracle."""
+    wl, dec = _gauss_decoder(5, 1.5, H_q=H_q, H_kv=H_kv)
+    c = wl.cfg
+    q = dev_bits(wl.q(0), c.dtype)
+    dec.attend(q)
+    torch.cuda.synchronize()
+    heads = [(b, g) for b in range(c.B) for g in range(c.H_q)]
+    assert _check_selection(dec, wl, 0, wl.q(0), 1.5, heads) >= 0.9 * len(heads)
+    sel = dec.sel_idx.cpu().numpy()
+    cnt = dec.sel_cnt.cpu().numpy()
+    out = dec.out.float().cpu().numpy()
+    sc = _scale(c)
+    for b, gq in heads:
+        h = gq // c.G
+        L = int(wl.prefill_lens[b])
+        pos = O.selected_positions(sel[b, gq, :cnt[b, gq]], L, c.ps)
+        k = O.decode_kdt(wl.k_seq(b)[:, h, :][pos], c.dtype)
+        v = O.decode_kdt(wl.v_seq(b)[:, h, :][pos], c.dtype)
+        o, _, _ = O.attention_entmax(O.decode_kdt(wl.q(0)[b, gq], c.dtype)[None], k, v, sc, 1.5)
+        assert_attention(out[b, gq][None], o)
+    assert dev_status(dec) == 0
+
+
+def test_gauss_select_bad_block_and_overflow():
+    """A page with an out-of-range block id gets (-inf, 0) moments, is never
+    kept and sets SA_DEV_BAD_BLOCK, the other pages' moments unchanged; a
+    request longer than its block-table row sets SA_DEV_OVERFLOW and is read
+    up to the row's end (selection ascending, ending at the row's last page);
+    the untouched request still matches the oracle."""
+    from sparse_paged_kv_page_gb300 import sa_gauss_select
+    from sparse_paged_kv_page_gb300._lib import SA_DEV_BAD_BLOCK, SA_DEV_OVERFLOW
+    wl, dec = _gauss_decoder(3)
+    c = wl.cfg
+    q = dev_bits(wl.q(0), c.dtype)
+    n1 = O.num_pages(int(wl.prefill_lens[1]), c.ps)
+    assert n1 >= 3
+    lens = dec.seq_lens.clone()
+    bt = dec.block_table.clone()
+    dec.block_table[1, 1] = wl.num_blocks + 5               # page 1 of request 1 (never its tail)
+    dec.seq_lens[0] = dec.block_table.shape[1] * c.ps + 100  # more pages than the row holds
+    sa_gauss_select(dec.cache.struct, dec.batch, q, c.H_q, 1.5, dec.scale, dec.moments, dec.max_pages,
+                    dec.sel_idx, dec.sel_cnt, dec.sel_stride, tau_hat=dec.tau_hat,
+                    dev_status=dec.dev_status)
+    torch.cuda.synchronize()
+    st = dev_status(dec)
+    assert st & SA_DEV_BAD_BLOCK and st & SA_DEV_OVERFLOW
+    mom = dec.moments.cpu().numpy()
+    sel = dec.sel_idx.cpu().numpy()
+    cnt = dec.sel_cnt.cpu().numpy()
+    row = dec.block_table.shape[1]
+    for g in range(c.H_q):
+        assert mom[1, g, 1, 0] == -np.inf and mom[1, g, 1, 1] == 0.0
+        assert 1 not in sel[1, g, :cnt[1, g]]
+        r = _oracle_head(wl, 1, g, 0, wl.q(0), 1.5)
+        m = mom[1, g, :n1, 0].astype(np.float64)
+        keep = np.arange(n1) != 1
+        qd = np.abs(O.decode_kdt(wl.q(0)[1, g], c.dtype))
+        tol_m = 1e-5 * _scale(c) * (np.abs(r["mean"]) @ qd) + 1e-9
+        assert np.all(np.abs(m - r["m"])[keep] <= tol_m[keep])
+        s0 = sel[0, g, :cnt[0, g]]
+        assert 1 <= cnt[0, g] <= row and s0[-1] == row - 1 and np.all(np.diff(s0) > 0)
+    assert _check_selection(dec, wl, 0, wl.q(0), 1.5, [(2, g) for g in range(c.H_q)]) >= 0
+    dec.block_table.copy_(bt)
+    dec.seq_lens.copy_(lens)
