@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(kMomThreads) gauss_moments_kernel(GaussArgs a)
   __shared__ float4 s_q[kG][D / 4];      // scale * q
   const int h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const int G = a.G;
+  pdl_wait();                            // everything the previous kernel wrote is visible
+  pdl_trigger();
   const uint16_t* qb = static_cast<const uint16_t*>(a.q) + (int64_t(b) * a.H_q + int64_t(h) * G) * D;
   for (int i = tid; i < G * D; i += kMomThreads) {
     reinterpret_cast<float*>(s_q)[i] = a.scale * E::lo(uint32_t(qb[i]));
@@ -161,6 +163,8 @@ __global__ void __launch_bounds__(32 * kMmaWarps, SA_GMOM_MINB) gauss_moments_mm
   constexpr int kTiles = kG > 8 ? 2 : 1;
   const int h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g4 = lane >> 2, t4 = lane & 3;
+  pdl_wait();                                              // everything the previous kernel wrote is visible
+  pdl_trigger();
   const int L = a.seq_lens[b];
   const int n_all = L > 0 ? (L + a.ps - 1) >> a.ps_shift : 0;
   if (n_all > a.bt_stride && blockIdx.x == 0 && h == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
@@ -279,12 +283,6 @@ __device__ __forceinline__ void csum(float& s, float& c, float x) {
   s = t;
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
-
 // E[(A - t)_+^r] and its derivative in t for A ~ N(mu_a, s_a^2), r = 1 / (alpha - 1)
 __device__ __forceinline__ void tail_moment(float mu_a, float s_a, float t, bool sparsemax, float& e,
                                             float& de) {
@@ -315,12 +313,38 @@ __device__ __forceinline__ float est_max(float2 mv, int f, int ps, float kappa_f
   return mv.x + kappa * sqrtf(fmaxf(mv.y, 0.f));
 }
 
+// a + b = s + e exactly (Knuth's TwoSum)
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// a compensated pair (s, c) summed over the warp, the rounding of each step kept in c
+__device__ __forceinline__ void warp_sum_pair(float& s, float& c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float s2 = __shfl_xor_sync(kFull, s, o), c2 = __shfl_xor_sync(kFull, c, o);
+    float t, e;
+    two_sum(s, s2, t, e);
+    s = t;
+    c = c + c2 + e;
+  }
+}
+
+constexpr int kSelBatch = 16;                              // page moments in flight per thread
+
 __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) {
-  __shared__ double s_red[kSelWarps][3];
+  __shared__ float s_red[kSelWarps][4];                    // per warp: S1 (s, c), S2 (s, c)
+  __shared__ int s_n[kSelWarps];
   __shared__ int s_cnt[kSelWarps];
+  __shared__ float s_par[4];                               // mu_a, s_a, N, closed-form tau
+  __shared__ int s_mode;                                   // 0 no tokens, 1 closed form, 2 solve
   __shared__ float s_tau;
   const int gq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  pdl_wait();                                              // the moments are complete
+  pdl_trigger();
   const int L = a.seq_lens[b];
   const int n_all = L > 0 ? (L + a.ps - 1) >> a.ps_shift : 0;
   if (n_all > a.bt_stride && tid == 0) flag(a.status, SA_DEV_OVERFLOW);
@@ -338,53 +362,94 @@ __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) 
   extern __shared__ float s_est[];                          // [max_pages] when it fits, else unused
   const bool cached = a.est_in_smem;
   const float kappa_full = a.ps > 1 ? sqrtf(2.0f * logf(float(a.ps))) : 0.f;
-  float f_s = 0.f, s1 = 0.f, c1 = 0.f, s2 = 0.f, c2 = 0.f;
-#pragma unroll 8
-  for (int p = tid; p < n; p += kSelThreads) {
-    const float2 mv = __ldcg(mom + p);
-    const bool ok = mv.x > -INFINITY && mv.x < INFINITY;
-    const int fi = min(a.ps, L - (p << a.ps_shift));
-    if (cached) s_est[p] = ok ? est_max(mv, fi, a.ps, kappa_full) : -INFINITY;
-    if (!ok) continue;
-    const float f = float(fi);
-    f_s += f;
-    csum(s1, c1, f * mv.x);
-    csum(s2, c2, f * (mv.y + mv.x * mv.x));
+  int f_s = 0;
+  float s1 = 0.f, c1 = 0.f, s2 = 0.f, c2 = 0.f;
+  for (int p0 = tid; p0 < n; p0 += kSelBatch * kSelThreads) {
+    float2 mv[kSelBatch];
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {                   // every load issued before any is used
+      const int p = p0 + u * kSelThreads;
+      mv[u] = p < n ? __ldcg(mom + p) : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const int p = p0 + u * kSelThreads;
+      const bool ok = p < n && mv[u].x > -INFINITY && mv[u].x < INFINITY;
+      const int fi = min(a.ps, L - (p << a.ps_shift));
+      if (cached && p < n) s_est[p] = ok ? est_max(mv[u], fi, a.ps, kappa_full) : -INFINITY;
+      if (!ok) continue;
+      const float f = float(fi);
+      f_s += fi;
+      csum(s1, c1, f * mv[u].x);
+      csum(s2, c2, f * (mv[u].y + mv[u].x * mv[u].x));
+    }
   }
-  double dn = warp_sum_d(double(f_s)), d1 = warp_sum_d(double(s1) + double(c1)),
-         d2 = warp_sum_d(double(s2) + double(c2));
-  if (lane == 0) { s_red[warp][0] = dn; s_red[warp][1] = d1; s_red[warp][2] = d2; }
+  f_s = __reduce_add_sync(kFull, f_s);
+  warp_sum_pair(s1, c1);
+  warp_sum_pair(s2, c2);
+  if (lane == 0) {
+    s_n[warp] = f_s;
+    s_red[warp][0] = s1; s_red[warp][1] = c1; s_red[warp][2] = s2; s_red[warp][3] = c2;
+  }
   __syncthreads();
-  if (tid == 0) {
-    double N = 0.0, S1 = 0.0, S2 = 0.0;
-    for (int w = 0; w < kSelWarps; ++w) { N += s_red[w][0]; S1 += s_red[w][1]; S2 += s_red[w][2]; }
-    float tau = -INFINITY;                                  // nothing resolves: only the tail
-    if (N > 0.0) {
-      const double Md = S1 / N;
-      const float M = float(Md), V = float(fmax(S2 / N - Md * Md, 0.0));
-      const bool sparsemax = a.alpha == 2.0f;
+  const bool sparsemax = a.alpha == 2.0f;
+  if (tid == 0) {                                           // float64 on one thread only
+    long long N = 0;
+    double S1 = 0.0, S2 = 0.0;
+    for (int w = 0; w < kSelWarps; ++w) {
+      N += s_n[w];
+      S1 += double(s_red[w][0]) + double(s_red[w][1]);
+      S2 += double(s_red[w][2]) + double(s_red[w][3]);
+    }
+    int mode = 0;                                           // nothing resolves: only the tail
+    if (N > 0) {
+      const double Nd = double(N), Md = S1 / Nd;
+      const float M = float(Md), V = float(fmax(S2 / Nd - Md * Md, 0.0));
       const float am1 = a.alpha - 1.0f;
-      const float mu_a = am1 * M, s_a = am1 * sqrtf(V), Nf = float(N);
-      if (s_a <= 0.f) {
-        tau = mu_a - (sparsemax ? 1.0f / Nf : rsqrtf(Nf));  // N (mu_a - tau)^r = 1
-      } else {
-        tau = mu_a - 1.0f;                                  // left of the root (Jensen)
-        for (int it = 0; it < 100; ++it) {
-          float e, de;
-          tail_moment(mu_a, s_a, tau, sparsemax, e, de);
-          const float g = Nf * e - 1.0f;
-          if (!(g > 0.f) || !(de < 0.f)) break;
-          const float step = -g / (Nf * de);
-          tau += step;
-          if (step <= 1e-7f * (1.0f + fabsf(tau))) break;
-        }
+      const float mu_a = am1 * M, s_a = am1 * sqrtf(V), Nf = float(Nd);
+      s_par[0] = mu_a; s_par[1] = s_a; s_par[2] = Nf;
+      s_par[3] = mu_a - (sparsemax ? 1.0f / Nf : rsqrtf(Nf));   // N (mu_a - tau)^r = 1 when s_a = 0
+      mode = s_a <= 0.f ? 1 : 2;
+    }
+    s_mode = mode;
+  }
+  __syncthreads();
+  const int mode = s_mode;
+  float tau = mode == 1 ? s_par[3] : -INFINITY;
+  if (mode == 2) {
+    // the constraint at kSelThreads points from (alpha - 1) M - 1 (left of the
+    // root by Jensen) to 10 deviations above the mean, one per thread; Newton
+    // starts from the largest point still left of the root (any start there
+    // converges monotonically: the function is convex and decreasing)
+    const float mu_a = s_par[0], s_a = s_par[1], Nf = s_par[2];
+    const float lo = mu_a - 1.0f, span = 1.0f + 10.0f * s_a;
+    auto point = [&](int i) { return lo + span * (float(i) / float(kSelThreads)); };
+    float e, de;
+    tail_moment(mu_a, s_a, point(tid), sparsemax, e, de);
+    const unsigned pos = __ballot_sync(kFull, Nf * e - 1.0f > 0.f);
+    if (lane == 0) s_cnt[warp] = pos ? warp * 32 + 31 - __clz(pos) : -1;
+    __syncthreads();
+    if (tid == 0) {
+      int best = 0;
+      for (int w = 0; w < kSelWarps; ++w) best = max(best, s_cnt[w]);
+      tau = point(best);
+      for (int it = 0; it < 100; ++it) {
+        tail_moment(mu_a, s_a, tau, sparsemax, e, de);
+        const float g = Nf * e - 1.0f;
+        if (!(g > 0.f) || !(de < 0.f)) break;
+        const float step = -g / (Nf * de);
+        tau += step;
+        if (step <= 1e-7f * (1.0f + fabsf(tau))) break;
       }
     }
+  }
+  if (tid == 0) {
     s_tau = tau;
     if (a.tau_hat) a.tau_hat[row] = tau;
   }
   __syncthreads();
-  const float tau = s_tau, am1 = a.alpha - 1.0f;
+  tau = s_tau;
+  const float am1 = a.alpha - 1.0f;
   auto keep_of = [&](int p) -> bool {
     if (p == n - 1) return true;                            // the tail page
     float e;
@@ -401,6 +466,7 @@ __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) 
   const int seg = (((n + kSelWarps - 1) / kSelWarps) + 31) & ~31;
   const int p0 = warp * seg, p1 = min(n, p0 + seg);
   int mine = 0;
+#pragma unroll 4
   for (int base = p0; base < p1; base += 32) {
     const int p = base + lane;
     mine += __popc(__ballot_sync(kFull, p < p1 && keep_of(p)));
@@ -413,6 +479,7 @@ __global__ void __launch_bounds__(kSelThreads) gauss_select_kernel(GaussArgs a) 
     total += s_cnt[w];
   }
   int32_t* out = a.sel + row * a.sel_stride;
+#pragma unroll 4
   for (int base = p0; base < p1; base += 32) {
     const int p = base + lane;
     const bool k = p < p1 && keep_of(p);
@@ -428,15 +495,16 @@ int g_mom_smem[12][64];
 template <typename T, int D, int kG>
 sa_status launch_moments(const GaussArgs& a, dim3 grid, cudaStream_t s, int* attr) {
   if (!ensure_smem(gauss_moments_kernel<T, D, kG>, 0, attr)) return SA_ERR_CUDA;
-  gauss_moments_kernel<T, D, kG><<<grid, kMomThreads, 0, s>>>(a);
-  return launch_status();
+  return launch_ex(gauss_moments_kernel<T, D, kG>, grid, dim3(kMomThreads), 0, s, true, 1u, a) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
 }
 
 template <int D>
 sa_status launch_moments_mma(const GaussArgs& a, dim3 grid, cudaStream_t s) {
-  if (a.G <= 8) gauss_moments_mma_kernel<D, 8><<<grid, 32 * kMmaWarps, 0, s>>>(a);
-  else gauss_moments_mma_kernel<D, 16><<<grid, 32 * kMmaWarps, 0, s>>>(a);
-  return launch_status();
+  const cudaError_t e = a.G <= 8 ? launch_ex(gauss_moments_mma_kernel<D, 8>, grid, dim3(32 * kMmaWarps), 0, s, true, 1u, a)
+                                  : launch_ex(gauss_moments_mma_kernel<D, 16>, grid, dim3(32 * kMmaWarps), 0, s, true, 1u, a);
+  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
 template <typename T, int D>
@@ -493,6 +561,10 @@ extern "C" sa_status sa_gauss_select(const sa_cache* cache, const sa_batch* batc
   a.est_in_smem = est_bytes <= 160 * 1024;
   const int smem = a.est_in_smem ? est_bytes : 0;
   if (!ensure_smem(gauss_select_kernel, smem, g_sel_smem)) return SA_ERR_CUDA;
-  gauss_select_kernel<<<dim3(unsigned(num_q_heads), unsigned(batch->batch)), kSelThreads, smem, s>>>(a);
-  return launch_status();
+  // both launches programmatic: each kernel waits on the device for its
+  // predecessor before reading anything, so only the launch latency overlaps
+  return launch_ex(gauss_select_kernel, dim3(unsigned(num_q_heads), unsigned(batch->batch)), dim3(kSelThreads),
+                   size_t(smem), s, true, 1u, a) == cudaSuccess
+             ? SA_OK
+             : SA_ERR_CUDA;
 }
