@@ -330,20 +330,22 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(AppendArgs a) {
 }
 
 // Grid (B): a request's (at most two) pages, then its length, in one CTA.
-// At most 128 registers a thread: with the page scorer's two CTAs resident,
-// the sub-partitions holding three of its warps have exactly one 128-register
-// warp's worth of registers left, so this kernel can run beside the scorer.
-template <typename T, bool kStd>
-__global__ void __launch_bounds__(kFusedThreads, 4) append_fused_kernel(AppendArgs a) {
+// NT = kFusedThreads when launched beside the page scorer: at most 128
+// registers a thread, and with the scorer's two CTAs resident the
+// sub-partitions holding three of its warps have exactly one 128-register
+// warp's worth of registers left. A plain launch takes NT = kAppendThreads,
+// one (head, column pair) a thread at 8 KV heads of 128 dimensions.
+template <typename T, bool kStd, int NT>
+__global__ void __launch_bounds__(NT, 512 / NT) append_fused_kernel(AppendArgs a) {
   const int b = blockIdx.x;
   int L_old, n, row0;
   const bool any = plan(a, b, threadIdx.x == 0, L_old, n, row0);
   if (any)
     for (int p = L_old / a.ps; p <= (L_old + n - 1) / a.ps; ++p)
-      refresh_page<T, kFusedThreads, kStd>(a, b, p, L_old, L_old + n, row0);
+      refresh_page<T, NT, kStd>(a, b, p, L_old, L_old + n, row0);
   __syncthreads();                                          // every read of the old length is done
   if (any) {
-    for (int h = threadIdx.x; h < a.H && a.ret_cnt; h += kFusedThreads) {
+    for (int h = threadIdx.x; h < a.H && a.ret_cnt; h += NT) {
       const int c = a.ret_cnt[b * a.H + h] + n;
       a.ret_cnt[b * a.H + h] = min(max(c, 0), a.ret_cap);
     }
@@ -402,11 +404,18 @@ sa_status sa::append_impl(const sa_cache* cache, const sa_batch* batch, const vo
   a.max_new = max_new_per_req; a.ret_cap = ret_pos ? ret_cap : 0;
   const bool bf = cache->dtype == SA_BF16;
   if (max_new_per_req <= a.ps) {                            // touches at most two pages per request
-    static int g_fused_attr[4][64];
-    auto kern = bf ? (a.kstd ? append_fused_kernel<__nv_bfloat16, true> : append_fused_kernel<__nv_bfloat16, false>)
-                   : (a.kstd ? append_fused_kernel<__half, true> : append_fused_kernel<__half, false>);
-    if (!ensure_smem(kern, 0, g_fused_attr[(bf ? 0 : 2) + (a.kstd ? 1 : 0)])) return SA_ERR_CUDA;
-    const cudaError_t e = launch_ex(kern, dim3(batch->batch), dim3(kFusedThreads), 0, s, pdl, 1, a);
+    static int g_fused_attr[8][64];
+    auto kern = pdl ? (bf ? (a.kstd ? append_fused_kernel<__nv_bfloat16, true, kFusedThreads>
+                                    : append_fused_kernel<__nv_bfloat16, false, kFusedThreads>)
+                          : (a.kstd ? append_fused_kernel<__half, true, kFusedThreads>
+                                    : append_fused_kernel<__half, false, kFusedThreads>))
+                    : (bf ? (a.kstd ? append_fused_kernel<__nv_bfloat16, true, kAppendThreads>
+                                    : append_fused_kernel<__nv_bfloat16, false, kAppendThreads>)
+                          : (a.kstd ? append_fused_kernel<__half, true, kAppendThreads>
+                                    : append_fused_kernel<__half, false, kAppendThreads>));
+    if (!ensure_smem(kern, 0, g_fused_attr[(pdl ? 0 : 4) + (bf ? 0 : 2) + (a.kstd ? 1 : 0)])) return SA_ERR_CUDA;
+    const cudaError_t e =
+        launch_ex(kern, dim3(batch->batch), dim3(pdl ? kFusedThreads : kAppendThreads), 0, s, pdl, 1, a);
     return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
   }
   const int64_t pages = (int64_t(max_new_per_req) + a.ps - 1) / a.ps + 1;
