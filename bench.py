@@ -760,8 +760,11 @@ def main():
         if args.gaussian:
             ab = res["score_ab"] * 2 // 3                   # k_mean and k_std rows, not k_min / k_max
             kms = res["kern"]["select"]
-            tr = None
-            kname = "gauss_moments_kernel + gauss_select_kernel (sa_gauss_select)"
+            tm = traffic_from_profile("gauss.cu", "gauss_moments.long_context_gqa.md") if args.config == 5 else None
+            ts = traffic_from_profile("gauss.cu", "gauss_select.long_context_gqa.md") if args.config == 5 else None
+            tr = tm + ts if tm is not None and ts is not None else None
+            mk = "gauss_moments_mma_kernel" if c.dtype == "bf16" else "gauss_moments_kernel"
+            kname = mk + " + gauss_select_kernel (sa_gauss_select)"
         elif c.ps > 1:
             ab = res["score_ab"]
             kms = res["kern"]["score"]
