@@ -765,6 +765,11 @@ def main():
             tr = tm + ts if tm is not None and ts is not None else None
             mk = "gauss_moments_mma_kernel" if c.dtype == "bf16" else "gauss_moments_kernel"
             kname = mk + " + gauss_select_kernel (sa_gauss_select)"
+        elif c.ps > 1 and args.per_query_head:
+            ab = res["score_ab"]
+            kms = res["kern"]["score"]
+            tr = None
+            kname = ("score_qh_kernel" if c.H_q // c.H_kv <= 8 else "score_kernel<per-head>") + " (sa_score_pages_qh)"
         elif c.ps > 1:
             ab = res["score_ab"]
             kms = res["kern"]["score"]

@@ -379,6 +379,131 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
   }
 }
 
+// ---------------------------------------------------------------------------
+// Per-query-head scores for G <= 8 without a shared-memory ring
+// ---------------------------------------------------------------------------
+#ifndef SA_QH_GROUPS
+#define SA_QH_GROUPS 16
+#endif
+constexpr int kQhWarps = 4;
+constexpr int kQhGroups = SA_QH_GROUPS;                    // 8-page groups per warp
+
+// The same product S[g, page] = sum_k A[g, k] B[k, page] over the page's 3D
+// statistics, one warp per run of kQhGroups groups of 8 pages of one
+// (request, KV head), the pages the n columns of m16n8k16. The sum over k may
+// take the statistics in any order, so lane (g4, t4) reads, of page g4 of the
+// group, the 16-byte pieces at byte offsets 64 i + 16 t4 of its 3D-element
+// row (the four lanes of a page read 64 contiguous bytes per load) straight
+// into B fragments: piece i fills k steps 2 i (its first 4 elements) and
+// 2 i + 1 (the next 4). A, built once per warp in that order, holds head g4's
+// coefficient hi in row g4 and lo in row g4 + 8, so the score of head g4 at
+// page j is the sum of the two rows. The next group's rows are loaded while
+// the current one is multiplied.
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kQhWarps, 2) score_qh_kernel(ScoreArgs a) {
+  using E = Elem<T>;
+  constexpr int KD = 3 * D;
+  constexpr int NP = KD / 32;                              // pieces per lane per row
+  constexpr int KS = KD / 16;                              // k steps
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g4 = lane >> 2, t4 = lane & 3;
+  pdl_wait();
+  const int L = a.seq_lens[b];
+  pdl_trigger();
+  const int n_all = L > 0 ? (L + a.ps - 1) / a.ps : 0;
+  const int cap = min(a.max_pages, a.bt_stride);
+  if (n_all > cap && blockIdx.x == 0 && h == 0 && threadIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
+  const int n = min(n_all, cap);
+  const int base = (blockIdx.x * kQhWarps + warp) * (8 * kQhGroups);
+  if (base >= n) return;
+
+  int blk[kQhGroups];
+#pragma unroll
+  for (int gi = 0; gi < kQhGroups; ++gi) {
+    const int p = base + 8 * gi + g4;
+    blk[gi] = p < n ? a.bt[int64_t(b) * a.bt_stride + p] : -1;
+  }
+  // A fragments: k step 2 i + hf covers elements 32 i + 8 t4 + 4 hf + {0, 1} (a0 / a1)
+  // and + {2, 3} (a2 / a3) of the coefficient row (w_peak q- | w_peak q+ | w_avg q)
+  uint32_t af[KS][4];
+  {
+    const uint16_t* qh = static_cast<const uint16_t*>(a.q) + (int64_t(b) * a.H_q + int64_t(h) * a.G + g4) * D;
+    const bool live = g4 < a.G;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const int k0 = 32 * i + 8 * t4;                      // first element of this lane's piece
+      const int third = k0 / D, d0 = k0 % D;
+      const uint4 u = live ? *reinterpret_cast<const uint4*>(qh + d0) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float c[2];
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+          const float x = z ? E::hi(w[e]) : E::lo(w[e]);
+          c[z] = third == 0 ? a.w_peak * fminf(x, 0.f) : (third == 1 ? a.w_peak * fmaxf(x, 0.f) : a.w_avg * x);
+        }
+        const uint32_t hv = E::pack(c[0], c[1]);
+        hi[e] = hv;
+        lo[e] = E::pack(c[0] - E::lo(hv), c[1] - E::hi(hv));
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        af[2 * i + hf][0] = hi[2 * hf];
+        af[2 * i + hf][1] = lo[2 * hf];
+        af[2 * i + hf][2] = hi[2 * hf + 1];
+        af[2 * i + hf][3] = lo[2 * hf + 1];
+      }
+    }
+  }
+  const uint4* meta4 = static_cast<const uint4*>(a.meta);
+  auto good = [&](int bk) { return bk >= 0 && bk < a.num_blocks; };
+  auto load = [&](int bk, uint4 (&r)[NP]) {
+    const int64_t row = (int64_t(bk) * a.H_kv + h) * (KD / 8);
+#pragma unroll
+    for (int i = 0; i < NP; ++i) r[i] = good(bk) ? __ldg(meta4 + row + 4 * i + t4) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  uint4 cur[NP];
+  load(blk[0], cur);
+#pragma unroll
+  for (int gi = 0; gi < kQhGroups; ++gi) {
+    const int p0 = base + 8 * gi;
+    if (p0 >= n) break;
+    uint4 nxt[NP];
+    if (gi + 1 < kQhGroups) load(blk[gi + 1], nxt);       // the next group's rows in flight
+    if (p0 + g4 < n && !good(blk[gi]) && t4 == 0) flag(a.status, SA_DEV_BAD_BLOCK);
+    const uint32_t ok = __ballot_sync(kFull, good(blk[gi]));
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      E::mma(acc, af[2 * i], cur[i].x, cur[i].y);
+      E::mma(acc, af[2 * i + 1], cur[i].z, cur[i].w);
+    }
+    if (g4 < a.G) {
+      float* out = a.scores + (int64_t(b) * a.H_q + int64_t(h) * a.G + g4) * a.max_pages + p0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = 2 * t4 + e;
+        if (p0 + j < n) out[j] = ((ok >> (4 * j)) & 1u) ? acc[e] + acc[2 + e] : __int_as_float(0x7fc00000);
+      }
+    }
+    if (gi + 1 < kQhGroups) {
+#pragma unroll
+      for (int i = 0; i < NP; ++i) cur[i] = nxt[i];
+    }
+  }
+}
+
+template <typename T, int D>
+sa_status launch_score_qh(const ScoreArgs& a, cudaStream_t s) {
+  const int per_cta = 8 * kQhGroups * kQhWarps;
+  const int cap = a.max_pages < a.bt_stride ? a.max_pages : a.bt_stride;
+  const dim3 grid(unsigned((cap + per_cta - 1) / per_cta), unsigned(a.H_kv), unsigned(a.B));
+  score_qh_kernel<T, D><<<grid, 32 * kQhWarps, 0, s>>>(a);
+  return launch_status();
+}
+
 int g_sc_smem[8][64];
 
 template <typename T, int D, bool kQH>
@@ -425,6 +550,11 @@ sa_status sa::score_impl(const sa_cache* cache, const sa_batch* batch, const voi
   const int grid = int(max_chunks < full ? max_chunks : full);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = cache->dtype == SA_BF16;
+  if (per_query_head && G <= 8) {
+    if (cache->head_dim == 128)
+      return bf ? launch_score_qh<__nv_bfloat16, 128>(a, s) : launch_score_qh<__half, 128>(a, s);
+    return bf ? launch_score_qh<__nv_bfloat16, 64>(a, s) : launch_score_qh<__half, 64>(a, s);
+  }
   if (per_query_head) {
     if (cache->head_dim == 128)
       return bf ? launch_score<__nv_bfloat16, 128, true>(a, grid, s, g_sc_smem[4])

@@ -92,3 +92,44 @@ def test_per_head_agrees_with_group_of_one():
                 assert torch.equal(a.out[r, h].view(torch.int16), b.out[r, h].view(torch.int16))
                 assert torch.equal(a.lse[r, h].view(torch.int32), b.lse[r, h].view(torch.int32))
     assert same >= cfg.B * cfg.H_kv // 2
+
+
+@pytest.mark.parametrize("G", [8, 16])
+def test_per_head_scores_bad_block_and_overflow(G):
+    """A page with an out-of-range block id scores NaN for every head of its
+    KV head and sets SA_DEV_BAD_BLOCK; a request longer than its block-table
+    row sets SA_DEV_OVERFLOW and is scored up to the row's end; every other
+    page's scores match the oracle."""
+    from sparse_paged_kv_page_gb300 import sa_score_pages_qh
+    from sparse_paged_kv_page_gb300._lib import SA_DEV_BAD_BLOCK, SA_DEV_OVERFLOW
+    cfg = config(3, small=True)
+    cfg = cfg.replace(H_q=cfg.H_kv * G)
+    wl = make_workload(cfg)
+    c = wl.cfg
+    dec = make_decoder(wl, extra=dict(per_query_head=True))
+    q = dev_bits(wl.q(0), c.dtype)
+    lens, bt = dec.seq_lens.clone(), dec.block_table.clone()
+    dec.block_table[1, 1] = wl.num_blocks + 3
+    dec.seq_lens[0] = dec.block_table.shape[1] * c.ps + 50
+    dec.scores.fill_(7.0)
+    sa_score_pages_qh(dec.cache.struct, dec.batch, q, c.H_q, c.w_avg, c.w_peak, dec.scores, dec.max_pages,
+                      dev_status=dec.dev_status)
+    torch.cuda.synchronize()
+    st = dev_status(dec)
+    assert st & SA_DEV_BAD_BLOCK and st & SA_DEV_OVERFLOW
+    scores = dec.scores.cpu().numpy()
+    row = dec.block_table.shape[1]
+    assert np.all(scores[0, :, :row] != 7.0)                # the overflowing request: its whole row scored
+    for b in (1, 2):
+        for g in range(c.H_q):
+            S, A, L = _head_oracle(wl, b, g, 0, wl.q(0)[b])
+            n = O.num_pages(L, c.ps)
+            got = scores[b, g, :n]
+            if b == 1:
+                assert np.isnan(got[1])
+                keep = np.arange(n) != 1
+                assert_scores(got[keep], S[keep], A[keep])
+            else:
+                assert_scores(got, S, A)
+    dec.block_table.copy_(bt)
+    dec.seq_lens.copy_(lens)
