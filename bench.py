@@ -768,7 +768,8 @@ def main():
         elif c.ps > 1 and args.per_query_head:
             ab = res["score_ab"]
             kms = res["kern"]["score"]
-            tr = None
+            tr = traffic_from_profile("score.cu", "score_qh.long_context_gqa.md") \
+                if args.config == 5 and c.H_q // c.H_kv <= 8 else None
             kname = ("score_qh_kernel" if c.H_q // c.H_kv <= 8 else "score_kernel<per-head>") + " (sa_score_pages_qh)"
         elif c.ps > 1:
             ab = res["score_ab"]
