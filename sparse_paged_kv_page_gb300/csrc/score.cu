@@ -360,15 +360,17 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
         const uint32_t m0[4] = {vmn.x, vmn.y, vmn.z, vmn.w};
         const uint32_t m1[4] = {vmx.x, vmx.y, vmx.z, vmx.w};
         const uint32_t m2[4] = {vme.x, vme.y, vme.z, vme.w};
+        float acc_p = 0.f, acc_n = 0.f;                    // three independent FMA chains
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           acc = fmaf(ca[2 * e], E::lo(m2[e]), acc);
           acc = fmaf(ca[2 * e + 1], E::hi(m2[e]), acc);
-          acc = fmaf(cp[2 * e], E::lo(m1[e]), acc);
-          acc = fmaf(cp[2 * e + 1], E::hi(m1[e]), acc);
-          acc = fmaf(cn[2 * e], E::lo(m0[e]), acc);
-          acc = fmaf(cn[2 * e + 1], E::hi(m0[e]), acc);
+          acc_p = fmaf(cp[2 * e], E::lo(m1[e]), acc_p);
+          acc_p = fmaf(cp[2 * e + 1], E::hi(m1[e]), acc_p);
+          acc_n = fmaf(cn[2 * e], E::lo(m0[e]), acc_n);
+          acc_n = fmaf(cn[2 * e + 1], E::hi(m0[e]), acc_n);
         }
+        acc += acc_p + acc_n;
       }
 #pragma unroll
       for (int o = LPP / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
