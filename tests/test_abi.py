@@ -71,6 +71,19 @@ def test_misaligned_pointers_are_rejected_on_the_host(lib):
         st = lib.sa_score_pages(ctypes.byref(cache), ctypes.byref(batch), qq, 1, 1.0, 0.25, scores, 4,
                                 None, None)
         assert st == 1, field
+    # q read in 16-byte units by the decode, entmax and Gaussian entry points too
+    kw = dict(good)
+    kw["kstd"] = ctypes.c_void_p(0x600000)
+    cache = _lib.SaCache(**kw)
+    bad_q = ctypes.c_void_p(0x400004)
+    P = ctypes.c_void_p
+    sel, cnt, out = P(0x700000), P(0x710000), P(0x720000)
+    assert lib.sa_sparse_decode(ctypes.byref(cache), ctypes.byref(batch), bad_q, 1, sel, cnt, 4, 0.0, out,
+                                None, None, 0, P(0x730000), 1 << 20, None, None) == 1
+    assert lib.sa_sparse_decode_entmax(ctypes.byref(cache), ctypes.byref(batch), bad_q, 1, sel, cnt, 4, 1.5,
+                                       0.0, out, None, None, 0, P(0x730000), 1 << 20, None, None) == 1
+    assert lib.sa_gauss_select(ctypes.byref(cache), ctypes.byref(batch), bad_q, 1, 1.5, 0.0, scores, 4, sel,
+                               cnt, 4, None, None, None) == 1
 
 
 def test_struct_layouts_match_the_binding(lib):
