@@ -508,8 +508,11 @@ def merge_partials(o_parts, lse_parts):
     """Merge split-K partial states by their log-sum-exps.
 
     [vllmcpp] MergeAttnStates: lse = log sum_s exp(lse_s), o = sum_s
-    exp(lse_s - lse) o_s; a +inf lse is treated as -inf (an empty split);
-    when every split is empty the result is o = 0, lse = -inf.
+    exp(lse_s - lse) o_s; a +inf lse is treated as -inf (an empty split).
+    When every split is empty the sum is 0/0; that test's reference then
+    emits the PREFIX output with lse = -inf, so the result is the first
+    part's o (the prefix is part 0) and lse = -inf. (A decode split with no
+    keys carries o = 0, so an empty request still yields o = 0.)
     o_parts: [S, G, D]; lse_parts: [S, G].
     """
     o_parts = np.asarray(o_parts, dtype=np.float64)
@@ -521,6 +524,7 @@ def merge_partials(o_parts, lse_parts):
     for g in range(G):
         m = lse[:, g].max()
         if not np.isfinite(m):
+            o[g] = o_parts[0, g, :]
             continue
         w = np.exp(lse[:, g] - m)
         tot = w.sum()

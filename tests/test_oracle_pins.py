@@ -142,6 +142,29 @@ def test_cache_meta_ignores_positions_past_length():
 # ---------------------------------------------------------------------------
 # A2 page scores
 # ---------------------------------------------------------------------------
+def test_head_meta_is_cache_meta_of_one_head_and_brute_force():
+    """head_meta over one KV head's rows equals that head's slice of
+    cache_meta, and both equal min / max / once-rounded mean of each page's
+    valid rows taken directly (a partial tail page included)."""
+    rng = np.random.default_rng(19)
+    for dtype in ("bf16", "fp16"):
+        L, H, D, ps = 53, 3, 8, 16
+        bits = O.encode_kdt(rng.standard_normal((L + 7, H, D)) * 3, dtype)   # rows past L are stale
+        mn, mx, me = O.cache_meta(bits, L, ps, dtype)
+        x = O.decode_kdt(bits, dtype)
+        for h in range(H):
+            hm = O.head_meta(bits[:, h, :], L, ps, dtype)
+            for a, c in zip(hm, (mn, mx, me)):
+                assert np.array_equal(a, c[:, h, :])
+            for p in range(4):
+                rows = x[p * ps:min((p + 1) * ps, L), h, :]
+                assert np.array_equal(hm[0][p], np.min(rows, axis=0))
+                assert np.array_equal(hm[1][p], np.max(rows, axis=0))
+                # the exact sum / f rounded once (round_to_kdt is pinned above)
+                assert np.array_equal(hm[2][p], O.round_to_kdt(rows.sum(0) / rows.shape[0], dtype))
+        assert mn.shape == (4, H, D)
+
+
 def test_envelope_bounds_true_max_per_head_and_group():
     rng = np.random.default_rng(6)
     for _ in range(200):
@@ -358,8 +381,8 @@ def test_merge_edge_cases_from_vllmcpp_construction():
             e = expect.get((t, h))
             if e == "suffix":
                 assert np.allclose(o[0], s_out[t, h], atol=1e-15) and lse[0] == s_lse[h, t]
-            elif e == "empty":
-                assert np.all(o == 0) and lse[0] == -np.inf
+            elif e == "prefix":
+                assert np.array_equal(o[0], p_out[t, h]) and lse[0] == -np.inf
             else:
                 # both finite: the merge weights are a softmax over the two lse
                 w = 1.0 / (1.0 + math.exp(s_lse[h, t] - p_lse[h, t]))
@@ -689,6 +712,38 @@ def test_entmax_special_cases():
     assert np.allclose(O.entmax(z, 1.001), sm, atol=5e-3)
 
 
+def test_attention_entmax_by_hand_with_a_non_unit_scale():
+    """Two query rows, three keys, scale 1/2, every product worked out by hand.
+
+    Row 0: q = (1, 2); q.k = (1, 2, -3), z = (0.5, 1, -1.5). Sparsemax
+    (alpha 2): sorted (1, 0.5, -1.5), support 2 (1 + 2 * 0.5 > 1.5,
+    1 + 3 * -1.5 < 0.5... gives tau = (1 + 0.5 - 1) / 2 = 0.25), p = (0.25,
+    0.75, 0), o = 0.25 * (4, 0) + 0.75 * (0, 8) = (1, 6).
+    Row 1: q = (0, 0): equal logits, p = 1/3 each, tau = 0 - 1/3.
+    Without the scale row 0 would give tau = 1, p = (0, 1, 0), o = (0, 8);
+    with q and k swapped in the product the shapes would not even agree."""
+    q = np.array([[1.0, 2.0], [0.0, 0.0]])
+    k = np.array([[1.0, 0.0], [0.0, 1.0], [-1.0, -1.0]])
+    v = np.array([[4.0, 0.0], [0.0, 8.0], [100.0, 100.0]])
+    o, tau, z = O.attention_entmax(q, k, v, 0.5, 2.0)
+    assert np.array_equal(z, [[0.5, 1.0, -1.5], [0.0, 0.0, 0.0]])
+    assert np.allclose(o[0], [1.0, 6.0], atol=1e-15) and abs(tau[0] - 0.25) < 1e-15
+    assert np.allclose(o[1], v.mean(0), atol=1e-13) and abs(tau[1] + 1.0 / 3.0) < 1e-15
+    # 1.5-entmax of two keys: a = z / 2 = (q.k) / 4; with q.k = (2, 0),
+    # a = (0.5, 0); both in the support iff (a1 - t)^2 + (a2 - t)^2 = 1 has
+    # its root t below a2 = 0: t = (0.5 - sqrt(0.25 - 2 * (0.25 - 1))) / 2
+    # = (0.5 - sqrt(1.75)) / 2 < 0, so p = ((0.5 - t)^2, t^2).
+    q2 = np.array([[2.0, 0.0]])
+    k2 = np.array([[1.0, 3.0], [0.0, -5.0]])
+    v2 = np.array([[1.0, 0.0], [0.0, 1.0]])
+    o2, tau2, z2 = O.attention_entmax(q2, k2, v2, 0.5, 1.5)
+    t = (0.5 - math.sqrt(1.75)) / 2
+    assert np.array_equal(z2, [[1.0, 0.0]])
+    assert abs(tau2[0] - t) < 1e-15
+    assert np.allclose(o2[0], [(0.5 - t) ** 2, t * t], atol=1e-15)
+    assert abs((0.5 - t) ** 2 + t * t - 1.0) < 1e-14
+
+
 def test_page_decode_unit_entmax_with_every_page_is_dense_entmax():
     """All pages selected: the unit's entmax output is entmax attention over
     every cached token, and alpha = 1 keeps the softmax path."""
@@ -806,6 +861,54 @@ def test_gauss_select_rule():
     a = set(O.gauss_select(m, v, fill, 0.5, 2.0).tolist())
     b = set(O.gauss_select(m, v, fill, 2.0, 2.0).tolist())
     assert b <= a
+
+
+def test_gauss_select_against_the_pages_known_maxima():
+    """Pages built so the maximum of their scores is known exactly, the
+    threshold crossing it: every single-token page and every page of equal
+    keys (v = 0) is kept exactly when its one score value is in the entmax
+    support at tau_hat ((alpha - 1) z > tau_hat), whatever kappa is; a page of
+    two-valued scores (Hadamard rows: scores m +- s, half each, so v = s^2)
+    whose top value crosses is always kept (kappa_16 > 1 makes the estimate
+    an upper bound of that top value); such a page whose top value stays
+    below but whose estimate m + kappa s crosses is kept too (the estimate,
+    not the sample, decides), and one whose estimate stays below is dropped.
+    The tail (last page) is kept regardless."""
+    H = _hadamard(16)[:, 1:2]                             # one +-1 column, 16 tokens
+    scale = 0.5
+    q = np.array([1.0])
+    kap = math.sqrt(2 * math.log(16))
+    for alpha in (1.5, 2.0):
+        th = 0.8 * (alpha - 1.0)                          # a score z crosses iff z > 0.8
+        pages, top, kind = [], [], []
+        # single tokens (f = 1): z = scale * key
+        for key in (1.2, 1.6, 1.61, -4.0):
+            pages.append(np.array([[key]])); top.append(scale * key); kind.append("point")
+        # equal keys (f = 16, v = 0)
+        for key in (1.0, 2.0):
+            pages.append(np.full((16, 1), key)); top.append(scale * key); kind.append("point")
+        # two-valued pages: key = c + d * (+-1): m = scale c, s = scale d
+        for c_, d_, want in ((1.2, 0.6, "top"), (0.8, 0.5, "est"), (0.0, 0.25, "none")):
+            pages.append(c_ + d_ * H); top.append(scale * (c_ + d_)); kind.append(want)
+        pages.append(np.array([[-9.0]])); top.append(-4.5); kind.append("tail")
+        means = np.array([pg.mean(0) for pg in pages])
+        stds = np.array([O.page_std(pg, "bf16") for pg in pages])
+        fill = np.array([pg.shape[0] for pg in pages])
+        m, v = O.gauss_page_moments(q, means, stds, scale)
+        sel = set(O.gauss_select(m, v, fill, th, alpha).tolist())
+        n = len(pages)
+        for p in range(n):
+            crosses = (alpha - 1.0) * top[p] > th
+            if kind[p] == "point":
+                assert (p in sel) == crosses, (alpha, p, top[p])
+            elif kind[p] == "top":
+                assert crosses and p in sel
+            elif kind[p] == "est":
+                assert not crosses and (alpha - 1.0) * (m[p] + kap * math.sqrt(v[p])) > th
+                assert p in sel
+            elif kind[p] == "none":
+                assert (alpha - 1.0) * (m[p] + kap * math.sqrt(v[p])) < th and p not in sel
+        assert n - 1 in sel and not (alpha - 1.0) * top[n - 1] > th
 
 
 def test_gauss_decode_unit_one_page_is_dense_entmax():
