@@ -575,8 +575,11 @@ sa_status sa_gauss_select(const sa_cache* cache, const sa_batch* batch, const vo
  *   shard_cnt; entries beyond shard_stride set SA_DEV_OVERFLOW.
  * sa_merge_states: o_parts [num_shards, rows, head_dim] (dtype), lse_parts
  *   [num_shards, rows] float32 (natural log; -inf for an empty part) ->
- *   out [rows, head_dim] (dtype) and lse (nullable) [rows]; all parts empty
- *   gives o = 0, lse = -inf.
+ *   out [rows, head_dim] (dtype) and lse (nullable) [rows]; +inf and NaN
+ *   count as empty parts. A row whose parts are all empty would be 0/0:
+ *   as in the MergeAttnStates test's reference, it takes the prefix (part
+ *   0) output and lse = -inf (a sa_sparse_decode part with no keys holds
+ *   o = 0, so an empty request still merges to 0).
  */
 sa_status sa_shard_lengths(const int32_t* seq_lens, int32_t batch, int32_t page_size, int32_t page_lo,
                            int32_t page_hi, int32_t* shard_lens, void* stream);
@@ -586,6 +589,23 @@ sa_status sa_shard_selection(const int32_t* sel_idx, const int32_t* sel_cnt, int
                              void* stream);
 sa_status sa_merge_states(const void* o_parts, const float* lse_parts, int32_t num_shards, int32_t rows,
                           int32_t head_dim, int32_t dtype, void* out, float* lse, void* stream);
+
+/*
+ * Self-test of the bounded in-kernel wait (no counterpart on the pages: it
+ * checks this library's "Bad data" contract -- every wait inside a kernel
+ * gives up after a time limit, sets SA_DEV_TIMEOUT in the caller's status
+ * word and lets the kernel return, so the context stays usable).
+ *
+ * One warp waits, through the wait the library's kernels use, on an mbarrier
+ * that expects two arrivals and receives `arrivals` (0, 1 or 2) of them,
+ * giving up after limit_ns (0 < limit_ns <= 100 ms) instead of the default
+ * ~1 s. arrivals = 2: the wait completes, *result = 1, dev_status unchanged.
+ * arrivals < 2: the wait runs out, *result = 0 and SA_DEV_TIMEOUT is set.
+ * dev_status, result: device int32 (caller-owned). Asynchronous on `stream`;
+ * SA_ERR_INVALID_ARG for other arguments, nothing launched.
+ */
+sa_status sa_wait_selftest(int32_t arrivals, int64_t limit_ns, int32_t* dev_status, int32_t* result,
+                           void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* sa_status_string(sa_status status);

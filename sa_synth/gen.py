@@ -286,19 +286,25 @@ class Workload:
         """Length of request b after ``steps_done`` decode-step appends."""
         return int(self.prefill_lens[b]) + steps_done
 
-    def k_seq(self, b: int, steps_done: int = 0) -> np.ndarray:
-        """Logical keys of request b (prefill then appended), uint16 [L, H_kv, D]."""
-        return self._seq(b, steps_done, 0)
+    def k_seq(self, b: int, steps_done: int = 0, head: Optional[int] = None) -> np.ndarray:
+        """Logical keys of request b (prefill then appended), uint16 [L, H_kv, D]
+        (or [L, D] of one KV head when ``head`` is given)."""
+        return self._seq(b, steps_done, 0, head)
 
-    def v_seq(self, b: int, steps_done: int = 0) -> np.ndarray:
-        return self._seq(b, steps_done, 1)
+    def v_seq(self, b: int, steps_done: int = 0, head: Optional[int] = None) -> np.ndarray:
+        return self._seq(b, steps_done, 1, head)
 
-    def _seq(self, b, steps_done, which):
+    def _seq(self, b, steps_done, which, head=None):
         src = self.k_pre if which == 0 else self.v_pre
         rows = src[self.pre_cu[b]:self.pre_cu[b + 1]]
+        if head is not None:
+            rows = rows[:, head]
         if steps_done == 0:
             return rows
-        new = np.stack([self.kv_new(t)[which][b] for t in range(steps_done)], 0)
+        if head is None:
+            new = np.stack([self.kv_new(t)[which][b] for t in range(steps_done)], 0)
+        else:
+            new = np.stack([self.kv_new(t)[which][b, head] for t in range(steps_done)], 0)
         return np.concatenate([rows, new], 0)
 
 

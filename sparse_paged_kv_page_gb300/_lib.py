@@ -79,6 +79,7 @@ SIGNATURES = {
                                    c_ptr]),
     "sa_merge_states": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_i32, c_i32, c_ptr, c_ptr, c_ptr]),
     "sa_struct_size": (c_size, [c_i32]),
+    "sa_wait_selftest": (c_i32, [c_i32, ctypes.c_int64, c_ptr, c_ptr, c_ptr]),
     "sa_status_string": (ctypes.c_char_p, [c_i32]),
     "sa_version": (ctypes.c_char_p, []),
 }

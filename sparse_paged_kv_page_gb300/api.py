@@ -24,7 +24,7 @@ __all__ = ["SaError", "SaCache", "SaBatch", "make_cache", "make_batch", "PagedKV
            "alloc_entmax_workspace", "sa_sparse_decode_entmax", "sa_sparse_decode_entmax_qh",
            "sa_gauss_select", "sa_shard_lengths", "sa_shard_selection", "sa_merge_states",
            "batch_view",
-           "sa_status_string", "sa_struct_size",
+           "sa_status_string", "sa_struct_size", "sa_wait_selftest",
            "sa_version", "alloc_decode_workspace"]
 
 _DT = {torch.bfloat16: _lib.SA_BF16, torch.float16: _lib.SA_FP16}
@@ -298,6 +298,15 @@ def sa_merge_states(o_parts, lse_parts, num_shards: int, rows: int, head_dim: in
         _p(o_parts, name="o_parts"), _p(lse_parts, torch.float32, "lse_parts"), int(num_shards),
         int(rows), int(head_dim), _DT[o_parts.dtype], _p(out, name="out"),
         _p(lse, torch.float32, "lse"), _s(stream)))
+
+
+def sa_wait_selftest(arrivals: int, limit_ns: int, dev_status, result, stream=None):
+    """The library's bounded in-kernel wait on an mbarrier given `arrivals` of
+    its 2 expected arrivals (fewer: it runs out after limit_ns, sets
+    SA_DEV_TIMEOUT and writes result = 0)."""
+    _check("sa_wait_selftest", _lib.load().sa_wait_selftest(
+        int(arrivals), int(limit_ns), _p(dev_status, torch.int32, "dev_status"),
+        _p(result, torch.int32, "result"), _s(stream)))
 
 
 def batch_view(block_table: torch.Tensor, seq_lens: torch.Tensor, page_lo: int) -> SaBatch:

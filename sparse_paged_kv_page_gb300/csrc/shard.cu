@@ -4,8 +4,9 @@
 // "test_ops_mla_chunked_context.cpp" (vllm.cpp tests), "MergeAttnStates":
 // attention over a split of the keys is exact once the partial states are
 // merged by their log-sum-exp, lse = log sum_s exp(lse_s), o = sum_s
-// exp(lse_s - lse) o_s, an empty part carrying lse = -inf and the all-empty
-// case giving o = 0, lse = -inf. "EntmaxKV" README, "How it works" / "Top-k":
+// exp(lse_s - lse) o_s, an empty part carrying lse = -inf; when every part is
+// empty (0/0) the test's reference emits the prefix output, so the merge
+// returns part 0's o with lse = -inf (a decode part with no keys holds o = 0). "EntmaxKV" README, "How it works" / "Top-k":
 // the selection is the top pages of the whole request with the tail page
 // forced, so each shard scores its own pages into its slice of the request's
 // score row (the exchange step), one selection is taken over the whole row,
@@ -78,8 +79,12 @@ __global__ void merge_states_kernel(const uint16_t* o_parts, const float* lse_pa
   if (!empty)
     for (int s = 0; s < S; ++s) l += expf(part_lse(lse_parts, int64_t(s) * rows + r) - m);
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    if (empty) {                                // every part empty: the prefix (part 0) output
+      out[int64_t(r) * D + d] = o_parts[int64_t(r) * D + d];
+      continue;
+    }
     float o = 0.f;
-    if (!empty) {
+    {
       for (int s = 0; s < S; ++s) {
         const float w = expf(part_lse(lse_parts, int64_t(s) * rows + r) - m);   // 0 for an empty part
         if (w > 0.f) o = fmaf(w, E::lo(uint32_t(o_parts[(int64_t(s) * rows + r) * D + d])), o);

@@ -123,8 +123,76 @@ def oracle_unit(wl: Workload, b: int, h: int, steps_done: int, q_bits):
     """Oracle of one (request, KV head) after `steps_done` appends, for query q_bits [H_q, D]."""
     c = wl.cfg
     L = wl.seq_len(b, steps_done)
-    ks = wl.k_seq(b, steps_done)[:, h, :]
-    vs = wl.v_seq(b, steps_done)[:, h, :]
+    ks = wl.k_seq(b, steps_done, head=h)
+    vs = wl.v_seq(b, steps_done, head=h)
     qg = q_bits[h * c.G:(h + 1) * c.G]
     return O.page_decode_unit(ks, vs, L, qg, ps=c.ps, topk=c.topk, w_avg=c.w_avg,
                               w_peak=c.w_peak, dtype=c.dtype, scale=c.scale), ks, vs, qg, L
+
+
+def h2o_teacher_forced(dec, wl, units, steps, window=False, every_unit_invariants=True):
+    """Run `steps` token-level decode steps on the GPU and check each sampled
+    (request, KV head) unit at every step against the oracle started from the
+    GPU's own state before that step: its retained list and its bf16 scores.
+
+    Per unit and step:
+      * attention output of the step within atol 2e-2 + rtol 2e-2;
+      * the GPU's folded bf16 score of every entry (the new token included)
+        within 1 bf16 ulp of the oracle's once-rounded float64 fold;
+      * the oracle's eviction rule applied to the GPU's own folded bf16
+        scores reproduces the GPU's retained list and its evicted positions
+        bit for bit (the rule is exact integer / bf16 comparison, so this is
+        the form in which eviction parity is well defined).
+    Every unit (sampled or not) keeps the budget, sinks and grace entries.
+    Returns the number of (unit, step) checks made."""
+    c = wl.cfg
+    bt = wl.block_table
+    rows = lambda h: slice(h * c.G, (h + 1) * c.G)
+    rp, rc = dec.ret_pos.cpu().numpy(), dec.ret_cnt.cpu().numpy()
+    hh = host_bits(dec.cache.hh)
+    prev = {}
+    for b, h in units:
+        pos = rp[b, h, :rc[b, h]].astype(np.int64)
+        prev[(b, h)] = (pos, O.decode_kdt(hh[bt[b, pos], h], "bf16"))
+    checks = 0
+    for t in range(steps):
+        q, kn, vn = step_inputs(wl, t)
+        dec.step(q, kn, vn)
+        torch.cuda.synchronize()
+        rp, rc = dec.ret_pos.cpu().numpy(), dec.ret_cnt.cpu().numpy()
+        ev, evc = dec.evicted.cpu().numpy(), dec.evicted_cnt.cpu().numpy()
+        hh = host_bits(dec.cache.hh)
+        out = dec.out.float().cpu().numpy()
+        qb = wl.q(t)
+        if every_unit_invariants:
+            for b in range(c.B):
+                L = wl.seq_len(b, t + 1)
+                for h in range(c.H_kv):
+                    k = int(rc[b, h])
+                    assert k == min(c.budget, L), (t, b, h, k)
+                    gk = rp[b, h, :k]
+                    assert gk[:c.n_sink].tolist() == list(range(c.n_sink))
+                    if c.grace:
+                        assert gk[-c.grace:].tolist() == list(range(L - c.grace, L))
+        for b, h in units:
+            pos0, hb0 = prev[(b, h)]
+            L = wl.seq_len(b, t + 1)
+            assert L - 1 not in set(pos0.tolist())
+            pos = np.append(pos0, L - 1)
+            hb = np.append(hb0, 0.0)                  # zeroed on write by the append
+            r = O.h2o_unit_step(hb, pos, wl.k_seq(b, t + 1, head=h), wl.v_seq(b, t + 1, head=h),
+                                qb[b, rows(h)], dtype=c.dtype, decay=c.decay, budget=c.budget,
+                                n_sink=c.n_sink, grace=c.grace, scale=c.scale,
+                                window_softmax=window)
+            assert_attention(out[b, rows(h)], r["out"])
+            g = O.decode_kdt(hh[bt[b, pos], h], "bf16")      # the GPU's folded score of every entry
+            ulp = O.ulp_kdt(np.maximum(np.abs(g), np.abs(r["hh_bf16"])), "bf16")
+            bad = np.abs(g - r["hh_bf16"]) > ulp
+            assert not bad.any(), (t, b, h, np.nonzero(bad)[0][:5])
+            kept, _, evd = O.h2o_evict(g, pos, c.budget, c.n_sink, c.grace)
+            gk = rp[b, h, :rc[b, h]].astype(np.int64)
+            assert np.array_equal(gk, kept), (t, b, h)
+            assert ev[b, h, :evc[b, h]].tolist() == sorted(evd), (t, b, h)
+            prev[(b, h)] = (gk, g[np.isin(pos, gk)])
+            checks += 1
+    return checks

@@ -48,6 +48,14 @@ def test_host_only_calls(lib):
                               0, 1, None, None, 0.0, None, None, None, 0, None, None) == 1
 
 
+def test_wait_selftest_rejects_bad_arguments_on_the_host(lib):
+    import ctypes
+    st, res = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000)
+    for arrivals, limit in ((3, 1000), (-1, 1000), (1, 0), (1, 200_000_000)):
+        assert lib.sa_wait_selftest(arrivals, limit, st, res, None) == 1
+    assert lib.sa_wait_selftest(1, 1000, None, res, None) == 1
+
+
 def test_misaligned_pointers_are_rejected_on_the_host(lib):
     """Pools and q must start on 16-byte boundaries; the check runs before any
     launch (the pointer values are never dereferenced on the host)."""

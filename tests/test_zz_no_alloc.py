@@ -2,17 +2,19 @@
 device memory at the call site (plugins given fixed buffers, frozen memory
 plans, allocation-free real-time loops).
 
-It must give the same results as sa_sparse_decode with a caller workspace --
-within the decode tolerance of the other tests -- on two calls in a row (the
-second reuses the shared scratch the first left behind), and refuse sizes that
-need more scratch than its fixed capacity. Kept in a file collected last.
+It must give the same results as sa_sparse_decode with a caller workspace and
+as the oracle's attention over the same given selection -- within the decode
+tolerance of the other tests -- on two calls in a row (the second reuses the
+shared scratch the first left behind), and refuse sizes that need more scratch
+than its fixed capacity. Kept in a file collected last.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle as O
 from sa_synth import config, make_workload
-from gpu_util import make_decoder, dev_bits
+from gpu_util import make_decoder, dev_bits, assert_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +46,18 @@ def test_noalloc_matches_workspace_decode_twice():
     ref_l = torch.empty_like(dec.lse)
     S.sa_sparse_decode(dec.cache.struct, dec.batch, q, cfg.H_q, sel, cnt, cfg.topk, 0.0, ref_o,
                        lse=ref_l, workspace=ws, dev_status=dec.dev_status)
+    # the oracle's attention of every (request, KV head) over the same given selection
+    sc = O.default_scale(cfg.D)
+    sel_h, cnt_h = sel.cpu().numpy(), cnt.cpu().numpy()
+    want = {}
+    for b in range(cfg.B):
+        L = int(wl.prefill_lens[b])
+        for h in range(cfg.H_kv):
+            pos = O.selected_positions(sel_h[b, h, :cnt_h[b, h]], L, cfg.ps)
+            k = O.decode_kdt(wl.k_seq(b, head=h)[pos], cfg.dtype)
+            v = O.decode_kdt(wl.v_seq(b, head=h)[pos], cfg.dtype)
+            qg = O.decode_kdt(wl.q(0)[b, h * cfg.G:(h + 1) * cfg.G], cfg.dtype)
+            want[(b, h)] = O.attention(qg, k, v, sc)[:2]
     for call in range(2):
         out = torch.full_like(dec.out, float("nan"))
         lse = torch.full_like(dec.lse, float("nan"))
@@ -53,6 +67,10 @@ def test_noalloc_matches_workspace_decode_twice():
         a, b = out.float().cpu().numpy(), ref_o.float().cpu().numpy()
         assert np.all(np.abs(a - b) <= 2e-2 + 2e-2 * np.abs(b)), call
         assert np.allclose(lse.cpu().numpy(), ref_l.cpu().numpy(), atol=1e-3), call
+        ln = lse.cpu().numpy()
+        for (bb, h), (wo, wlse) in want.items():
+            rows = slice(h * cfg.G, (h + 1) * cfg.G)
+            assert_attention(a[bb, rows], wo, ln[bb, rows], wlse)
     assert int(dec.dev_status.item()) == 0
 
 
