@@ -11,8 +11,17 @@ the vllm.cpp chunked-context test; "EntmaxKV" README, Top-k).
 
 `SequenceShards` runs all shards of one cache on one device (each shard a
 view of its page range), which is how the sharded path is exercised on a
-single GPU; `gather_slices` is the exchange when the shards live on
-different ranks (torch.distributed all-gather, plumbing only).
+single GPU. When the shards live on different ranks the step has two
+exchanges (torch.distributed all-gathers, plumbing only): `gather_slices`
+joins the score slices of every rank's page range (ranges may differ by a
+page) into whole rows before the selection, and `gather_states` collects every
+rank's partial (o, lse) for `sa_merge_states` (`merge_across_ranks`).
+
+KV-head partitioning needs no exchange at all: a rank holding KV heads
+[h0, h1) keeps those heads' pool and statistics slices and their G query
+heads each, and decodes them exactly as the whole cache would
+(`kv_head_slice`, `query_head_slice`); the rows of the heads it holds are the
+output of the step for those heads.
 """
 from __future__ import annotations
 
@@ -38,13 +47,67 @@ def page_ranges(num_pages: int, num_shards: int) -> List[Tuple[int, int]]:
 
 
 def gather_slices(local: torch.Tensor, dim: int, group=None) -> torch.Tensor:
-    """All-gather of equally shaped per-rank slices, concatenated along `dim`
-    in rank order (the score rows of a sharded step)."""
+    """All-gather of per-rank slices along `dim`, concatenated in rank order
+    (the score rows of a sequence-sharded step: each rank's page range, whose
+    widths may differ, e.g. 2732 / 2731 / 2731). The widths are exchanged
+    first; every slice is padded to the widest for the gather and trimmed after."""
     import torch.distributed as dist
     world = dist.get_world_size(group)
-    parts = [torch.empty_like(local) for _ in range(world)]
-    dist.all_gather(parts, local.contiguous(), group=group)
-    return torch.cat(parts, dim=dim)
+    width = torch.tensor([local.shape[dim]], dtype=torch.int64, device=local.device)
+    widths = [torch.zeros_like(width) for _ in range(world)]
+    dist.all_gather(widths, width, group=group)
+    widths = [int(w.item()) for w in widths]
+    shape = list(local.shape)
+    shape[dim] = max(widths)
+    buf = local.new_zeros(shape)
+    buf.narrow(dim, 0, local.shape[dim]).copy_(local)
+    parts = [torch.empty_like(buf) for _ in range(world)]
+    dist.all_gather(parts, buf, group=group)
+    return torch.cat([p.narrow(dim, 0, w) for p, w in zip(parts, widths)], dim=dim)
+
+
+def gather_states(o_part: torch.Tensor, lse_part: torch.Tensor, group=None):
+    """All-gather every rank's partial attention state -- o [..., D] and lse
+    [...] over its own page range (lse = -inf where it attended nothing) --
+    stacked in rank order: ([world, ...D], [world, ...]), the o_parts /
+    lse_parts layout of sa_merge_states."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    o_all = [torch.empty_like(o_part) for _ in range(world)]
+    l_all = [torch.empty_like(lse_part) for _ in range(world)]
+    dist.all_gather(o_all, o_part.contiguous(), group=group)
+    dist.all_gather(l_all, lse_part.contiguous(), group=group)
+    return torch.stack(o_all), torch.stack(l_all)
+
+
+def merge_across_ranks(o_part: torch.Tensor, lse_part: torch.Tensor, out: torch.Tensor,
+                       lse: torch.Tensor = None, group=None):
+    """The second exchange of a sequence-sharded step on several ranks: gather
+    the partial states, then merge them by log-sum-exp on this rank's device
+    (sa_merge_states). o_part [B, H_q, D] (bf16/fp16), lse_part [B, H_q] float32."""
+    o_parts, lse_parts = gather_states(o_part, lse_part, group)
+    rows = o_part.numel() // o_part.shape[-1]
+    sa_merge_states(o_parts, lse_parts, o_parts.shape[0], rows, o_part.shape[-1], out, lse=lse)
+    return out
+
+
+def kv_head_range(num_kv_heads: int, num_ranks: int, rank: int) -> Tuple[int, int]:
+    """KV heads [h0, h1) held by `rank` when the heads are partitioned (as equal as possible)."""
+    return page_ranges(num_kv_heads, num_ranks)[rank]
+
+
+def kv_head_slice(t: torch.Tensor, h0: int, h1: int, head_axis: int = 1) -> torch.Tensor:
+    """The rows of KV heads [h0, h1) of a pool ([num_blocks, H_kv, ps, D]),
+    statistics ([num_blocks, H_kv, 3, D]) or per-token score ([slots, H_kv],
+    head_axis = 1 as well) tensor, as the contiguous tensor a rank holding
+    those heads keeps."""
+    return t.narrow(head_axis, h0, h1 - h0).contiguous()
+
+
+def query_head_slice(q: torch.Tensor, h0: int, h1: int, group_size: int) -> torch.Tensor:
+    """The query heads of KV heads [h0, h1) (each KV head's G consecutive
+    query heads) of q [B, H_q, D]."""
+    return q.narrow(1, h0 * group_size, (h1 - h0) * group_size).contiguous()
 
 
 class SequenceShards:
