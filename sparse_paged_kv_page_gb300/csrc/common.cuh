@@ -204,45 +204,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
   }
   return true;
 }
-// gpu-scope acquire load / release store of a flag another CTA (or kernel) sets
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
-}
-// Wait until *f != 0, giving up after limit_ns (sets SA_DEV_TIMEOUT, returns false).
-__device__ __forceinline__ bool flag_wait(const int32_t* f, int32_t* status,
-                                          uint64_t limit_ns = kWaitLimitNs) {
-  if (ld_acquire_gpu(f)) return true;
-  const uint64_t t0 = global_ns();
-  while (!ld_acquire_gpu(f)) {
-    __nanosleep(64);
-    if (global_ns() - t0 > limit_ns) {
-      flag(status, SA_DEV_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
-// Counters a page-level step shares between its scorer and its selection
-// (int32 in the step's workspace, all zero between steps): the scorer's chunk
-// queue and exit ticket, then per request the consumer-warp chunk completions,
-// a ready flag set once every score of the request is written, and the
-// selection's pass ticket (its last CTA of a request puts the three back to 0).
-struct StepSync {
-  int32_t* base;
-  int B;
-  __device__ int32_t* queue() const { return base; }
-  __device__ int32_t* exit_ticket() const { return base + 1; }
-  __device__ int32_t* done(int b) const { return base + 2 + b; }
-  __device__ int32_t* ready(int b) const { return base + 2 + B + b; }
-  __device__ int32_t* pass_ticket(int b) const { return base + 2 + 2 * B + b; }
-};
-
 // Bulk copy global -> this CTA's shared memory, completion counted in bytes on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -17,19 +17,25 @@
 //
 // Design: persistent CTAs (two per SM). A block's statistics for all KV heads
 // are one contiguous run (head after head), so the KV heads are taken Hc at a
-// time (Hc = gcd(H_kv, consumer lane groups)) and the batch's pages are cut
-// into chunks of 32 / Hc pages x Hc heads of one request: 32 (page, head)
-// pairs per chunk, one TMA copy of Hc heads' rows per page. The chunk list is
-// split evenly across CTAs (a device-side prefix over request lengths, so
-// ragged batches balance). In each CTA one producer warp resolves a chunk's
-// block ids and has the TMA engine gather the pages with one cp.async.bulk
-// each into a 4-stage shared-memory ring, completion counted in bytes on the
-// stage's mbarrier; four consumer warps score from shared memory (D/8 lanes
-// per (page, head), one 16-byte slice of each row per lane, shuffle reduction;
-// a lane group always serves the same head of the group, so its query
-// coefficients stay in registers) and release the stage. Block ids of the
-// next chunks are loaded before waiting for a free stage, so the table lookup
-// overlaps the copies.
+// time (Hc = gcd(H_kv, consumer lane groups)) and the pages into chunks of
+// 32 / Hc pages x Hc heads: 32 (page, head) pairs per chunk, one TMA copy of
+// Hc heads' rows per page. The chunk space runs over the block table's row
+// width, page-major (page run, then request, then head group): CTAs working
+// at the same time read the same logical pages of every request, whose blocks
+// a serving loop that appends to all requests together allocates near each
+// other, so the gathers keep some DRAM locality (on the long-context workload
+// the scorer takes ~39 us this way against ~43 us request by request). A
+// chunk's block ids can be requested before the lengths are known -- the two
+// loads overlap at start-up -- and chunks past a request's length are
+// skipped. CTA i takes chunks i, i + grid, ... In each CTA one producer warp
+// resolves a chunk's block ids and has the TMA engine gather the pages with
+// one cp.async.bulk each into a shared-memory ring, completion counted in
+// bytes on the stage's mbarrier; four consumer warps score from shared memory
+// (D/8 lanes per (page, head), one 16-byte slice of each row per lane,
+// shuffle reduction; a lane group always serves the same head of the group,
+// so its query coefficients stay in registers) and release the stage. Block
+// ids of the next chunk are loaded while the current one is copied; a header
+// with a negative count tells the consumers the producer is done.
 #include "common.cuh"
 #include "host.h"
 
@@ -40,7 +46,7 @@ namespace {
 #define SA_SCORE_CONSUMER_WARPS 4
 #endif
 #ifndef SA_SCORE_STAGES
-#define SA_SCORE_STAGES 4
+#define SA_SCORE_STAGES 3
 #endif
 #ifndef SA_SCORE_CTAS_PER_SM
 #define SA_SCORE_CTAS_PER_SM 2
@@ -61,6 +67,7 @@ struct ScoreArgs {
   int32_t* status;
   int B, H_kv, H_q, G, ps, num_blocks, bt_stride, max_pages;
   int hc_shift;                                            // log2(heads per chunk)
+  int cpr;                                                 // chunks per (request, head group) row
   float w_avg, w_peak;
 };
 
@@ -82,10 +89,10 @@ struct ScoreTile {
 struct ChunkHdr {
   int b, hg, p0, count;                                    // request, head group, pages p0 .. +count
   uint32_t valid;                                          // bit j: page p0+j has a good block
-};
+};                                                         // count < 0: no more chunks
 
 template <typename T, int D, bool kQH>
-__global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs a) {
+__global__ void __maxnreg__(128) score_kernel(ScoreArgs a) {
   using E = Elem<T>;
   using TL = ScoreTile<D, kQH>;
   constexpr int NS = TL::kNStages;
@@ -96,42 +103,39 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
   __shared__ __align__(8) uint64_t coef_bar;               // per-head mode: consumers meet here
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ ChunkHdr hdr[kStages];
-  __shared__ int s_prefix[kMaxBatch + 1];                  // chunks before request b
-  __shared__ int s_pages[kMaxBatch];                       // pages of request b (clamped)
-  __shared__ int scan_tmp[32];
+  __shared__ int s_pages[kMaxBatch];                       // pages of request b (clamped to the row)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hcs = a.hc_shift, Hc = 1 << hcs;
   const int P = kChunk >> hcs;                             // pages per chunk
   const int n_hg = a.H_kv >> hcs;                          // head groups
+  const int cap = min(a.max_pages, a.bt_stride);
+  const int per_req = n_hg * a.cpr;
+  const int total = a.B * per_req;                         // the chunk space
+  // chunk c: page run k = c / (B n_hg) (pages kP .. kP+P-1), then request,
+  // then head group -- page-major, so CTAs working at the same time read
+  // the same logical pages of every request
+  auto locate = [&](int c, int& b, int& hg, int& p0) {
+    const int k = c / (a.B * n_hg);
+    const int r = c - k * (a.B * n_hg);
+    b = r / n_hg;
+    hg = r - b * n_hg;
+    p0 = k * P;
+  };
   pdl_wait();
 
-  // chunk prefix over requests: request b owns n_hg * ceil(n_b / P) chunks
-  {
-    const int per = (a.B + kScThreads - 1) / kScThreads;
-    const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
-    int local = 0;
-    for (int b = b0; b < b1; ++b) {
-      int n = (a.seq_lens[b] + a.ps - 1) / a.ps;
-      n = max(0, min(n, min(a.max_pages, a.bt_stride)));
-      local += n_hg * ((n + P - 1) / P);
-    }
-    int total;
-    int run = block_exclusive_scan<kScThreads>(local, scan_tmp, &total);
-    for (int b = b0; b < b1; ++b) {
-      s_prefix[b] = run;
-      int n = (a.seq_lens[b] + a.ps - 1) / a.ps;
-      n = max(0, min(n, min(a.max_pages, a.bt_stride)));
-      s_pages[b] = n;
-      run += n_hg * ((n + P - 1) / P);
-    }
-    if (tid == 0) s_prefix[a.B] = total;
-    if (tid == 0 && blockIdx.x == 0)
-      for (int b = 0; b < a.B; ++b)
-        if ((a.seq_lens[b] + a.ps - 1) / a.ps > min(a.max_pages, a.bt_stride)) {
-          flag(a.status, SA_DEV_OVERFLOW);
-          break;
-        }
+  // The producer's chunks are blockIdx.x, blockIdx.x + gridDim.x, ...; the
+  // block ids of its first one are requested before the lengths are known.
+  int x_cur = blockIdx.x, cb = 0, cg = 0, cp0 = 0, ck = -1;
+  if (warp == kConsumerWarps && x_cur < total) {
+    locate(x_cur, cb, cg, cp0);
+    ck = (lane < P && cp0 + lane < cap) ? a.bt[int64_t(cb) * a.bt_stride + cp0 + lane] : -1;
+  }
+  for (int b = tid; b < a.B; b += kScThreads) {
+    const int L = a.seq_lens[b];
+    const int n_all = L > 0 ? (L + a.ps - 1) / a.ps : 0;
+    if (n_all > cap && blockIdx.x == 0) flag(a.status, SA_DEV_OVERFLOW);
+    s_pages[b] = min(n_all, cap);
   }
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -145,69 +149,61 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
   // every length this CTA needs is in shared memory: a programmatically
   // launched successor (the step's append) may start now
   pdl_trigger();
-  const int total = s_prefix[a.B];
-  const int c_begin = int((int64_t(total) * blockIdx.x) / gridDim.x);
-  const int c_end = int((int64_t(total) * (blockIdx.x + 1)) / gridDim.x);
-  if (c_begin >= c_end) return;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    auto locate = [&](int ci, int& b, int& hg, int& p0, int& count) {
-      int lo = 0, hi = a.B;                                // largest b with prefix[b] <= ci
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_prefix[mid] <= ci) lo = mid; else hi = mid;
-      }
-      b = lo;
-      const int n = s_pages[b];
-      const int kb = (n + P - 1) / P;
-      const int r = ci - s_prefix[b];
-      hg = r / kb;
-      p0 = (r % kb) * P;
-      count = min(P, n - p0);
-    };
-    // block ids of the next two chunks are in flight while a stage is waited for
-    int b1, g1, p01, c1, k1 = -1, b2 = 0, g2 = 0, p02 = 0, c2 = 0, k2 = -1;
-    locate(c_begin, b1, g1, p01, c1);
-    k1 = lane < c1 ? a.bt[int64_t(b1) * a.bt_stride + p01 + lane] : -1;
-    if (c_begin + 1 < c_end) {
-      locate(c_begin + 1, b2, g2, p02, c2);
-      k2 = lane < c2 ? a.bt[int64_t(b2) * a.bt_stride + p02 + lane] : -1;
-    }
+    // Chunk x_cur is being copied while the block ids of the next one load.
     bool ok = true;
-    for (int ci = c_begin, it = 0; ci < c_end; ++ci, ++it) {
-      const int b = b1, hg = g1, p0 = p01, count = c1, blk = k1;
-      b1 = b2; g1 = g2; p01 = p02; c1 = c2; k1 = k2;
-      if (ci + 2 < c_end) {
-        locate(ci + 2, b2, g2, p02, c2);
-        k2 = lane < c2 ? a.bt[int64_t(b2) * a.bt_stride + p02 + lane] : -1;
+    int it = 0;                                               // stages used (non-empty chunks)
+    while (x_cur < total) {
+      const int x_nxt = x_cur + int(gridDim.x);
+      int nb = 0, ng = 0, np0 = 0, nk = -1;
+      if (x_nxt < total) {
+        locate(x_nxt, nb, ng, np0);
+        nk = (lane < P && np0 + lane < cap) ? a.bt[int64_t(nb) * a.bt_stride + np0 + lane] : -1;
       }
-      const int s = it % NS;
-      if (it >= NS && !mbar_wait(smem_u32(&empty_bar[s]), ((it / NS) - 1) & 1, a.status)) {
-        ok = false;
-        break;
+      const int count = min(P, s_pages[cb] - cp0);
+      if (count > 0) {
+        const int s = it % NS;
+        // the stage is free once the consumers released the chunk NS before
+        // (one lane waits; the warp takes its answer)
+        int freed = 1;
+        if (it >= NS && lane == 0) freed = mbar_wait(smem_u32(&empty_bar[s]), ((it / NS) - 1) & 1, a.status);
+        if (!__shfl_sync(kFull, freed, 0)) {
+          ok = false;
+          break;
+        }
+        const bool good = lane < count && ck >= 0 && ck < a.num_blocks;
+        if (lane < count && !good) flag(a.status, SA_DEV_BAD_BLOCK);
+        const uint32_t valid = __ballot_sync(kFull, good);
+        const uint32_t bytes = uint32_t(TL::kPageBytes) << hcs;   // Hc heads of one block
+        if (lane == 0) {
+          hdr[s] = ChunkHdr{cb, cg, cp0, count, valid};
+          mbar_arrive_expect_tx(smem_u32(&full_bar[s]), uint32_t(__popc(valid)) * bytes);
+        }
+        __syncwarp();
+        if (good) {
+          const uint8_t* src = static_cast<const uint8_t*>(a.meta) +
+                               (int64_t(ck) * a.H_kv + (cg << hcs)) * int64_t(TL::kPageBytes);
+          bulk_g2s(smem_u32(smem + s * TL::kStageBytes + lane * (kQH ? uint32_t(TL::kPageStride) : bytes)),
+                   src, bytes, smem_u32(&full_bar[s]));
+        }
+        ++it;
       }
-      const bool good = lane < count && blk >= 0 && blk < a.num_blocks;
-      if (lane < count && !good) flag(a.status, SA_DEV_BAD_BLOCK);
-      const uint32_t valid = __ballot_sync(kFull, good);
-      const uint32_t bytes = uint32_t(TL::kPageBytes) << hcs;   // Hc heads of one block
-      if (lane == 0) {
-        hdr[s] = ChunkHdr{b, hg, p0, count, valid};
-        mbar_arrive_expect_tx(smem_u32(&full_bar[s]), uint32_t(__popc(valid)) * bytes);
-      }
-      __syncwarp();
-      if (good) {
-        const uint8_t* src = static_cast<const uint8_t*>(a.meta) +
-                             (int64_t(blk) * a.H_kv + (hg << hcs)) * int64_t(TL::kPageBytes);
-        bulk_g2s(smem_u32(smem + s * TL::kStageBytes + lane * (kQH ? uint32_t(TL::kPageStride) : bytes)),
-                 src, bytes, smem_u32(&full_bar[s]));
-      }
+      x_cur = x_nxt; cb = nb; cg = ng; cp0 = np0; ck = nk;
     }
-    // never leave with copies in flight: wait (bounded) for the last stages
+    // Drain: wait (bounded) until the consumers have released the last
+    // stages -- so no copy is in flight -- then tell them there is nothing
+    // more (a header with count -1 in the next stage, whose previous chunk is
+    // released).
     if (lane == 0) {
-      const int n_it = c_end - c_begin;
-      for (int it = max(0, n_it - NS); it < n_it && ok; ++it)
-        ok = mbar_wait(smem_u32(&full_bar[it % NS]), (it / NS) & 1, a.status);
+      for (int j = max(0, it - NS); j < it && ok; ++j)
+        ok = mbar_wait(smem_u32(&empty_bar[j % NS]), (j / NS) & 1, a.status);
+      if (ok) {
+        const int s = it % NS;
+        hdr[s] = ChunkHdr{0, 0, 0, -1, 0u};
+        mbar_arrive(smem_u32(&full_bar[s]));
+      }
     }
     return;
   }
@@ -238,10 +234,11 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
     };
     int cur_b = -1, cur_h = -1;
     const int g4 = lane >> 2, t4 = lane & 3;
-    for (int ci = c_begin, it = 0; ci < c_end && alive; ++ci, ++it) {
+    for (int it = 0; alive; ++it) {
       const int s = it % NS;
-      if (!mbar_wait(smem_u32(&full_bar[s]), (it / NS) & 1, a.status)) break;
+      if (!__all_sync(kFull, mbar_wait(smem_u32(&full_bar[s]), (it / NS) & 1, a.status))) break;
       const ChunkHdr hd = hdr[s];
+      if (hd.count < 0) break;                   // the producer has no more chunks
       const int head = hd.hg;
       if (hd.b != cur_b || head != cur_h) {
         if (cur_b >= 0) meet();                  // every consumer is done with the old table
@@ -312,10 +309,11 @@ __global__ void __launch_bounds__(kScThreads, kCtasPerSm) score_kernel(ScoreArgs
   const int hl = grp & (Hc - 1);
   float ca[8], cp[8], cn[8];
   int cur_b = -1, cur_h = -1;
-  for (int ci = c_begin, it = 0; ci < c_end; ++ci, ++it) {
+  for (int it = 0;; ++it) {
     const int s = it % NS;
-    if (!mbar_wait(smem_u32(&full_bar[s]), (it / NS) & 1, a.status)) break;
+    if (!__all_sync(kFull, mbar_wait(smem_u32(&full_bar[s]), (it / NS) & 1, a.status))) break;
     const ChunkHdr hd = hdr[s];
+    if (hd.count < 0) break;                     // the producer has no more chunks
     const int head = (hd.hg << hcs) + hl;
     if (hd.b != cur_b || head != cur_h) {
       cur_b = hd.b;
@@ -544,10 +542,13 @@ sa_status sa::score_impl(const sa_cache* cache, const sa_batch* batch, const voi
   int hc = 1;
   while (!per_query_head && hc < groups && a.H_kv % (2 * hc) == 0) hc *= 2;
   a.hc_shift = log2i(hc);
-  // enough persistent CTAs for two per SM, never more than chunks could exist
+  // the chunk space over the table rows; enough persistent CTAs for two per
+  // SM, never more than chunks exist
   const int cap = max_pages < batch->bt_stride ? max_pages : batch->bt_stride;
   const int per_chunk = kChunk / hc;
-  const int64_t max_chunks = int64_t(batch->batch) * (a.H_kv / hc) * ((cap + per_chunk - 1) / per_chunk);
+  a.cpr = (cap + per_chunk - 1) / per_chunk;
+  const int64_t max_chunks = int64_t(batch->batch) * (a.H_kv / hc) * a.cpr;
+  if (max_chunks > 0x7fffffff - 4 * 1024 * 1024) return SA_ERR_UNSUPPORTED;
   const int full = kCtasPerSm * sm_count();
   const int grid = int(max_chunks < full ? max_chunks : full);
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -121,3 +121,47 @@ def test_sharded_step_with_an_empty_request_and_empty_shards():
         assert torch.allclose(lse_s[b][ok], dec.lse[b][ok], atol=1e-3)
         assert torch.allclose(out_s[b].float(), dec.out[b].float(), atol=2e-2, rtol=2e-2)
     assert dev_status(dec) == 0
+
+
+def test_kv_head_partition_reproduces_the_whole_step():
+    """KV-head partitioning has no exchange: a decoder holding only KV heads
+    [h0, h1) -- their pool and statistics slices, their G query heads each --
+    reproduces the whole decoder's scores, selection, output and lse rows for
+    those heads bit for bit (the same per-(page, head) arithmetic, and here the
+    same split count per unit)."""
+    from sparse_paged_kv_page_gb300.shard import kv_head_range, kv_head_slice, query_head_slice
+    from sparse_paged_kv_page_gb300.step import SparseDecoder
+    wl = make_workload(config(5, small=True))
+    c = wl.cfg
+    dec = make_decoder(wl)
+    q = dev_bits(wl.q(0), c.dtype)
+    dec.step(q)
+    torch.cuda.synchronize()
+    lens = dec.seq_lens.cpu().numpy()
+    for r in range(2):
+        h0, h1 = kv_head_range(c.H_kv, 2, r)
+        part = SparseDecoder(batch=c.B, num_q_heads=(h1 - h0) * c.G, num_kv_heads=h1 - h0,
+                             head_dim=c.D, page_size=c.ps, num_blocks=wl.num_blocks,
+                             bt_stride=wl.max_pages, dtype=dec.dtype, scale=c.scale, topk=c.topk,
+                             w_avg=c.w_avg, w_peak=c.w_peak)
+        part.cache.k.copy_(kv_head_slice(dec.cache.k, h0, h1))
+        part.cache.v.copy_(kv_head_slice(dec.cache.v, h0, h1))
+        part.cache.meta.copy_(kv_head_slice(dec.cache.meta, h0, h1))
+        part.set_block_table(torch.from_numpy(wl.block_table))
+        part.seq_lens.copy_(dec.seq_lens)
+        part.step(query_head_slice(q, h0, h1, c.G))
+        torch.cuda.synchronize()
+        rows = slice(h0 * c.G, h1 * c.G)
+        for b in range(c.B):
+            n = O.num_pages(int(lens[b]), c.ps)
+            assert torch.equal(part.scores[b, :, :n].view(torch.int32),
+                               dec.scores[b, h0:h1, :n].view(torch.int32))
+        assert torch.equal(part.sel_cnt, dec.sel_cnt[:, h0:h1])
+        for b in range(c.B):
+            for hh in range(h1 - h0):
+                k = int(part.sel_cnt[b, hh])
+                assert torch.equal(part.sel_idx[b, hh, :k], dec.sel_idx[b, h0 + hh, :k])
+        assert torch.equal(part.out.view(torch.int16), dec.out[:, rows].view(torch.int16))
+        assert torch.equal(part.lse.view(torch.int32), dec.lse[:, rows].view(torch.int32))
+        assert dev_status(part) == 0
+    assert dev_status(dec) == 0
