@@ -30,6 +30,7 @@ namespace {
 constexpr int kSelThreads = SA_SELECT_THREADS;
 constexpr int kBpt = 4096 / kSelThreads;   // histogram bins owned per thread in the digit search
 constexpr int kWarps = kSelThreads / 32;
+constexpr int kFirst = 9;                  // candidates a thread loads with the length
 static_assert(kSelThreads == 1024, "the digit search maps 4096 bins and 32 warps onto the block");
 constexpr int kSelMaxPages = 45056;      // keys in shared memory next to two 16 KB histograms
 
@@ -53,14 +54,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   const int unit = b * a.H + h;
   pdl_wait();                                  // scores and lengths of this step are final
   pdl_trigger();                               // the decode may start its prologue
-  // Candidate i is page n_bos + i. The first 8 * kSelThreads candidates'
-  // scores are loaded together with the length (the row holds max_pages
-  // entries; entries past the length are ignored).
+  // Candidate i is page n_bos + i. The first kFirst * kSelThreads
+  // candidates' scores are loaded together with the length (the row holds
+  // max_pages entries; entries past the length are ignored): 9 a thread, so
+  // the 8193 candidates of a 131072-token request need one round trip.
   const int bos = a.n_bos, eos = a.n_eos;
   const float* sc = a.scores + int64_t(unit) * a.max_pages + bos;
-  float v0[8];
+  float v0[kFirst];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
+  for (int u = 0; u < kFirst; ++u) {
     const int i = u * kSelThreads + tid;
     v0[u] = bos + i < a.max_pages ? sc[i] : 0.f;
   }
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
   __syncthreads();
   // keys to shared memory; the first digit's histogram straight from registers
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
+  for (int u = 0; u < kFirst; ++u) {
     const int i = u * kSelThreads + tid;
     if (i < nc) {
       const uint32_t k = f32_key(v0[u]);
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
       atomicAdd(&hist[0][k >> 20], 1);
     }
   }
-  for (int i0 = 8 * kSelThreads; i0 < nc; i0 += 8 * kSelThreads) {   // long rows
+  for (int i0 = kFirst * kSelThreads; i0 < nc; i0 += 8 * kSelThreads) {   // long rows
     float v[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
