@@ -131,6 +131,35 @@ def test_select_bit_exact_on_generated_scores(kind, topk):
             assert np.all(sel[b, h, cnt[b, h]:] == -7)
 
 
+@pytest.mark.parametrize("kind", ["boundary_ties", "narrow", "outlier"])
+@pytest.mark.parametrize("topk", [8, 256])
+def test_select_value_binned_path(kind, topk):
+    """Rows the value-binned fast path handles: exact duplicates of the
+    boundary score scattered over the row (ranked by page index inside the
+    boundary bin), a spread of only ~1e-6, and one huge outlier that squeezes
+    every other score into the lowest bins (then the radix path decides)."""
+    rng = np.random.default_rng([13, topk, len(kind)])
+    B, H, maxp, ps = 2, 3, 9000, 16
+    s = rng.standard_normal((B, H, maxp)).astype(np.float32)
+    if kind == "boundary_ties":
+        for b in range(B):
+            for h in range(H):
+                row = s[b, h, :maxp - 1]
+                kth = np.sort(row)[::-1][topk - 2] if topk > 1 else row.max()
+                row[rng.choice(maxp - 1, size=40, replace=False)] = kth
+    elif kind == "narrow":
+        s = (1.0 + 1e-6 * s).astype(np.float32)
+    else:
+        s[:, :, 17] = 3e38
+    lens = [maxp * ps, (maxp - 333) * ps + 1]
+    sel, cnt, st = _run_select(s, lens, ps, topk, H)
+    assert st == 0
+    for b in range(B):
+        n = O.num_pages(lens[b], ps)
+        for h in range(H):
+            assert np.array_equal(sel[b, h, :cnt[b, h]], O.select_pages(s[b, h], n, topk)), (b, h)
+
+
 @pytest.mark.parametrize("maxp", [2048, 2049, 8192, 9000, 16384, 16385])
 def test_select_row_lengths(maxp):
     """Rows of up to 16 K pages keep their keys in registers (2, 4, 8 or 16 per
