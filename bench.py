@@ -349,7 +349,7 @@ def run_gpu(args, rank, world):
     cfg = rank_config(config(args.config), rank, world)
     append = cfg.decode_steps > 0
     # input schedule: 1 eager step, W warm-up replays, K timed, kernel reps, e2e steps
-    n_in = 1 + args.warmup + args.steps + args.kernel_reps + 2 * args.e2e_steps
+    n_in = 1 + args.warmup + args.steps + args.kernel_reps + args.e2e_steps + max(args.e2e_steps, 16)
     wl = make_workload(cfg, extra_steps=max(0, n_in + 2 - cfg.decode_steps))
     c = wl.cfg
     tdt = torch.bfloat16 if c.dtype == "bf16" else torch.float16
@@ -568,58 +568,84 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         serial_ms = dist_max(statistics.mean(x.elapsed_time(y) for x, y in marks), world, dev)
 
-        # Pipelined, as a serving loop runs: every step still copies its own
-        # inputs in from pinned host memory and its output back, on a copy
-        # stream, double-buffered so step i's copies overlap steps i -+ 1.
-        # Steps run back to back without the L2 flush: a step streams about
-        # twice L2 (the flush changes the device time by ~2%).
-        inbufs = [inbuf, torch.empty_like(inbuf)]
-        outs = [dec.out, torch.empty_like(dec.out)]
-        saved = (dec.q_buf, dec.k_buf, dec.v_buf, dec.out)
-        dec.q_buf = inbufs[1][:nq].view(c.B, c.H_q, c.D)
-        dec.k_buf = inbufs[1][nq:nq + nk].view(c.B, c.H_kv, c.D)
-        dec.v_buf = inbufs[1][nq + nk:].view(c.B, c.H_kv, c.D)
-        dec.out = outs[1]
-        graphs = [graph, dec.capture(append=append)]
-        dec.q_buf, dec.k_buf, dec.v_buf, dec.out = saved
-        torch.cuda.synchronize()
+        # Pipelined, as a serving loop runs: groups of G steps are captured,
+        # with their copies, into one CUDA graph (two graphs alternating). In
+        # a group, step j's inputs are copied in from pinned host slot j on a
+        # copy branch (the copy for step j + 1 overlaps step j), the step runs
+        # on its own input buffer into its own output buffer, and its output
+        # is copied back to pinned slot j on the copy branch while step j + 1
+        # runs. The host refills a graph's pinned input slots with the inputs
+        # of the steps it runs next only after that graph's previous launch
+        # has finished. Steps run back to back without the L2 flush: a step
+        # streams about twice L2 (the flush changes the device time by ~2%).
+        G = 8
+        N = (args.e2e_steps // G) * G
+        if N < 2 * G:
+            N = 2 * G
         copy = torch.cuda.Stream(device=dev)
-        pin_outs = [pin_out, torch.empty_like(pin_out).pin_memory()]
-        N = args.e2e_steps
-        ev = lambda: torch.cuda.Event(enable_timing=True)
-        e_h = [ev() for _ in range(N)]
-        e_r = [ev() for _ in range(N)]
-        e_d = [ev() for _ in range(N)]
-        t0, t1 = ev(), ev()
-        t0.record(copy)
-        with torch.cuda.stream(copy):
-            inbufs[0].view(torch.int16).copy_(pin_in[t_next], non_blocking=True)
-        e_h[0].record(copy)
-        for i in range(N):
-            if i + 1 < N:                                  # the next step's inputs
-                if i >= 1:
-                    copy.wait_event(e_r[i - 1])            # its buffer was read by step i - 1
+        saved_out = dec.out
+        groups = []
+        for gi in range(2):
+            ins = [torch.empty_like(inbuf) for _ in range(G)]
+            outs = [torch.empty_like(dec.out) for _ in range(G)]
+            pins = torch.empty((G, nq + 2 * nk), dtype=torch.int16).pin_memory()
+            pouts = torch.empty((G, c.B, c.H_q, c.D), dtype=torch.int16).pin_memory()
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(device=dev)
+            cap.wait_stream(stream)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=cap):
+                h_ev = [torch.cuda.Event() for _ in range(G)]
+                r_ev = [torch.cuda.Event() for _ in range(G)]
+                copy.wait_stream(cap)
                 with torch.cuda.stream(copy):
-                    inbufs[(i + 1) % 2].view(torch.int16).copy_(pin_in[t_next + i + 1], non_blocking=True)
-                e_h[i + 1].record(copy)
-            stream.wait_event(e_h[i])
-            if i >= 2:
-                stream.wait_event(e_d[i - 2])              # its output buffer was read back
-            graphs[i % 2].replay()
-            e_r[i].record(stream)
-            copy.wait_event(e_r[i])
-            with torch.cuda.stream(copy):
-                pin_outs[i % 2].copy_(outs[i % 2].view(torch.int16), non_blocking=True)
-            e_d[i].record(copy)
-        t1.record(copy)
+                    for j in range(G):
+                        ins[j].view(torch.int16).copy_(pins[j], non_blocking=True)
+                        h_ev[j].record(copy)
+                for j in range(G):
+                    cap.wait_event(h_ev[j])
+                    dec.out = outs[j]
+                    dec.step(ins[j][:nq].view(c.B, c.H_q, c.D),
+                             ins[j][nq:nq + nk].view(c.B, c.H_kv, c.D) if append else None,
+                             ins[j][nq + nk:].view(c.B, c.H_kv, c.D) if append else None)
+                    r_ev[j].record(cap)
+                    copy.wait_event(r_ev[j])
+                    with torch.cuda.stream(copy):
+                        pouts[j].copy_(outs[j].view(torch.int16), non_blocking=True)
+                cap.wait_stream(copy)
+            groups.append((g, pins, pouts, ins, outs))
+        dec.out = saved_out
+        torch.cuda.synchronize()
+        done = [None, None]
+
+        def fill(gi, k):                                   # group k's inputs into graph gi's slots
+            groups[gi][1].copy_(pin_in[t_next + k * G:t_next + (k + 1) * G])
+
+        fill(0, 0)
+        fill(1, 1)
+        ev = lambda: torch.cuda.Event(enable_timing=True)
+        t0, t1 = ev(), ev()
+        t0.record(stream)
+        for k in range(N // G):
+            gi = k % 2
+            if k >= 2:
+                done[gi].synchronize()                     # its previous launch has read its slots
+                fill(gi, k)
+            groups[gi][0].replay()
+            done[gi] = torch.cuda.Event()
+            done[gi].record(stream)
+        t1.record(stream)
         torch.cuda.synchronize()
         t_next += N
         em = dist_max(t0.elapsed_time(t1) / N, world, dev)
         e2e = {"value": aggregate_steps_per_s(em, world), "unit": "steps/s",
                "h2d_bytes_per_step": int((nq + 2 * nk if append else nq) * 2),
                "d2h_bytes_per_step": int(c.B * c.H_q * c.D * 2), "ms_per_step": em,
-               "mode": "pipelined: per-step H2D of its inputs and D2H of its output on a copy "
-                       "stream, double-buffered, steps back to back without the L2 flush",
+               "mode": "pipelined: groups of 8 steps captured with their copies into CUDA graphs "
+                       "(two alternating); every step copies its own inputs in from pinned host "
+                       "memory and its output back on a copy branch that overlaps the neighbouring "
+                       "steps; the host refills a graph's pinned input slots after its previous "
+                       "launch; steps back to back without the L2 flush",
                "serial": {"value": aggregate_steps_per_s(serial_ms, world), "ms_per_step": serial_ms,
                           "mode": "one step at a time: L2 flush, H2D, step, D2H inside the events"}}
     status |= int(dec.dev_status.item())
