@@ -46,7 +46,7 @@ namespace {
 #define SA_SCORE_CONSUMER_WARPS 4
 #endif
 #ifndef SA_SCORE_STAGES
-#define SA_SCORE_STAGES 3
+#define SA_SCORE_STAGES 4
 #endif
 #ifndef SA_SCORE_CTAS_PER_SM
 #define SA_SCORE_CTAS_PER_SM 2
