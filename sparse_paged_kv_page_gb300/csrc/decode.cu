@@ -80,6 +80,14 @@ struct DecodeArgs {
 // Byte offset (from the 1024-aligned base) of a CTA's cluster partial, past the
 // warp-merge scratch (<= 4 warps x 16 rows x (D + 4) floats + 512 bytes).
 constexpr int kClusterOff = 36 * 1024;
+// Cluster merge receive area, past the selection entries: every peer's partial
+// of the slice this CTA merges ([nsplit][chunk] floats, nsplit * chunk <=
+// 16 * D + kMaxCluster) and every peer's lse of each row ([kMaxCluster][16]).
+template <int D>
+constexpr int recv_bytes() { return 4 * (16 * D + kMaxCluster + kMaxCluster * 16); }
+__host__ __device__ constexpr int recv_off(int tile_smem, int ent_max) {
+  return (tile_smem + ent_max * 8 + 15) & ~15;
+}
 
 // Shared-memory tile of 16 rows x D columns (2-byte elements): 64-column
 // halves of 16 x 128 bytes, each 16-byte chunk c of row r stored at chunk
@@ -121,6 +129,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   __shared__ float s_rl[16];                   // this CTA's lse of each row
   // 1024-byte aligned base for the swizzled tiles
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  // Cluster merge: peers store into this CTA's receive area only after this
+  // arrive has been waited on, i.e. once every CTA of the cluster has started.
+  const bool push = kCluster && !a.logits_only && a.nsplit > 1;
+  if (push) cluster_arrive_relaxed();
 
   // h: the selection unit within the request -- a KV head with its G query
   // heads, or (per-query-head selection, G = 1) one query head of KV head kvh
@@ -477,27 +489,38 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 
   if constexpr (kCluster) {
-    // The unit's nsplit CTAs form one cluster. Each leaves its partial in its
-    // own shared memory; after a cluster barrier each CTA merges a 1/nsplit
-    // slice of the unit's G*D outputs from every peer's partial over DSMEM; a
-    // second barrier keeps all shared memory alive until every peer is done.
-    float* cl_o = reinterpret_cast<float*>(smem + kClusterOff);   // [G][D]
-    float* cl_lse = cl_o + 16 * D;                                 // [G] natural log
-    for (int idx = threadIdx.x; idx < G * D; idx += kThreads) cl_o[idx] = merged(idx / D, idx % D);
-    if (threadIdx.x < G) cl_lse[threadIdx.x] = s_rl[threadIdx.x];
-    cluster_sync();
+    // The unit's nsplit CTAs form one cluster; CTA r merges the slice
+    // [r * chunk, (r + 1) * chunk) of the unit's G*D outputs. Each CTA stores
+    // its partial of every slice, and its lse of every row, into the owner's
+    // receive area (a region no tile uses, so a peer may store there while
+    // this CTA still streams tiles); one barrier phase (release / acquire)
+    // makes the stores visible, and each owner merges from its own shared
+    // memory, after which no CTA touches another's shared memory again.
     const int ns = a.nsplit;
     const int n_el = G * D, chunk = (n_el + ns - 1) / ns;
-    const int e0 = int(cluster_rank()) * chunk, e1 = min(n_el, e0 + chunk);
-    const uint32_t o_base = smem_u32(cl_o), l_base = smem_u32(cl_lse);
+    const uint32_t me = cluster_rank();
+    float* rv_o = reinterpret_cast<float*>(smem_raw + recv_off(TL::kSmem, a.ent_max));   // [ns][chunk]
+    float* rv_l = rv_o + 16 * D + kMaxCluster;                                          // [ns][16]
+    const uint32_t o_base = smem_u32(rv_o), l_base = smem_u32(rv_l);
+    cluster_wait();                              // every peer has started (the arrive at entry)
+    for (int idx = threadIdx.x; idx < n_el; idx += kThreads) {
+      const int dst = idx / chunk;
+      dsmem_st_f32(dsmem_map(o_base + 4u * (me * uint32_t(chunk) + uint32_t(idx - dst * chunk)), uint32_t(dst)),
+                   merged(idx / D, idx % D));
+    }
+    for (int i = threadIdx.x; i < ns * G; i += kThreads) {
+      const int dst = i / G, row = i - dst * G;
+      dsmem_st_f32(dsmem_map(l_base + 4u * (me * 16u + uint32_t(row)), uint32_t(dst)), s_rl[row]);
+    }
+    cluster_sync();
+    const int e0 = int(me) * chunk, e1 = min(n_el, e0 + chunk);
     for (int idx = e0 + threadIdx.x; idx < e1; idx += kThreads) {
-      const int row = idx / D;
-      // the row's lse and the element from every peer, all loads in flight at once
+      const int row = idx / D, off = idx - e0;
       float lv[kMaxCluster], ov[kMaxCluster];
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r) {
-        lv[r] = r < ns ? dsmem_ld_f32(dsmem_map(l_base + 4u * row, r)) : -INFINITY;
-        ov[r] = r < ns ? dsmem_ld_f32(dsmem_map(o_base + 4u * idx, r)) : 0.f;
+        lv[r] = r < ns ? rv_l[r * 16 + row] : -INFINITY;
+        ov[r] = r < ns ? rv_o[r * chunk + off] : 0.f;
       }
       float M = -INFINITY;
 #pragma unroll
@@ -515,7 +538,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (a.lse && idx % D == 0)
         a.lse[int64_t(b) * a.H_q + int64_t(h) * G + row] = tot > 0.f ? M + lg2_approx(tot) * kLn2 : -INFINITY;
     }
-    cluster_sync();
   } else {
   // ticket merge: partials to the workspace, the last CTA of the unit merges
   for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
@@ -678,7 +700,8 @@ template <typename T, int D, bool kTma, bool kCluster>
 sa_status launch_decode(const DecodeArgs& a, dim3 grid, cudaStream_t s, const CUtensorMap& mk,
                         const CUtensorMap& mv, int* cache, bool pdl) {
   auto k = decode_kernel<T, D, kTma, kCluster>;
-  const int smem = Tile<D>::kSmem + a.ent_max * int(sizeof(int2));
+  const int smem = kCluster ? recv_off(Tile<D>::kSmem, a.ent_max) + recv_bytes<D>()
+                            : Tile<D>::kSmem + a.ent_max * int(sizeof(int2));
   if (!ensure_smem(k, smem, cache)) return SA_ERR_CUDA;
   const cudaError_t e = launch_ex(k, grid, dim3(kThreads), size_t(smem), s, pdl, kCluster ? grid.x : 1u,
                                   a, mk, mv);
