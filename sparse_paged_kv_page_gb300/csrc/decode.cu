@@ -77,9 +77,6 @@ struct DecodeArgs {
   float scale, scale_log2;
 };
 
-// Byte offset (from the 1024-aligned base) of a CTA's cluster partial, past the
-// warp-merge scratch (<= 4 warps x 16 rows x (D + 4) floats + 512 bytes).
-constexpr int kClusterOff = 36 * 1024;
 // Cluster merge receive area, past the selection entries: every peer's partial
 // of the slice this CTA merges ([nsplit][chunk] floats, nsplit * chunk <=
 // 16 * D + kMaxCluster) and every peer's lse of each row ([kMaxCluster][16]).
@@ -102,8 +99,9 @@ struct Tile {
   static constexpr int kOps = 16 / kRowsPerOp;       // cp.async per lane per tile
   static constexpr int kStageBytes = 2 * kBytes;     // K + V
   static constexpr int kStageArea = kWarps * kStages * kStageBytes;
-  // the stage area is reused for the merge scratch and the cluster partial
-  static constexpr int kMergeArea = kClusterOff + 4 * (16 * D + 16);
+  // the stage area is reused for the warp-merge scratch: row maxima and sums
+  // ([kWarps][16] each) and partial outputs ([kWarps][16][D + 4] floats)
+  static constexpr int kMergeArea = 4 * (kWarps * 32 + kWarps * 16 * (D + 4));
   static constexpr int kSmem = (kStageArea > kMergeArea ? kStageArea : kMergeArea) + 1024;   // + alignment slack
 };
 
@@ -119,8 +117,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                   const __grid_constant__ CUtensorMap tmv) {
   using E = Elem<T>;
   using TL = Tile<D>;
-  static_assert(kClusterOff >= 4 * (kWarps * 32 + kWarps * 16 * (D + 4)), "warp-merge scratch overlaps");
-  static_assert(kClusterOff + 4 * (16 * D + 16) <= TL::kSmem - 1024, "cluster partial must fit");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ uint32_t s_mask[kWarps][kStages];
   __shared__ __align__(8) uint64_t s_bar[kWarps][kStages];
