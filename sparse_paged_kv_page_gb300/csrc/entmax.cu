@@ -24,10 +24,10 @@
 //      and loads V rows only for tokens some head of the group keeps
 //      (entmax is sparse), accumulating sum_j p_j v_j and sum_j p_j in fp32;
 //      the splits of a (request, KV head), at most 8, form a thread-block
-//      cluster and add their partials over distributed shared memory in a
-//      fixed order (where a cluster cannot launch, the last CTA adds them
-//      from the workspace), dividing by sum_j p_j (1 up to the rounding of
-//      tau).
+//      cluster: each stores its partials into the shared memory of the CTA
+//      that adds that slice, which adds them in split order (where a cluster
+//      cannot launch, the last CTA adds them from the workspace), dividing
+//      by sum_j p_j (1 up to the rounding of tau).
 #include "common.cuh"
 #include "host.h"
 
@@ -38,6 +38,15 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxClusterSplits = 8;     // splits of a unit merged inside one (portable) cluster
 constexpr int kWarps = kThreads / 32;
+// Dynamic shared memory of the weighted-V kernel: the warps' partials
+// ([kWarps][G][D + 1] floats), the (block, fill) entries, and the cluster
+// merge's receive area (every peer's partial of this CTA's slice,
+// [nsplit][chunk] <= G * D + kMaxClusterSplits floats, and every peer's
+// sum p of each row, [kMaxClusterSplits][16]).
+inline int64_t attend_smem(int G, int D, int ent_cap) {
+  return int64_t(kWarps) * G * (D + 1) * 4 + int64_t(ent_cap) * 8 +
+         (int64_t(G) * D + kMaxClusterSplits + kMaxClusterSplits * 16) * 4;
+}
 constexpr int kCand = 256;               // candidates each warp of the tau kernel gathers (beyond: the row is streamed)
 constexpr int kMaxIter = 100;
 constexpr int kRowReg = 16;              // row entries per thread the tau kernel keeps in registers
@@ -491,6 +500,10 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int G = a.G;
+  // Cluster merge: peers store into this CTA's receive area only after this
+  // arrive has been waited on, i.e. once every CTA of the cluster has started.
+  const bool push = kCluster && a.nsplit > 1;
+  if (push) cluster_arrive_relaxed();
   // the selection and lengths come from before the logits pass: resolve the
   // entries this CTA touches to (block, fill) before waiting for the thresholds
   const int kvh = h / a.kv_div;                           // the unit's KV head
@@ -611,18 +624,20 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
   }
   __syncthreads();
   const int64_t prow = (int64_t(b) * a.H_q + int64_t(h) * G) * a.nsplit;   // (b, head h*G, split 0)
-  for (int idx = tid; idx < G * D; idx += kThreads) {
-    float sum = 0.f;
+  if (!kCluster && a.nsplit > 1) {                         // the ticket merge reads these
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) sum += s_red[w * G * D + idx];
-    const int g = idx / D, d = idx % D;
-    a.part_o[((prow + int64_t(g) * a.nsplit) + split) * D + d] = sum;
-  }
-  if (tid < G) {
-    float sum = 0.f;
+      for (int w = 0; w < kWarps; ++w) sum += s_red[w * G * D + idx];
+      const int g = idx / D, d = idx % D;
+      a.part_o[((prow + int64_t(g) * a.nsplit) + split) * D + d] = sum;
+    }
+    if (tid < G) {
+      float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) sum += s_red[kWarps * G * D + w * G + tid];
-    a.part_l[prow + int64_t(tid) * a.nsplit + split] = sum;
+      for (int w = 0; w < kWarps; ++w) sum += s_red[kWarps * G * D + w * G + tid];
+      a.part_l[prow + int64_t(tid) * a.nsplit + split] = sum;
+    }
   }
   T* outp = static_cast<T*>(a.out) + (int64_t(b) * a.H_q + int64_t(h) * G) * D;
   if (a.nsplit == 1) {                                     // one split: normalise and write
@@ -638,41 +653,48 @@ __global__ void __launch_bounds__(kThreads, 2) entmax_attend_kernel(EntArgs a) {
     return;
   }
   if constexpr (kCluster) {
-    // The unit's splits form one cluster: each leaves its partial (sum p v,
-    // sum p) in its own shared memory; after a cluster barrier each CTA adds
-    // a 1/nsplit slice of the G*D outputs over every peer's partial (DSMEM,
-    // all loads in flight at once); a second barrier keeps the partials alive
-    // until every peer has read them.
-    float* s_cl = reinterpret_cast<float*>(s_ent + a.ent_cap);   // [G][D], then [G]
-    for (int idx = tid; idx < G * D; idx += kThreads) {
+    // The unit's splits form one cluster; CTA r adds the slice
+    // [r * chunk, (r + 1) * chunk) of the G*D outputs. Each CTA stores its
+    // partial of every slice (sum p v), and its sum p of every row, into the
+    // owner's receive area (past the entries; nothing else uses it, so a peer
+    // may store there while this CTA still runs its tokens); one barrier phase
+    // (release / acquire) makes the stores visible and each owner adds the
+    // partials in split order from its own shared memory.
+    const int ns = a.nsplit, n_el = G * D, chunk = (n_el + ns - 1) / ns;
+    const uint32_t me = cluster_rank();
+    float* rv_o = reinterpret_cast<float*>(s_ent + a.ent_cap);   // [ns][chunk]
+    float* rv_l = rv_o + n_el + kMaxClusterSplits;                // [ns][16]
+    const uint32_t o_base = smem_u32(rv_o), l_base = smem_u32(rv_l);
+    cluster_wait();                                        // every peer has started (the arrive at entry)
+    for (int idx = tid; idx < n_el; idx += kThreads) {
       float o = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) o += s_red[w * G * D + idx];
-      s_cl[idx] = o;
+      const int dst = idx / chunk;
+      dsmem_st_f32(dsmem_map(o_base + 4u * (me * uint32_t(chunk) + uint32_t(idx - dst * chunk)), uint32_t(dst)), o);
     }
-    if (tid < G) {
+    for (int i = tid; i < ns * G; i += kThreads) {
+      const int dst = i / G, g = i - dst * G;
       float l = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) l += s_red[kWarps * G * D + w * G + tid];
-      s_cl[G * D + tid] = l;
+      for (int w = 0; w < kWarps; ++w) l += s_red[kWarps * G * D + w * G + g];
+      dsmem_st_f32(dsmem_map(l_base + 4u * (me * 16u + uint32_t(g)), uint32_t(dst)), l);
     }
     cluster_sync();
-    const int ns = a.nsplit, n_el = G * D, chunk = (n_el + ns - 1) / ns;
-    const int e0 = int(cluster_rank()) * chunk, e1 = min(n_el, e0 + chunk);
-    const uint32_t base = smem_u32(s_cl);
+    const int e0 = int(me) * chunk, e1 = min(n_el, e0 + chunk);
     for (int idx = e0 + tid; idx < e1; idx += kThreads) {
+      const int off = idx - e0, row = idx / D;
       float ov[kMaxClusterSplits], lv[kMaxClusterSplits];
 #pragma unroll
       for (int r = 0; r < kMaxClusterSplits; ++r) {
-        ov[r] = r < ns ? dsmem_ld_f32(dsmem_map(base + 4u * idx, r)) : 0.f;
-        lv[r] = r < ns ? dsmem_ld_f32(dsmem_map(base + 4u * (n_el + idx / D), r)) : 0.f;
+        ov[r] = r < ns ? rv_o[r * chunk + off] : 0.f;
+        lv[r] = r < ns ? rv_l[r * 16 + row] : 0.f;
       }
       float o = 0.f, l = 0.f;
 #pragma unroll
       for (int r = 0; r < kMaxClusterSplits; ++r) { o += ov[r]; l += lv[r]; }   // split order
       reinterpret_cast<uint16_t*>(outp)[idx] = E::from_f(l > 0.f ? o / l : 0.f);
     }
-    cluster_sync();
     return;
   }
   // the last split of this (request, KV head) adds the partials in split order
@@ -740,8 +762,9 @@ int g_att_smem[16][128];                  // [variant][device] ticket kernels, [
 
 template <typename T, int D, int kG>
 sa_status launch_attend(const EntArgs& a, dim3 grid, cudaStream_t s, int* attr) {
-  const int smem = (kWarps + 1) * a.G * (D + 1) * int(sizeof(float)) + a.ent_cap * int(sizeof(int2));
-  if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  const int64_t smem64 = attend_smem(a.G, D, a.ent_cap);
+  if (smem64 > 227 * 1024) return SA_ERR_UNSUPPORTED;
+  const int smem = int(smem64);
   if (a.nsplit > 1) {                                      // the cluster merge where it can launch
     auto kc = entmax_attend_kernel<T, D, kG, true>;
     if (ensure_smem(kc, smem, attr + 64) &&
@@ -804,8 +827,7 @@ sa_status entmax_impl(const sa_cache* cache, const sa_batch* batch, const void* 
   const EntLayout w = ent_layout(batch->batch, H_u, num_q_heads, cache->head_dim, cache->page_size,
                                  sel_stride, sm_count());
   if (!workspace || workspace_bytes < w.total) return SA_ERR_WORKSPACE;
-  const int64_t smem = int64_t(kWarps + 1) * G * (cache->head_dim + 1) * 4 + int64_t(w.ent_cap) * 8;
-  if (smem > 227 * 1024) return SA_ERR_UNSUPPORTED;       // (checked before any launch)
+  if (attend_smem(G, cache->head_dim, w.ent_cap) > 227 * 1024) return SA_ERR_UNSUPPORTED;   // (checked before any launch)
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* lg = logits ? logits : reinterpret_cast<float*>(ws + w.logits);
   const int lg_stride = logits ? logits_stride : int(rows);
