@@ -130,6 +130,26 @@ def test_decode_split_counts(B, topk):
     _check(dec, wl, qb, sel, cnt, out, lse)
 
 
+@pytest.mark.parametrize("topk", [2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("G,D,dtype", [(8, 128, "bf16"), (3, 64, "fp16"), (16, 128, "bf16")])
+def test_decode_every_cluster_size(topk, G, D, dtype):
+    # One request with two KV heads, a selection of topk pages of 16 tokens
+    # (one tile each): the split count is min(8, topk) on any GPU of 8 or more
+    # SMs, so every cluster size of the split merge runs, with output slices
+    # of G * D that do not always divide evenly, and some units selecting
+    # fewer pages than splits (empty partials)
+    cfg = config(5, small=True).replace(B=1, H_q=2 * G, H_kv=2, D=D, dtype=dtype,
+                                        prefill=(1500,), topk=topk, num_blocks=None)
+    wl = make_workload(cfg)
+    dec = make_decoder(wl)
+    rng = np.random.default_rng([topk, G, D])
+    sel, cnt = _random_selection(wl, rng, topk)
+    qb = wl.q(0)
+    out, lse, _ = _decode(dec, dev_bits(qb, dtype), sel, cnt, topk)
+    _check(dec, wl, qb, sel, cnt, out, lse)
+    assert dev_status(dec) == 0
+
+
 def test_empty_and_zero_length():
     cfg = config(3, small=True).replace(B=3, len_range=(1, 50))
     wl = make_workload(cfg)

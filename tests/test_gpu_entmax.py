@@ -130,6 +130,26 @@ def test_entmax_group_sizes(D, G, dtype):
     assert dev_status(dec) == 0
 
 
+@pytest.mark.parametrize("splits", [2, 3, 5, 6, 7, 8])
+@pytest.mark.parametrize("G,D,dtype", [(8, 128, "bf16"), (3, 64, "fp16")])
+def test_entmax_every_cluster_size(splits, G, D, dtype):
+    # One request with two KV heads and a selection of 8 * splits pages of 16
+    # tokens: the weighted-V pass takes min(8, tokens / 128) = splits splits
+    # on any GPU of 8 or more SMs, so every cluster size of its merge runs
+    k = 8 * splits
+    cfg = config(5, small=True).replace(B=1, H_q=2 * G, H_kv=2, D=D, dtype=dtype,
+                                        prefill=(1500,), topk=k, num_blocks=None)
+    wl = make_workload(cfg)
+    dec = make_decoder(wl)
+    c = wl.cfg
+    rng = np.random.default_rng([splits, G, D])
+    sel, cnt = _selection(wl, rng, k)
+    qb = wl.q(0)
+    out, tau, lg = _run(dec, dev_bits(qb, c.dtype), sel, cnt, k, 1.5)
+    _check(wl, qb, sel, cnt, out, tau, lg, 1.5, _scale(c))
+    assert dev_status(dec) == 0
+
+
 def test_nan_stale_slots_are_never_read():
     wl = make_workload(config(2, small=True))
     dec = make_decoder(wl, stale="nan")
