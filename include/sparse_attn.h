@@ -79,7 +79,7 @@ extern "C" {
 typedef enum sa_status {
   SA_OK = 0,
   SA_ERR_INVALID_ARG = 1,   /* a null required pointer, a bad size or a broken constraint */
-  SA_ERR_UNSUPPORTED = 2,   /* a valid configuration this build does not implement */
+  SA_ERR_UNSUPPORTED = 2,   /* a valid configuration the library does not implement */
   SA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than sa_decode_workspace_size() */
   SA_ERR_CUDA = 4           /* a CUDA launch or runtime call failed */
 } sa_status;
