@@ -119,7 +119,7 @@ def gather_rows(pool_bits, block_table_row, positions, h: int, ps: int) -> np.nd
     """Rows of KV head h at logical positions, read from a paged pool through the
     block table: position j lives in physical block bt[j // ps], slot j % ps.
 
-    pool_bits: uint16 [num_blocks, H_kv, ps, D] (one contiguous (block, head) tile).
+    pool_bits: uint16 [num_blocks, H_kv, ps, D]: each (block, head) a contiguous ps x D tile.
     [entmax] "How it works": pages in a block-table paged layout.
     """
     positions = np.asarray(positions, dtype=np.int64)
