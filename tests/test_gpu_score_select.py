@@ -133,11 +133,12 @@ def test_select_bit_exact_on_generated_scores(kind, topk):
 
 @pytest.mark.parametrize("kind", ["boundary_ties", "narrow", "outlier"])
 @pytest.mark.parametrize("topk", [8, 256])
-def test_select_value_binned_path(kind, topk):
-    """Rows the value-binned fast path handles: exact duplicates of the
-    boundary score scattered over the row (ranked by page index inside the
-    boundary bin), a spread of only ~1e-6, and one huge outlier that squeezes
-    every other score into the lowest bins (then the radix path decides)."""
+def test_select_adversarial_rows(kind, topk):
+    """Rows that stress the radix select's digits: exact duplicates of the
+    boundary score scattered over the row (the kept ones are the lowest page
+    indices among them), a spread of only ~1e-6 (keys that differ in their
+    low mantissa bits alone, so every digit is needed), and one huge outlier
+    (the first digit puts it alone above all other keys)."""
     rng = np.random.default_rng([13, topk, len(kind)])
     B, H, maxp, ps = 2, 3, 9000, 16
     s = rng.standard_normal((B, H, maxp)).astype(np.float32)
